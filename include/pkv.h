@@ -1,0 +1,255 @@
+/*
+ * pkv.h -- C ABI of pkv: single-token grouped-query decode attention over a
+ * block-table paged KV cache, hand-written CUDA for GB300 (sm_103a).
+ *
+ * The operation is the one "PersistentKV: Page-Aware Decode Scheduling for
+ * Long-Context LLM Serving on Commodity GPUs" (gist.science summary) states in
+ * its Technical Summary:
+ *   - Problem Statement: decode attention is bound by KV-cache movement;
+ *   - Methodology section 1 "Native Block-Table Decode Engine": G = Hq/Hkv query
+ *     heads share one KV head; attention runs directly over the paged layout
+ *     through the block table ("Layout"); the sequence is cut into disjoint
+ *     splits whose partial softmax states a merge combines exactly ("Sequence
+ *     Splitting"); split ranges follow each row's true length and empty splits
+ *     write neutral states ("Row-Local Bounds"); only non-empty
+ *     (row, KV head, split) tiles are emitted ("Compact Workqueue");
+ *   - Methodology section 2 "Calibrated Adaptive Policy": the route (split,
+ *     queue, or a single-pass kernel) is chosen from the batch size and the
+ *     longest context.
+ * The persistent mode drains the work queue with an atomic counter, as the
+ * persistent worker of "GPUOS" (arXiv 2604.17861, section 4.1 "Persistent
+ * Kernel Executor") and the resident kernel of "WPK persistent kernel"
+ * (dotwave.ai, "What a persistent kernel is") do with their task lists.
+ *
+ * Definition computed, for row b < B, query head h < Hq, kvh = floor(h / G):
+ *     s_t = (1/sqrt(D)) * <q[b][h], K[kvh] of token t>     for t < seq_lens[b]
+ *     out[b][h] = sum_t softmax(s)_t * V[kvh] of token t
+ *     lse[b][h] = ln sum_t exp(s_t)             (natural log; -inf for an empty row)
+ * Token t of row b lives in page block_table[b][t / page_size], slot
+ * t % page_size.  An empty row gives out = 0, lse = -inf.
+ *
+ * Layouts (all row-major, dense, device memory unless stated):
+ *   q            bf16  [B][Hq][D]
+ *   k_pages      bf16  [num_pages][page_size][Hkv][D]   (v_pages the same)
+ *   block_table  int32 [B][max_pages_per_seq]
+ *   seq_lens     int32 [B]
+ *   out          fp32  [B][Hq][D]
+ *   lse          fp32  [B][Hq]
+ * Supported shapes: D in {64, 128}; G in {1, 2, 4, 8}; page_size a multiple of
+ * 16 up to 256.  Every device pointer must be 16-byte aligned.
+ *
+ * Ownership: the caller owns every tensor.  The library owns the plan (host
+ * queue in pinned memory, device queue, split workspace, counters, status
+ * word) and the page pool.  Nothing else is allocated per call.
+ *
+ * Errors: every call returns a pkv_status_code.  No call aborts, and device
+ * code never traps: a bad page id, a plan that does not match the device
+ * lengths, or a wait that runs out sets a bit in the plan's device status word
+ * (read with pkv_status) and poisons the affected outputs with NaN.
+ *
+ * Streams: pkv_stream_t is the same type as cudaStream_t; NULL is the legacy
+ * default stream.  Calls that take a stream only enqueue work on it.
+ */
+#ifndef PKV_H
+#define PKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *pkv_stream_t;
+
+/* Return codes. */
+enum pkv_status_code {
+    PKV_OK = 0,
+    PKV_EINVAL = 1,         /* bad argument: geometry, length, page id, null pointer */
+    PKV_ENOMEM = 2,         /* host or device allocation failed */
+    PKV_ECUDA = 3,          /* a CUDA runtime call failed (see pkv_last_cuda_error) */
+    PKV_EUNSUPPORTED = 4,   /* shape the kernels are not built for */
+    PKV_EDEVICE = 5,        /* the device status word is non-zero (pkv_status) */
+    PKV_ENOSPACE = 6        /* page pool exhausted / row table full */
+};
+
+/* Bits of the device status word. */
+enum pkv_device_status_bits {
+    PKV_DEV_PAGE_OOB = 1u,       /* a block-table entry outside [0, num_pages) */
+    PKV_DEV_PLAN_MISMATCH = 2u,  /* the device seq_lens disagree with the plan */
+    PKV_DEV_TIMEOUT = 4u,        /* a bounded wait inside a kernel ran out */
+    PKV_DEV_ROW_FULL = 8u        /* pkv_append found no page slot for a row */
+};
+
+/* Execution routes (Methodology section 2 of the PersistentKV summary). */
+enum pkv_mode {
+    PKV_MODE_AUTO = 0,          /* let the policy choose */
+    PKV_MODE_DIRECT = 1,        /* one CTA per (row, KV head); no split, no merge */
+    PKV_MODE_SPLIT_QUEUE = 2,   /* partial kernel over the compact queue + merge kernel */
+    PKV_MODE_SPLIT_PADDED = 3,  /* partial kernel over the padded B*Hkv*S_max grid + merge */
+    PKV_MODE_PERSISTENT = 4     /* SM-sized grid drains the compact queue; fused merge */
+};
+
+typedef struct {
+    int32_t batch;              /* B */
+    int32_t num_q_heads;        /* Hq */
+    int32_t num_kv_heads;       /* Hkv; Hq % Hkv == 0 */
+    int32_t head_dim;           /* D */
+    int32_t max_pages_per_seq;  /* row stride of block_table */
+    int32_t num_pages;          /* pages in the pool */
+} pkv_geom;
+
+/* Planner options.  Zero means "default" for every field, so a zeroed struct
+ * (or a NULL pointer) gives the calibrated policy. */
+typedef struct {
+    int32_t force_mode;          /* pkv_mode; PKV_MODE_AUTO lets the policy choose */
+    int32_t num_splits;          /* > 0: split count S, chunk C = ceil(P_max / S) pages */
+    int32_t direct_units_per_sm; /* policy: DIRECT when B*Hkv >= this * SMs (default 2) */
+    int32_t target_ctas_per_sm;  /* policy: aim for this many tiles per SM (default 2) */
+    int32_t min_chunk_pages;     /* policy: smallest split chunk in pages (default 8) */
+    int32_t ctas_per_sm;         /* persistent grid = SMs * this (default: occupancy) */
+    int32_t separate_merge;      /* persistent: 1 = merge in its own launch, 0 = fused */
+    int32_t num_sms;             /* SM count to plan for (default: current device) */
+} pkv_plan_opts;
+
+/* One work tile: KV head `kvh` of row `b`, split `split`, pages
+ * [page_begin, page_end) of the row (end exclusive). 20 bytes. */
+typedef struct {
+    int32_t b, kvh, split, page_begin, page_end;
+} pkv_work_item;
+
+typedef struct {
+    int32_t mode;               /* resolved pkv_mode */
+    int32_t chunk_pages;        /* C */
+    int32_t max_splits;         /* S_max = ceil(P_max / C) */
+    int32_t num_tiles;          /* tiles the attention launch covers */
+    int32_t num_work_items;     /* length of the compact queue */
+    int32_t empty_tiles;        /* padded-grid slots with no pages */
+    int32_t launches_per_step;  /* kernels pkv_decode launches */
+    int32_t grid_ctas;          /* CTAs of the attention launch */
+    int32_t num_sms;            /* SM count planned for */
+    int32_t reserved;
+    int64_t kv_bytes;           /* sum_b N_b * Hkv * D * 2 (K and V) * 2 B */
+    int64_t workspace_bytes;    /* split partial states written + read per step */
+    int64_t table_bytes;        /* block-table entries read per step */
+} pkv_plan_info;
+
+typedef struct pkv_plan_s *pkv_plan_t;
+typedef struct pkv_pool_s *pkv_pool_t;
+
+/*
+ * Build a plan: validate the problem, run the policy, enumerate the work tiles
+ * in lexicographic (b, kvh, split) order and size the split workspace.
+ *   seq_lens_h     host int32 [B]; 0 <= N_b <= max_pages_per_seq * page_size
+ *   block_table_h  host int32 [B][max_pages_per_seq] or NULL; when given, the
+ *                  first ceil(N_b / page_size) entries of every row are checked
+ *                  to lie in [0, num_pages)
+ *   page_size      tokens per page
+ *   opts           NULL for defaults
+ * Binds to the current CUDA device.  On success *plan owns device memory until
+ * pkv_plan_destroy.  The queue reaches the device inside the next pkv_decode,
+ * on that call's stream.  Errors: PKV_EINVAL, PKV_EUNSUPPORTED, PKV_ENOMEM,
+ * PKV_ECUDA; *plan is left NULL on error.
+ */
+int pkv_plan(const int32_t *seq_lens_h, const int32_t *block_table_h, int32_t page_size,
+             const pkv_geom *geom, const pkv_plan_opts *opts, pkv_plan_t *plan);
+
+/* The planner alone, on the host: validation, policy and tile enumeration with
+ * no device touched.  opts->num_sms must be set (> 0); the persistent grid uses
+ * opts->ctas_per_sm (default 1).  Fills *info (nullable), copies up to
+ * `capacity` tiles (as pkv_plan_queue would) and sets *count. */
+int pkv_plan_dry_run(const int32_t *seq_lens_h, const int32_t *block_table_h, int32_t page_size,
+                     const pkv_geom *geom, const pkv_plan_opts *opts, pkv_plan_info *info,
+                     pkv_work_item *items, int32_t capacity, int32_t *count);
+
+/* Re-plan for new lengths (same geometry, page size and options), reusing the
+ * plan's buffers; they grow only when the new tile count needs more room.
+ * Waits for the previous upload of the queue to finish before rewriting it. */
+int pkv_plan_update(pkv_plan_t plan, const int32_t *seq_lens_h, const int32_t *block_table_h);
+
+void pkv_plan_destroy(pkv_plan_t plan);
+
+int pkv_plan_get_info(pkv_plan_t plan, pkv_plan_info *info);
+
+/* Copy the plan's tiles to host memory: the compact queue (SPLIT_QUEUE,
+ * PERSISTENT), the padded grid with its empty slots (SPLIT_PADDED), or one tile
+ * per (row, KV head) (DIRECT).  *count receives the total; at most `capacity`
+ * items are written. */
+int pkv_plan_queue(pkv_plan_t plan, pkv_work_item *items, int32_t capacity, int32_t *count);
+
+/*
+ * Decode attention for every (row, query head); see the definition above.
+ *   q, k_pages, v_pages   device bf16 (as uint16 bit patterns or __nv_bfloat16)
+ *   block_table_d         device int32 [B][max_pages_per_seq]
+ *   seq_lens_d            device int32 [B]; must equal the lengths the plan was built from
+ *   out, lse              device fp32 outputs
+ * Enqueues 1 or 2 kernels (pkv_plan_info.launches_per_step) on `stream`.
+ * Errors: PKV_EINVAL (null pointer, misalignment), PKV_ECUDA (launch failure).
+ * Device-side faults are reported through pkv_status.
+ */
+int pkv_decode(const void *q, const void *k_pages, const void *v_pages,
+               const int32_t *block_table_d, const int32_t *seq_lens_d, pkv_plan_t plan,
+               float *out, float *lse, pkv_stream_t stream);
+
+/*
+ * Append one new token per row: for every row b and KV head, write
+ * k_new[b][kvh][:] / v_new[b][kvh][:] (device bf16 [B][Hkv][D]) at position
+ * seq_lens_d[b] -- page block_table_d[b][pos / page_size], slot
+ * pos % page_size -- and then increment seq_lens_d[b].  The page for a new
+ * position must already be in the table (see pkv_pool_reserve).  A row with no
+ * valid page sets PKV_DEV_ROW_FULL or PKV_DEV_PAGE_OOB and is left unchanged.
+ * Only the plan's geometry and page size are used.  One kernel on `stream`.
+ */
+int pkv_append(const void *k_new, const void *v_new, void *k_pages, void *v_pages,
+               const int32_t *block_table_d, int32_t *seq_lens_d, pkv_plan_t plan,
+               pkv_stream_t stream);
+
+/* Read and clear the plan's device status word (synchronises `stream`). */
+int pkv_status(pkv_plan_t plan, pkv_stream_t stream, uint32_t *status);
+
+/*
+ * Copy the split workspace of the last pkv_decode to host memory (synchronises
+ * `stream`): o_h fp32 [n][G][D] normalised partial outputs and lse_h fp32 [n][G]
+ * natural-log partial LSEs, one entry per tile in pkv_plan_queue order (SPLIT_*
+ * and PERSISTENT modes).  Entries of rows that needed no merge are not written
+ * by the kernels and hold stale data.  For tests and diagnostics.
+ */
+int pkv_read_workspace(pkv_plan_t plan, pkv_stream_t stream, float *o_h, float *lse_h,
+                       int32_t capacity, int32_t *count);
+
+/* Per-launch timing.  While enabled, pkv_decode brackets each kernel it
+ * launches with CUDA events; pkv_profile_read waits for them and returns the
+ * durations in milliseconds of the last pkv_decode's launches, in launch order. */
+int pkv_profile_enable(pkv_plan_t plan, int32_t enable);
+int pkv_profile_read(pkv_plan_t plan, float *ms, int32_t capacity, int32_t *count);
+
+/*
+ * Host page pool: a FIFO free list of page ids, for callers that grow rows one
+ * token at a time (the continuous-session workload).
+ *   pkv_pool_create     copies `count` free page ids, handed out in that order
+ *   pkv_pool_reserve    for every row whose next token (position seq_lens_h[b])
+ *                       starts a new page whose table entry is still unassigned
+ *                       (negative), pops a page into
+ *                       block_table_h[b][seq_lens_h[b] / page_size]; writes the
+ *                       rows it touched to rows_out (nullable, capacity B) and
+ *                       their number to *n_rows.  PKV_ENOSPACE when the pool or
+ *                       a row's table runs out (no row is changed then).
+ *   pkv_pool_release    returns pages to the back of the free list
+ */
+int pkv_pool_create(const int32_t *free_pages, int32_t count, int32_t num_pages, pkv_pool_t *pool);
+int pkv_pool_reserve(pkv_pool_t pool, const int32_t *seq_lens_h, int32_t *block_table_h,
+                     int32_t batch, int32_t max_pages_per_seq, int32_t page_size,
+                     int32_t *rows_out, int32_t *n_rows);
+int pkv_pool_release(pkv_pool_t pool, const int32_t *pages, int32_t count);
+int32_t pkv_pool_free_count(pkv_pool_t pool);
+void pkv_pool_destroy(pkv_pool_t pool);
+
+const char *pkv_strerror(int code);
+/* The CUDA error code behind the last PKV_ECUDA on this thread (0 if none). */
+int pkv_last_cuda_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PKV_H */

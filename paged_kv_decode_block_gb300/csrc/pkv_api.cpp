@@ -1,0 +1,692 @@
+// pkv_api.cpp -- host side of pkv: validation, the adaptive policy, the work
+// planner, plan memory, kernel launches and the page pool, behind the C ABI
+// declared in include/pkv.h.
+//
+// Planner and policy follow "PersistentKV: Page-Aware Decode Scheduling for
+// Long-Context LLM Serving on Commodity GPUs" (gist.science summary),
+// Technical Summary:
+//   * Methodology section 1 "Row-Local Bounds" / "Compact Workqueue": split
+//     ranges come from each row's true length; the queue lists only non-empty
+//     (row, KV head, split) tiles;
+//   * Methodology section 2 "Calibrated Adaptive Policy": the route is chosen
+//     from the batch and the longest context.  Its thresholds were fitted to a
+//     28-SM GPU; here they are restated in SM units: a batch whose B * Hkv
+//     (row, KV head) units already fill `direct_units_per_sm` CTAs per SM runs
+//     the single-pass DIRECT kernel (the summary's high-batch route), anything
+//     smaller is split so that the tiles fill `target_ctas_per_sm` CTAs per SM.
+// Split rule (the summary states none exactly): boundaries on pages, one chunk
+// of C pages per plan, row b gets S_b = ceil(P_b / C) splits, split s covers
+// pages [s*C, min((s+1)*C, P_b)); a requested split count S gives
+// C = ceil(P_max / S).  Queue order is lexicographic in (b, kvh, s).
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+#include <algorithm>
+#include <deque>
+#include <mutex>
+#include <new>
+#include <vector>
+
+#include "pkv.h"
+#include "pkv_internal.h"
+
+namespace {
+
+thread_local int g_last_cuda_error = 0;
+
+int cuda_fail(cudaError_t e) {
+    g_last_cuda_error = static_cast<int>(e);
+    return PKV_ECUDA;
+}
+
+#define PKV_CUDA(call)                                 \
+    do {                                               \
+        cudaError_t e_ = (call);                       \
+        if (e_ != cudaSuccess) return cuda_fail(e_);   \
+    } while (0)
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+struct Options {
+    int force_mode = PKV_MODE_AUTO;
+    int num_splits = 0;
+    int direct_units_per_sm = 2;
+    int target_ctas_per_sm = 2;
+    int min_chunk_pages = 8;
+    int ctas_per_sm = 0;
+    int separate_merge = 0;
+    int num_sms = 0;
+};
+
+int resolve_options(const pkv_plan_opts* o, Options* r) {
+    if (!o) return PKV_OK;
+    if (o->force_mode < PKV_MODE_AUTO || o->force_mode > PKV_MODE_PERSISTENT) return PKV_EINVAL;
+    if (o->num_splits < 0 || o->direct_units_per_sm < 0 || o->target_ctas_per_sm < 0 ||
+        o->min_chunk_pages < 0 || o->ctas_per_sm < 0 || o->num_sms < 0 || o->separate_merge < 0 ||
+        o->separate_merge > 1)
+        return PKV_EINVAL;
+    r->force_mode = o->force_mode;
+    r->num_splits = o->num_splits;
+    if (o->direct_units_per_sm) r->direct_units_per_sm = o->direct_units_per_sm;
+    if (o->target_ctas_per_sm) r->target_ctas_per_sm = o->target_ctas_per_sm;
+    if (o->min_chunk_pages) r->min_chunk_pages = o->min_chunk_pages;
+    r->ctas_per_sm = o->ctas_per_sm;
+    r->separate_merge = o->separate_merge;
+    r->num_sms = o->num_sms;
+    return PKV_OK;
+}
+
+int validate_geometry(const pkv_geom* g, int32_t page_size) {
+    if (!g) return PKV_EINVAL;
+    if (g->batch < 0 || g->num_q_heads <= 0 || g->num_kv_heads <= 0 || g->head_dim <= 0 ||
+        g->max_pages_per_seq <= 0 || g->num_pages <= 0 || page_size <= 0)
+        return PKV_EINVAL;
+    if (g->num_q_heads % g->num_kv_heads != 0) return PKV_EINVAL;
+    if (static_cast<int64_t>(g->num_pages) * page_size > INT32_MAX) return PKV_EINVAL;
+    if (static_cast<int64_t>(g->max_pages_per_seq) * page_size > INT32_MAX) return PKV_EINVAL;
+    if (page_size % pkv::kBlockRows != 0 || page_size > 256) return PKV_EUNSUPPORTED;
+    if (!pkv::shape_supported(g->head_dim, g->num_q_heads / g->num_kv_heads)) return PKV_EUNSUPPORTED;
+    return PKV_OK;
+}
+
+int validate_rows(const pkv_geom& g, int32_t page_size, const int32_t* lens, const int32_t* table) {
+    if (g.batch > 0 && !lens) return PKV_EINVAL;
+    const int64_t cap = static_cast<int64_t>(g.max_pages_per_seq) * page_size;
+    for (int b = 0; b < g.batch; ++b) {
+        if (lens[b] < 0 || lens[b] > cap) return PKV_EINVAL;
+        if (table) {
+            const int64_t pages = ceil_div(lens[b], page_size);
+            const int32_t* row = table + static_cast<size_t>(b) * g.max_pages_per_seq;
+            for (int64_t i = 0; i < pages; ++i)
+                if (row[i] < 0 || row[i] >= g.num_pages) return PKV_EINVAL;
+        }
+    }
+    return PKV_OK;
+}
+
+// Everything the planner decides, computed on the host only.
+struct Plan {
+    int32_t mode = PKV_MODE_DIRECT;
+    int32_t chunk = 1;
+    int32_t s_max = 0;
+    int32_t grid = 0;
+    int32_t empty_tiles = 0;
+    bool need_merge = false;
+    int32_t ws_slots = 0;
+    int64_t kv_bytes = 0, ws_bytes = 0, table_bytes = 0;
+    std::vector<pkv_work_item> items;   // queue (or padded grid / direct tiles, for inspection)
+    std::vector<int32_t> row_start, row_splits;
+};
+
+int compute_plan(const pkv_geom& g, int32_t ps, const int32_t* lens, const Options& o, int num_sms,
+                 int ctas_per_sm, Plan* r) {
+    const int B = g.batch, Hkv = g.num_kv_heads, G = g.num_q_heads / g.num_kv_heads, D = g.head_dim;
+    std::vector<int32_t> pages(B);
+    int64_t p_max = 0, p_total = 0, tokens = 0;
+    for (int b = 0; b < B; ++b) {
+        pages[b] = static_cast<int32_t>(ceil_div(lens[b], ps));
+        p_max = std::max<int64_t>(p_max, pages[b]);
+        p_total += pages[b];
+        tokens += lens[b];
+    }
+    const int64_t units = static_cast<int64_t>(B) * Hkv;
+    const bool big_batch = units >= static_cast<int64_t>(o.direct_units_per_sm) * num_sms;
+    auto policy_chunk = [&]() -> int64_t {
+        if (big_batch) return std::max<int64_t>(p_max, 1);
+        const int64_t target = std::max<int64_t>(1, static_cast<int64_t>(o.target_ctas_per_sm) * num_sms);
+        return std::max<int64_t>(o.min_chunk_pages, ceil_div(Hkv * p_total, target));
+    };
+
+    int64_t chunk;
+    int mode = o.force_mode;
+    if (o.num_splits > 0)
+        chunk = p_max > 0 ? ceil_div(p_max, o.num_splits) : 1;
+    else if (mode == PKV_MODE_DIRECT)
+        chunk = std::max<int64_t>(p_max, 1);
+    else
+        chunk = policy_chunk();
+    chunk = std::max<int64_t>(chunk, 1);
+    if (mode == PKV_MODE_AUTO) mode = chunk >= p_max ? PKV_MODE_DIRECT : PKV_MODE_SPLIT_QUEUE;
+    if (mode == PKV_MODE_DIRECT) chunk = std::max<int64_t>(p_max, 1);
+
+    r->mode = mode;
+    r->chunk = static_cast<int32_t>(chunk);
+    r->s_max = static_cast<int32_t>(ceil_div(p_max, chunk));
+    r->kv_bytes = tokens * Hkv * D * 2 * 2;
+    r->table_bytes = p_total * Hkv * 4;
+    r->items.clear();
+    r->row_start.assign(B, 0);
+    r->row_splits.assign(B, 0);
+    r->empty_tiles = 0;
+    r->need_merge = false;
+    int64_t merged_slots = 0;
+
+    if (mode == PKV_MODE_DIRECT) {
+        for (int b = 0; b < B; ++b)
+            for (int kvh = 0; kvh < Hkv; ++kvh) r->items.push_back({b, kvh, 0, 0, pages[b]});
+        r->grid = B * Hkv;
+        r->ws_slots = 0;
+    } else if (mode == PKV_MODE_SPLIT_PADDED) {
+        for (int b = 0; b < B; ++b) {
+            r->row_start[b] = b * Hkv * r->s_max;
+            r->row_splits[b] = r->s_max;
+            for (int kvh = 0; kvh < Hkv; ++kvh)
+                for (int s = 0; s < r->s_max; ++s) {
+                    const int32_t pb = static_cast<int32_t>(std::min<int64_t>(s * chunk, pages[b]));
+                    const int32_t pe = static_cast<int32_t>(std::min<int64_t>((s + 1) * chunk, pages[b]));
+                    if (pb == pe) ++r->empty_tiles;
+                    r->items.push_back({b, kvh, s, pb, pe});
+                }
+        }
+        r->grid = B * Hkv * r->s_max;
+        r->ws_slots = r->grid;
+        r->need_merge = r->s_max != 1;
+        if (r->need_merge) merged_slots = r->grid;
+    } else {   // compact queue: SPLIT_QUEUE and PERSISTENT
+        int32_t slot = 0;
+        bool any_unfinished = false;
+        for (int b = 0; b < B; ++b) {
+            const int32_t sb = static_cast<int32_t>(ceil_div(pages[b], chunk));
+            r->row_start[b] = slot;
+            r->row_splits[b] = sb;
+            if (sb != 1) any_unfinished = true;
+            if (sb > 1) merged_slots += static_cast<int64_t>(sb) * Hkv;
+            for (int kvh = 0; kvh < Hkv; ++kvh)
+                for (int s = 0; s < sb; ++s)
+                    r->items.push_back({b, kvh, s, static_cast<int32_t>(s * chunk),
+                                        static_cast<int32_t>(std::min<int64_t>((s + 1) * chunk, pages[b]))});
+            slot += sb * Hkv;
+        }
+        r->ws_slots = slot;
+        const int32_t T = static_cast<int32_t>(r->items.size());
+        if (mode == PKV_MODE_SPLIT_QUEUE) {
+            r->grid = T;
+            r->need_merge = any_unfinished;
+        } else {
+            r->grid = B > 0 ? std::max(1, std::min<int32_t>(T, num_sms * std::max(1, ctas_per_sm))) : 0;
+            bool any_split = false;
+            for (int b = 0; b < B; ++b) any_split |= r->row_splits[b] > 1;
+            r->need_merge = o.separate_merge && any_split;
+        }
+    }
+    r->ws_bytes = merged_slots * G * (D + 1) * 4 * 2;   // written once, read once
+    return PKV_OK;
+}
+
+int32_t launches_of(const Plan& p) { return (p.grid > 0 ? 1 : 0) + (p.need_merge ? 1 : 0); }
+
+void fill_info(const Plan& p, const pkv_geom& g, int num_sms, pkv_plan_info* info) {
+    memset(info, 0, sizeof(*info));
+    info->mode = p.mode;
+    info->chunk_pages = p.chunk;
+    info->max_splits = p.s_max;
+    info->num_tiles = p.grid;
+    if (p.mode == PKV_MODE_PERSISTENT) info->num_tiles = static_cast<int32_t>(p.items.size());
+    info->num_work_items = static_cast<int32_t>(p.items.size());
+    info->empty_tiles = p.empty_tiles;
+    info->launches_per_step = g.batch > 0 ? launches_of(p) : 0;
+    info->grid_ctas = p.grid;
+    info->num_sms = num_sms;
+    info->kv_bytes = p.kv_bytes;
+    info->workspace_bytes = p.ws_bytes;
+    info->table_bytes = p.table_bytes;
+}
+
+// ------------------------------------------------------------------ TMA descriptors
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+// The pool [num_pages][page_size][Hkv][D] bf16 as a 3-D tensor
+// {D, Hkv, num_pages * page_size} (innermost first); one box is kBlockRows
+// consecutive tokens of one KV head.
+int encode_pool_map(CUtensorMap* map, const void* pool, const pkv_geom& g, int32_t page_size) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return cuda_fail(cudaErrorNotSupported);
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(g.head_dim), static_cast<cuuint64_t>(g.num_kv_heads),
+                                static_cast<cuuint64_t>(g.num_pages) * page_size};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(g.head_dim) * 2,
+                                   static_cast<cuuint64_t>(g.num_kv_heads) * g.head_dim * 2};
+    const cuuint32_t box[3] = {static_cast<cuuint32_t>(g.head_dim), 1u, static_cast<cuuint32_t>(pkv::kBlockRows)};
+    const cuuint32_t estr[3] = {1u, 1u, 1u};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(pool), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return cuda_fail(cudaErrorInvalidValue);
+    return PKV_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+
+// ------------------------------------------------------------------ plan object
+
+struct pkv_plan_s {
+    pkv_geom g{};
+    int32_t page_size = 0;
+    Options opts;
+    int device = 0;
+    int num_sms = 0;
+    int ctas_per_sm = 1;
+    Plan plan;
+
+    // host staging (pinned) and device copy: [items][row_start B][row_splits B]
+    int32_t* host_buf = nullptr;
+    int32_t* dev_buf = nullptr;
+    size_t buf_cap_items = 0;
+    size_t upload_bytes = 0;
+    bool dirty = false;
+    cudaEvent_t upload_done = nullptr;
+    bool upload_recorded = false;
+
+    float* ws_o = nullptr;
+    float* ws_lse = nullptr;
+    size_t ws_cap_slots = 0;
+    uint32_t* arrive = nullptr;
+    pkv::DeviceCounters* ctr = nullptr;
+
+    const void* map_k = nullptr;
+    const void* map_v = nullptr;
+    CUtensorMap kmap{}, vmap{};
+
+    bool profile = false;
+    cudaEvent_t ev[3] = {nullptr, nullptr, nullptr};
+    int ev_launches = 0;
+};
+
+namespace {
+
+void release(pkv_plan_s* p) {
+    if (!p) return;
+    if (p->upload_recorded) cudaEventSynchronize(p->upload_done);
+    cudaFreeHost(p->host_buf);
+    cudaFree(p->dev_buf);
+    cudaFree(p->ws_o);
+    cudaFree(p->ws_lse);
+    cudaFree(p->arrive);
+    cudaFree(p->ctr);
+    if (p->upload_done) cudaEventDestroy(p->upload_done);
+    for (auto& e : p->ev)
+        if (e) cudaEventDestroy(e);
+    delete p;
+}
+
+// Size buffers for the current plan (grow only) and stage the queue for upload.
+int stage(pkv_plan_s* p) {
+    const Plan& pl = p->plan;
+    const size_t items = pl.items.size();
+    const int B = p->g.batch;
+    if (items > p->buf_cap_items || !p->host_buf) {
+        const size_t cap = std::max<size_t>(items + items / 2, 64);
+        if (p->upload_recorded) PKV_CUDA(cudaEventSynchronize(p->upload_done));
+        cudaFreeHost(p->host_buf);
+        cudaFree(p->dev_buf);
+        p->host_buf = nullptr;
+        p->dev_buf = nullptr;
+        const size_t bytes = (cap * 5 + 2 * static_cast<size_t>(B)) * sizeof(int32_t);
+        if (cudaMallocHost(&p->host_buf, bytes) != cudaSuccess) return PKV_ENOMEM;
+        if (cudaMalloc(&p->dev_buf, bytes) != cudaSuccess) return PKV_ENOMEM;
+        p->buf_cap_items = cap;
+    }
+    const size_t slots = static_cast<size_t>(std::max(pl.ws_slots, 1));
+    const int G = p->g.num_q_heads / p->g.num_kv_heads;
+    if (slots > p->ws_cap_slots) {
+        const size_t cap = slots + slots / 2;
+        cudaFree(p->ws_o);
+        cudaFree(p->ws_lse);
+        p->ws_o = nullptr;
+        p->ws_lse = nullptr;
+        if (cudaMalloc(&p->ws_o, cap * G * p->g.head_dim * sizeof(float)) != cudaSuccess) return PKV_ENOMEM;
+        if (cudaMalloc(&p->ws_lse, cap * G * sizeof(float)) != cudaSuccess) return PKV_ENOMEM;
+        p->ws_cap_slots = cap;
+    }
+    // host staging: the queue, then row_start, then row_splits
+    int32_t* h = p->host_buf;
+    memcpy(h, pl.items.data(), items * sizeof(pkv_work_item));
+    int32_t* rs = h + p->buf_cap_items * 5;
+    if (B > 0) {
+        memcpy(rs, pl.row_start.data(), B * sizeof(int32_t));
+        memcpy(rs + B, pl.row_splits.data(), B * sizeof(int32_t));
+    }
+    p->upload_bytes = (p->buf_cap_items * 5 + 2 * static_cast<size_t>(B)) * sizeof(int32_t);
+    p->dirty = pl.mode != PKV_MODE_DIRECT;
+    return PKV_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* pkv_strerror(int code) {
+    switch (code) {
+        case PKV_OK: return "ok";
+        case PKV_EINVAL: return "invalid argument";
+        case PKV_ENOMEM: return "out of memory";
+        case PKV_ECUDA: return "CUDA runtime error";
+        case PKV_EUNSUPPORTED: return "unsupported shape";
+        case PKV_EDEVICE: return "device status word set";
+        case PKV_ENOSPACE: return "no free page / row table full";
+        default: return "unknown error";
+    }
+}
+
+int pkv_last_cuda_error(void) { return g_last_cuda_error; }
+
+int pkv_plan_dry_run(const int32_t* seq_lens_h, const int32_t* block_table_h, int32_t page_size,
+                     const pkv_geom* geom, const pkv_plan_opts* opts, pkv_plan_info* info,
+                     pkv_work_item* items, int32_t capacity, int32_t* count) {
+    Options o;
+    int rc = resolve_options(opts, &o);
+    if (rc) return rc;
+    if ((rc = validate_geometry(geom, page_size))) return rc;
+    if ((rc = validate_rows(*geom, page_size, seq_lens_h, block_table_h))) return rc;
+    if (o.num_sms <= 0) return PKV_EINVAL;   // no device is consulted here
+    Plan pl;
+    if ((rc = compute_plan(*geom, page_size, seq_lens_h, o, o.num_sms, std::max(1, o.ctas_per_sm), &pl)))
+        return rc;
+    if (info) fill_info(pl, *geom, o.num_sms, info);
+    const int32_t n = static_cast<int32_t>(pl.items.size());
+    if (count) *count = n;
+    if (items && capacity > 0) memcpy(items, pl.items.data(), sizeof(pkv_work_item) * std::min(n, capacity));
+    return PKV_OK;
+}
+
+int pkv_plan(const int32_t* seq_lens_h, const int32_t* block_table_h, int32_t page_size, const pkv_geom* geom,
+             const pkv_plan_opts* opts, pkv_plan_t* plan) {
+    if (!plan) return PKV_EINVAL;
+    *plan = nullptr;
+    Options o;
+    int rc = resolve_options(opts, &o);
+    if (rc) return rc;
+    if ((rc = validate_geometry(geom, page_size))) return rc;
+    if ((rc = validate_rows(*geom, page_size, seq_lens_h, block_table_h))) return rc;
+
+    pkv_plan_s* p = new (std::nothrow) pkv_plan_s;
+    if (!p) return PKV_ENOMEM;
+    p->g = *geom;
+    p->page_size = page_size;
+    p->opts = o;
+    cudaError_t e = cudaGetDevice(&p->device);
+    if (e == cudaSuccess && o.num_sms <= 0)
+        e = cudaDeviceGetAttribute(&p->num_sms, cudaDevAttrMultiProcessorCount, p->device);
+    if (e != cudaSuccess) {
+        delete p;
+        return cuda_fail(e);
+    }
+    if (o.num_sms > 0) p->num_sms = o.num_sms;
+    const int G = geom->num_q_heads / geom->num_kv_heads;
+    p->ctas_per_sm = o.ctas_per_sm > 0 ? o.ctas_per_sm : std::max(1, pkv::attention_ctas_per_sm(geom->head_dim, G));
+
+    if ((rc = compute_plan(p->g, page_size, seq_lens_h, o, p->num_sms, p->ctas_per_sm, &p->plan))) {
+        delete p;
+        return rc;
+    }
+    if (cudaEventCreateWithFlags(&p->upload_done, cudaEventDisableTiming) != cudaSuccess ||
+        cudaMalloc(&p->ctr, sizeof(pkv::DeviceCounters)) != cudaSuccess ||
+        cudaMalloc(&p->arrive, sizeof(uint32_t) * std::max(1, geom->batch * geom->num_kv_heads)) != cudaSuccess) {
+        release(p);
+        return PKV_ENOMEM;
+    }
+    if (cudaMemset(p->ctr, 0, sizeof(pkv::DeviceCounters)) != cudaSuccess ||
+        cudaMemset(p->arrive, 0, sizeof(uint32_t) * std::max(1, geom->batch * geom->num_kv_heads)) != cudaSuccess ||
+        cudaDeviceSynchronize() != cudaSuccess) {
+        release(p);
+        return cuda_fail(cudaGetLastError());
+    }
+    if ((rc = stage(p))) {
+        release(p);
+        return rc;
+    }
+    *plan = p;
+    return PKV_OK;
+}
+
+int pkv_plan_update(pkv_plan_t p, const int32_t* seq_lens_h, const int32_t* block_table_h) {
+    if (!p) return PKV_EINVAL;
+    int rc = validate_rows(p->g, p->page_size, seq_lens_h, block_table_h);
+    if (rc) return rc;
+    if (p->upload_recorded) PKV_CUDA(cudaEventSynchronize(p->upload_done));
+    if ((rc = compute_plan(p->g, p->page_size, seq_lens_h, p->opts, p->num_sms, p->ctas_per_sm, &p->plan))) return rc;
+    return stage(p);
+}
+
+void pkv_plan_destroy(pkv_plan_t p) { release(p); }
+
+int pkv_plan_get_info(pkv_plan_t p, pkv_plan_info* info) {
+    if (!p || !info) return PKV_EINVAL;
+    fill_info(p->plan, p->g, p->num_sms, info);
+    return PKV_OK;
+}
+
+int pkv_plan_queue(pkv_plan_t p, pkv_work_item* items, int32_t capacity, int32_t* count) {
+    if (!p || !count) return PKV_EINVAL;
+    const int32_t n = static_cast<int32_t>(p->plan.items.size());
+    *count = n;
+    if (items && capacity > 0) memcpy(items, p->plan.items.data(), sizeof(pkv_work_item) * std::min(n, capacity));
+    return PKV_OK;
+}
+
+int pkv_decode(const void* q, const void* k_pages, const void* v_pages, const int32_t* block_table_d,
+               const int32_t* seq_lens_d, pkv_plan_t p, float* out, float* lse, pkv_stream_t stream) {
+    if (!p) return PKV_EINVAL;
+    if (p->g.batch == 0) return PKV_OK;
+    if (!q || !k_pages || !v_pages || !block_table_d || !seq_lens_d || !out || !lse) return PKV_EINVAL;
+    if (!aligned16(q) || !aligned16(k_pages) || !aligned16(v_pages) || !aligned16(out) ||
+        (reinterpret_cast<uintptr_t>(lse) & 3u) || (reinterpret_cast<uintptr_t>(block_table_d) & 3u) ||
+        (reinterpret_cast<uintptr_t>(seq_lens_d) & 3u))
+        return PKV_EINVAL;
+    int dev = -1;
+    PKV_CUDA(cudaGetDevice(&dev));
+    if (dev != p->device) return PKV_EINVAL;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+
+    if (p->dirty) {
+        PKV_CUDA(cudaMemcpyAsync(p->dev_buf, p->host_buf, p->upload_bytes, cudaMemcpyHostToDevice, s));
+        PKV_CUDA(cudaEventRecord(p->upload_done, s));
+        p->upload_recorded = true;
+        p->dirty = false;
+    }
+    if (k_pages != p->map_k) {
+        int rc = encode_pool_map(&p->kmap, k_pages, p->g, p->page_size);
+        if (rc) return rc;
+        p->map_k = k_pages;
+    }
+    if (v_pages != p->map_v) {
+        int rc = encode_pool_map(&p->vmap, v_pages, p->g, p->page_size);
+        if (rc) return rc;
+        p->map_v = v_pages;
+    }
+
+    const Plan& pl = p->plan;
+    pkv::AttnParams a{};
+    a.q = static_cast<const uint16_t*>(q);
+    a.block_table = block_table_d;
+    a.seq_lens = seq_lens_d;
+    a.queue = reinterpret_cast<const pkv_work_item*>(p->dev_buf);
+    a.row_start = p->dev_buf + p->buf_cap_items * 5;
+    a.row_splits = a.row_start + p->g.batch;
+    a.out = out;
+    a.lse = lse;
+    a.ws_o = p->ws_o;
+    a.ws_lse = p->ws_lse;
+    a.arrive = p->arrive;
+    a.ctr = p->ctr;
+    a.B = p->g.batch;
+    a.Hq = p->g.num_q_heads;
+    a.Hkv = p->g.num_kv_heads;
+    a.D = p->g.head_dim;
+    a.page_size = p->page_size;
+    a.max_pages = p->g.max_pages_per_seq;
+    a.num_pages = p->g.num_pages;
+    a.chunk_pages = pl.chunk;
+    a.max_splits = pl.s_max;
+    a.num_tiles = static_cast<int32_t>(pl.items.size());
+    a.fused_merge = p->opts.separate_merge ? 0 : 1;
+    a.scale_log2 = static_cast<float>(1.4426950408889634 / sqrt(static_cast<double>(p->g.head_dim)));
+    switch (pl.mode) {
+        case PKV_MODE_DIRECT: a.route = pkv::kRouteDirect; break;
+        case PKV_MODE_SPLIT_QUEUE: a.route = pkv::kRouteQueue; break;
+        case PKV_MODE_SPLIT_PADDED: a.route = pkv::kRoutePadded; break;
+        default: a.route = pkv::kRoutePersistent; break;
+    }
+
+    if (p->profile) {
+        for (auto& ev : p->ev)
+            if (!ev) PKV_CUDA(cudaEventCreate(&ev));
+        PKV_CUDA(cudaEventRecord(p->ev[0], s));
+    }
+    int n = 0;
+    if (pl.grid > 0) {
+        PKV_CUDA(pkv::launch_attention(a, p->kmap, p->vmap, pl.grid, s));
+        ++n;
+        if (p->profile) PKV_CUDA(cudaEventRecord(p->ev[n], s));
+    }
+    if (pl.need_merge) {
+        PKV_CUDA(pkv::launch_merge(a, s));
+        ++n;
+        if (p->profile) PKV_CUDA(cudaEventRecord(p->ev[n], s));
+    }
+    p->ev_launches = n;
+    return PKV_OK;
+}
+
+int pkv_append(const void* k_new, const void* v_new, void* k_pages, void* v_pages, const int32_t* block_table_d,
+               int32_t* seq_lens_d, pkv_plan_t p, pkv_stream_t stream) {
+    if (!p) return PKV_EINVAL;
+    if (p->g.batch == 0) return PKV_OK;
+    if (!k_new || !v_new || !k_pages || !v_pages || !block_table_d || !seq_lens_d) return PKV_EINVAL;
+    if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_pages) || !aligned16(v_pages)) return PKV_EINVAL;
+    PKV_CUDA(pkv::launch_append(static_cast<const uint16_t*>(k_new), static_cast<const uint16_t*>(v_new),
+                                static_cast<uint16_t*>(k_pages), static_cast<uint16_t*>(v_pages), block_table_d,
+                                seq_lens_d, p->g.batch, p->g.num_kv_heads, p->g.head_dim, p->page_size,
+                                p->g.max_pages_per_seq, p->g.num_pages, &p->ctr->status,
+                                reinterpret_cast<cudaStream_t>(stream)));
+    return PKV_OK;
+}
+
+int pkv_status(pkv_plan_t p, pkv_stream_t stream, uint32_t* status) {
+    if (!p || !status) return PKV_EINVAL;
+    PKV_CUDA(cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)));
+    PKV_CUDA(cudaMemcpy(status, &p->ctr->status, sizeof(uint32_t), cudaMemcpyDeviceToHost));
+    PKV_CUDA(cudaMemset(&p->ctr->status, 0, sizeof(uint32_t)));
+    return PKV_OK;
+}
+
+int pkv_read_workspace(pkv_plan_t p, pkv_stream_t stream, float* o_h, float* lse_h, int32_t capacity,
+                       int32_t* count) {
+    if (!p || !count) return PKV_EINVAL;
+    const int32_t n = p->plan.ws_slots;
+    *count = n;
+    if (!o_h || !lse_h || capacity <= 0 || n == 0) return PKV_OK;
+    const int32_t m = std::min(n, capacity);
+    const int G = p->g.num_q_heads / p->g.num_kv_heads;
+    PKV_CUDA(cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)));
+    PKV_CUDA(cudaMemcpy(o_h, p->ws_o, sizeof(float) * m * G * p->g.head_dim, cudaMemcpyDeviceToHost));
+    PKV_CUDA(cudaMemcpy(lse_h, p->ws_lse, sizeof(float) * m * G, cudaMemcpyDeviceToHost));
+    for (int64_t i = 0; i < static_cast<int64_t>(m) * G; ++i) lse_h[i] *= 0.69314718055994530942f;
+    return PKV_OK;
+}
+
+int pkv_profile_enable(pkv_plan_t p, int32_t enable) {
+    if (!p) return PKV_EINVAL;
+    p->profile = enable != 0;
+    return PKV_OK;
+}
+
+int pkv_profile_read(pkv_plan_t p, float* ms, int32_t capacity, int32_t* count) {
+    if (!p || !count) return PKV_EINVAL;
+    *count = p->profile ? p->ev_launches : 0;
+    if (!p->profile || !ms) return PKV_OK;
+    for (int i = 0; i < p->ev_launches && i < capacity; ++i) {
+        PKV_CUDA(cudaEventSynchronize(p->ev[i + 1]));
+        PKV_CUDA(cudaEventElapsedTime(&ms[i], p->ev[i], p->ev[i + 1]));
+    }
+    return PKV_OK;
+}
+
+}  // extern "C"
+
+// ------------------------------------------------------------------ page pool
+
+struct pkv_pool_s {
+    std::deque<int32_t> free_list;
+    int32_t num_pages = 0;
+};
+
+extern "C" {
+
+int pkv_pool_create(const int32_t* free_pages, int32_t count, int32_t num_pages, pkv_pool_t* pool) {
+    if (!pool || count < 0 || (count > 0 && !free_pages) || num_pages <= 0) return PKV_EINVAL;
+    *pool = nullptr;
+    for (int32_t i = 0; i < count; ++i)
+        if (free_pages[i] < 0 || free_pages[i] >= num_pages) return PKV_EINVAL;
+    pkv_pool_s* p = new (std::nothrow) pkv_pool_s;
+    if (!p) return PKV_ENOMEM;
+    p->free_list.assign(free_pages, free_pages + count);
+    p->num_pages = num_pages;
+    *pool = p;
+    return PKV_OK;
+}
+
+int pkv_pool_reserve(pkv_pool_t pool, const int32_t* seq_lens_h, int32_t* block_table_h, int32_t batch,
+                     int32_t max_pages_per_seq, int32_t page_size, int32_t* rows_out, int32_t* n_rows) {
+    if (!pool || batch < 0 || (batch > 0 && (!seq_lens_h || !block_table_h)) || max_pages_per_seq <= 0 ||
+        page_size <= 0)
+        return PKV_EINVAL;
+    // first pass: count and check, so that failure changes nothing
+    auto wants_page = [&](int32_t b) {
+        return seq_lens_h[b] % page_size == 0 &&
+               block_table_h[static_cast<size_t>(b) * max_pages_per_seq + seq_lens_h[b] / page_size] < 0;
+    };
+    int32_t need = 0;
+    for (int32_t b = 0; b < batch; ++b) {
+        if (seq_lens_h[b] < 0) return PKV_EINVAL;
+        if (seq_lens_h[b] % page_size == 0 && seq_lens_h[b] / page_size >= max_pages_per_seq) return PKV_ENOSPACE;
+        if (wants_page(b)) ++need;
+    }
+    if (static_cast<size_t>(need) > pool->free_list.size()) return PKV_ENOSPACE;
+    int32_t k = 0;
+    for (int32_t b = 0; b < batch; ++b) {
+        if (!wants_page(b)) continue;
+        block_table_h[static_cast<size_t>(b) * max_pages_per_seq + seq_lens_h[b] / page_size] =
+            pool->free_list.front();
+        pool->free_list.pop_front();
+        if (rows_out) rows_out[k] = b;
+        ++k;
+    }
+    if (n_rows) *n_rows = k;
+    return PKV_OK;
+}
+
+int pkv_pool_release(pkv_pool_t pool, const int32_t* pages, int32_t count) {
+    if (!pool || count < 0 || (count > 0 && !pages)) return PKV_EINVAL;
+    for (int32_t i = 0; i < count; ++i)
+        if (pages[i] < 0 || pages[i] >= pool->num_pages) return PKV_EINVAL;
+    pool->free_list.insert(pool->free_list.end(), pages, pages + count);
+    return PKV_OK;
+}
+
+int32_t pkv_pool_free_count(pkv_pool_t pool) { return pool ? static_cast<int32_t>(pool->free_list.size()) : 0; }
+
+void pkv_pool_destroy(pkv_pool_t pool) { delete pool; }
+
+}  // extern "C"

@@ -1,0 +1,67 @@
+// pkv_append.cu -- write one new K/V token per row into its page.
+//
+// Layout from "PersistentKV: Page-Aware Decode Scheduling for Long-Context LLM
+// Serving on Commodity GPUs" (gist.science summary), Methodology section 1
+// "Layout": token t of row b lives in page block_table[b][t / page_size], slot
+// t % page_size.  The operation is the KV-cache update of "GPUOS" (arXiv
+// 2604.17861, section 4 operator library): the new token goes to position
+// seq_lens[b], then the length grows by one.
+//
+// One CTA per row; each thread moves 16-byte vectors of the row's
+// Hkv * D bf16 K and V values.  A row whose position has no page (table full or
+// entry out of range) sets a status bit and is left unchanged.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "pkv_internal.h"
+
+namespace pkv {
+namespace {
+
+__global__ void __launch_bounds__(128) append_kernel(const uint16_t* __restrict__ k_new,
+                                                     const uint16_t* __restrict__ v_new,
+                                                     uint16_t* __restrict__ k_pages, uint16_t* __restrict__ v_pages,
+                                                     const int32_t* __restrict__ block_table,
+                                                     int32_t* __restrict__ seq_lens, int Hkv, int D, int page_size,
+                                                     int max_pages, int num_pages, uint32_t* status) {
+    __shared__ int s_page, s_pos;
+    const int b = blockIdx.x;
+    if (threadIdx.x == 0) {
+        const int pos = seq_lens[b];
+        int page = -1;
+        if (pos < 0 || pos / page_size >= max_pages) {
+            atomicOr(status, static_cast<uint32_t>(PKV_DEV_ROW_FULL));
+        } else {
+            page = block_table[static_cast<size_t>(b) * max_pages + pos / page_size];
+            if (page < 0 || page >= num_pages) {
+                atomicOr(status, static_cast<uint32_t>(PKV_DEV_PAGE_OOB));
+                page = -1;
+            }
+        }
+        s_page = page;
+        s_pos = pos;
+    }
+    __syncthreads();
+    if (s_page < 0) return;
+    const int row = Hkv * D;   // elements of one token across all KV heads
+    const size_t dst = (static_cast<size_t>(s_page) * page_size + s_pos % page_size) * row;
+    const size_t src = static_cast<size_t>(b) * row;
+    for (int c = threadIdx.x * 8; c < row; c += blockDim.x * 8) {
+        *reinterpret_cast<uint4*>(k_pages + dst + c) = *reinterpret_cast<const uint4*>(k_new + src + c);
+        *reinterpret_cast<uint4*>(v_pages + dst + c) = *reinterpret_cast<const uint4*>(v_new + src + c);
+    }
+    if (threadIdx.x == 0) seq_lens[b] = s_pos + 1;
+}
+
+}  // namespace
+
+cudaError_t launch_append(const uint16_t* k_new, const uint16_t* v_new, uint16_t* k_pages, uint16_t* v_pages,
+                          const int32_t* block_table, int32_t* seq_lens, int B, int Hkv, int D, int page_size,
+                          int max_pages, int num_pages, uint32_t* status, cudaStream_t stream) {
+    if (B == 0) return cudaSuccess;
+    append_kernel<<<B, 128, 0, stream>>>(k_new, v_new, k_pages, v_pages, block_table, seq_lens, Hkv, D, page_size,
+                                         max_pages, num_pages, status);
+    return cudaGetLastError();
+}
+
+}  // namespace pkv

@@ -1,0 +1,68 @@
+// pkv_internal.h -- interface between the host library (planner, C ABI) and
+// the CUDA kernels.  Not installed; not part of the public ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "pkv.h"
+
+namespace pkv {
+
+// Tokens per pipeline stage.  A page of page_size tokens is streamed as
+// page_size / kBlockRows stages; page_size must be a multiple of it.
+constexpr int kBlockRows = 16;
+
+// Device-side bookkeeping of a plan (zeroed once at creation; kernels that
+// change it put it back before they exit, so no host reset is needed between
+// launches or graph replays).
+struct DeviceCounters {
+    uint32_t next_tile;  // persistent mode: next queue index to hand out
+    uint32_t done_ctas;  // persistent mode: CTAs that found the queue empty
+    uint32_t status;     // pkv_device_status_bits, sticky until pkv_status
+    uint32_t pad;
+};
+
+enum Route : int32_t {
+    kRouteDirect = 0,   // tile = (b, kvh) from blockIdx; whole row; finalise
+    kRouteQueue = 1,    // tile = queue[blockIdx]
+    kRoutePadded = 2,   // tile = (b, kvh, s) from blockIdx over B*Hkv*S_max
+    kRoutePersistent = 3  // tiles from an atomic counter over the queue
+};
+
+struct AttnParams {
+    const uint16_t* q;            // bf16 [B][Hq][D]
+    const int32_t* block_table;   // [B][max_pages]
+    const int32_t* seq_lens;      // [B]
+    const pkv_work_item* queue;   // [num_tiles] for queue / persistent routes
+    const int32_t* row_start;     // [B] workspace slot of (b, kvh 0, split 0)
+    const int32_t* row_splits;    // [B] slots per (b, kvh); 1 = tile finalises in place
+    float* out;                   // [B][Hq][D]
+    float* lse;                   // [B][Hq]
+    float* ws_o;                  // [slots][G][D] normalised partial outputs
+    float* ws_lse;                // [slots][G] partial LSE, log2 units
+    uint32_t* arrive;             // [B*Hkv] fused-merge arrival counters
+    DeviceCounters* ctr;
+    int32_t B, Hq, Hkv, D, page_size, max_pages, num_pages;
+    int32_t chunk_pages, max_splits, num_tiles;
+    int32_t route;
+    int32_t fused_merge;          // persistent route: last arriving split merges
+    float scale_log2;             // log2(e) / sqrt(D)
+};
+
+// Attention launch: one of the four routes.  kmap / vmap are TMA descriptors
+// of the K and V pools viewed as [page_size * num_pages][Hkv][D] (innermost D),
+// box {D, 1, kBlockRows}.
+cudaError_t launch_attention(const AttnParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                             int grid, cudaStream_t stream);
+cudaError_t launch_merge(const AttnParams& p, cudaStream_t stream);
+cudaError_t launch_append(const uint16_t* k_new, const uint16_t* v_new, uint16_t* k_pages,
+                          uint16_t* v_pages, const int32_t* block_table, int32_t* seq_lens,
+                          int B, int Hkv, int D, int page_size, int max_pages, int num_pages,
+                          uint32_t* status, cudaStream_t stream);
+// Resident CTAs per SM of the attention kernel for this (D, G); 0 if unsupported.
+int attention_ctas_per_sm(int D, int G);
+bool shape_supported(int D, int G);
+
+}  // namespace pkv

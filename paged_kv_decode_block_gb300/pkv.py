@@ -1,0 +1,324 @@
+"""Python binding of libpkv (include/pkv.h): argument marshalling only.
+
+Every call forwards device pointers (``tensor.data_ptr()``), sizes and the CUDA
+stream handle to the C ABI; all of the decode path runs in the library's CUDA
+kernels.  PyTorch is used for device memory and streams.  If the library has
+not been built, every entry point raises -- there is no other implementation.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libpkv.so")
+
+MODE_AUTO, MODE_DIRECT, MODE_SPLIT_QUEUE, MODE_SPLIT_PADDED, MODE_PERSISTENT = range(5)
+MODE_NAMES = {MODE_AUTO: "auto", MODE_DIRECT: "direct", MODE_SPLIT_QUEUE: "split_queue",
+              MODE_SPLIT_PADDED: "split_padded", MODE_PERSISTENT: "persistent"}
+MODES = {v: k for k, v in MODE_NAMES.items()}
+
+OK, EINVAL, ENOMEM, ECUDA, EUNSUPPORTED, EDEVICE, ENOSPACE = range(7)
+DEV_PAGE_OOB, DEV_PLAN_MISMATCH, DEV_TIMEOUT, DEV_ROW_FULL = 1, 2, 4, 8
+
+
+class Geom(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int32), ("num_q_heads", ctypes.c_int32),
+                ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+                ("max_pages_per_seq", ctypes.c_int32), ("num_pages", ctypes.c_int32)]
+
+
+class PlanOpts(ctypes.Structure):
+    _fields_ = [("force_mode", ctypes.c_int32), ("num_splits", ctypes.c_int32),
+                ("direct_units_per_sm", ctypes.c_int32), ("target_ctas_per_sm", ctypes.c_int32),
+                ("min_chunk_pages", ctypes.c_int32), ("ctas_per_sm", ctypes.c_int32),
+                ("separate_merge", ctypes.c_int32), ("num_sms", ctypes.c_int32)]
+
+
+class WorkItem(ctypes.Structure):
+    _fields_ = [("b", ctypes.c_int32), ("kvh", ctypes.c_int32), ("split", ctypes.c_int32),
+                ("page_begin", ctypes.c_int32), ("page_end", ctypes.c_int32)]
+
+
+class PlanInfo(ctypes.Structure):
+    _fields_ = [("mode", ctypes.c_int32), ("chunk_pages", ctypes.c_int32),
+                ("max_splits", ctypes.c_int32), ("num_tiles", ctypes.c_int32),
+                ("num_work_items", ctypes.c_int32), ("empty_tiles", ctypes.c_int32),
+                ("launches_per_step", ctypes.c_int32), ("grid_ctas", ctypes.c_int32),
+                ("num_sms", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("kv_bytes", ctypes.c_int64), ("workspace_bytes", ctypes.c_int64),
+                ("table_bytes", ctypes.c_int64)]
+
+    def as_dict(self) -> dict:
+        d = {name: getattr(self, name) for name, _ in self._fields_ if name != "reserved"}
+        d["mode_name"] = MODE_NAMES.get(self.mode, "?")
+        return d
+
+
+# symbol -> (restype, argtypes); the full C ABI of include/pkv.h
+_P, _I32, _I64, _U32P = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.POINTER(ctypes.c_uint32)
+_I32P = ctypes.POINTER(ctypes.c_int32)
+SIGNATURES = {
+    "pkv_plan": (ctypes.c_int, [_I32P, _I32P, _I32, ctypes.POINTER(Geom), ctypes.POINTER(PlanOpts),
+                                ctypes.POINTER(ctypes.c_void_p)]),
+    "pkv_plan_dry_run": (ctypes.c_int, [_I32P, _I32P, _I32, ctypes.POINTER(Geom), ctypes.POINTER(PlanOpts),
+                                        ctypes.POINTER(PlanInfo), ctypes.POINTER(WorkItem), _I32, _I32P]),
+    "pkv_plan_update": (ctypes.c_int, [_P, _I32P, _I32P]),
+    "pkv_plan_destroy": (None, [_P]),
+    "pkv_plan_get_info": (ctypes.c_int, [_P, ctypes.POINTER(PlanInfo)]),
+    "pkv_plan_queue": (ctypes.c_int, [_P, ctypes.POINTER(WorkItem), _I32, _I32P]),
+    "pkv_decode": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, _P, _P]),
+    "pkv_append": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, _P]),
+    "pkv_status": (ctypes.c_int, [_P, _P, _U32P]),
+    "pkv_read_workspace": (ctypes.c_int, [_P, _P, _P, _P, _I32, _I32P]),
+    "pkv_profile_enable": (ctypes.c_int, [_P, _I32]),
+    "pkv_profile_read": (ctypes.c_int, [_P, ctypes.POINTER(ctypes.c_float), _I32, _I32P]),
+    "pkv_pool_create": (ctypes.c_int, [_I32P, _I32, _I32, ctypes.POINTER(ctypes.c_void_p)]),
+    "pkv_pool_reserve": (ctypes.c_int, [_P, _I32P, _I32P, _I32, _I32, _I32, _I32P, _I32P]),
+    "pkv_pool_release": (ctypes.c_int, [_P, _I32P, _I32]),
+    "pkv_pool_free_count": (ctypes.c_int32, [_P]),
+    "pkv_pool_destroy": (None, [_P]),
+    "pkv_strerror": (ctypes.c_char_p, [ctypes.c_int]),
+    "pkv_last_cuda_error": (ctypes.c_int, []),
+}
+
+_lib = None
+
+
+class PkvError(RuntimeError):
+    def __init__(self, code: int, what: str = ""):
+        self.code = code
+        msg = load().pkv_strerror(code).decode()
+        if code == ECUDA:
+            msg += f" (cudaError {load().pkv_last_cuda_error()})"
+        super().__init__(f"{what}: {msg} [code {code}]" if what else f"{msg} [code {code}]")
+
+
+def load(path: str = LIB_PATH):
+    """The loaded library; raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(path):
+            raise RuntimeError(f"libpkv is not built ({path} missing); run __graft_entry__.build() "
+                               "or python -m paged_kv_decode_block_gb300.csrc.build")
+        lib = ctypes.CDLL(path)
+        for name, (res, args) in SIGNATURES.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+    return _lib
+
+
+def _check(rc: int, what: str):
+    if rc != OK:
+        raise PkvError(rc, what)
+
+
+def _i32(a):
+    return np.ascontiguousarray(a, dtype=np.int32)
+
+
+def _ptr_i32(a):
+    return a.ctypes.data_as(_I32P) if a is not None else None
+
+
+def _opts(force_mode=MODE_AUTO, num_splits=0, direct_units_per_sm=0, target_ctas_per_sm=0,
+          min_chunk_pages=0, ctas_per_sm=0, separate_merge=False, num_sms=0) -> PlanOpts:
+    if isinstance(force_mode, str):
+        force_mode = MODES[force_mode]
+    return PlanOpts(int(force_mode), int(num_splits), int(direct_units_per_sm),
+                    int(target_ctas_per_sm), int(min_chunk_pages), int(ctas_per_sm),
+                    int(bool(separate_merge)), int(num_sms))
+
+
+def _geom(B, Hq, Hkv, D, max_pages, num_pages) -> Geom:
+    return Geom(int(B), int(Hq), int(Hkv), int(D), int(max_pages), int(num_pages))
+
+
+def dry_run(seq_lens, block_table, page_size, *, B, Hq, Hkv, D, max_pages, num_pages, **opts):
+    """Planner only (no device): returns (info dict, tiles int32 [n][5])."""
+    lib = load()
+    lens = _i32(seq_lens)
+    table = _i32(block_table) if block_table is not None else None
+    g = _geom(B, Hq, Hkv, D, max_pages, num_pages)
+    o = _opts(**opts)
+    info = PlanInfo()
+    n = ctypes.c_int32(0)
+    _check(lib.pkv_plan_dry_run(_ptr_i32(lens), _ptr_i32(table), int(page_size), ctypes.byref(g),
+                                ctypes.byref(o), ctypes.byref(info), None, 0, ctypes.byref(n)), "pkv_plan_dry_run")
+    items = (WorkItem * max(n.value, 1))()
+    _check(lib.pkv_plan_dry_run(_ptr_i32(lens), _ptr_i32(table), int(page_size), ctypes.byref(g),
+                                ctypes.byref(o), None, items, n.value, ctypes.byref(n)), "pkv_plan_dry_run")
+    arr = np.ctypeslib.as_array(ctypes.cast(items, _I32P), shape=(max(n.value, 1) * 5,))
+    return info.as_dict(), arr[: n.value * 5].reshape(-1, 5).copy()
+
+
+def _stream_handle(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+class Plan:
+    """An opaque pkv plan (see pkv_plan in include/pkv.h)."""
+
+    def __init__(self, seq_lens, block_table, page_size, *, B, Hq, Hkv, D, max_pages, num_pages, **opts):
+        lib = load()
+        lens = _i32(seq_lens)
+        table = _i32(block_table) if block_table is not None else None
+        self.geom = _geom(B, Hq, Hkv, D, max_pages, num_pages)
+        self.page_size = int(page_size)
+        self.G = Hq // Hkv
+        self.D = D
+        o = _opts(**opts)
+        h = ctypes.c_void_p()
+        _check(lib.pkv_plan(_ptr_i32(lens), _ptr_i32(table), self.page_size, ctypes.byref(self.geom),
+                            ctypes.byref(o), ctypes.byref(h)), "pkv_plan")
+        self._h = h
+
+    @property
+    def handle(self):
+        if self._h is None:
+            raise RuntimeError("plan destroyed")
+        return self._h
+
+    def update(self, seq_lens, block_table=None):
+        lens = _i32(seq_lens)
+        table = _i32(block_table) if block_table is not None else None
+        _check(load().pkv_plan_update(self.handle, _ptr_i32(lens), _ptr_i32(table)), "pkv_plan_update")
+
+    def info(self) -> dict:
+        info = PlanInfo()
+        _check(load().pkv_plan_get_info(self.handle, ctypes.byref(info)), "pkv_plan_get_info")
+        return info.as_dict()
+
+    def queue(self) -> np.ndarray:
+        n = ctypes.c_int32(0)
+        _check(load().pkv_plan_queue(self.handle, None, 0, ctypes.byref(n)), "pkv_plan_queue")
+        items = (WorkItem * max(n.value, 1))()
+        _check(load().pkv_plan_queue(self.handle, items, n.value, ctypes.byref(n)), "pkv_plan_queue")
+        arr = np.ctypeslib.as_array(ctypes.cast(items, _I32P), shape=(max(n.value, 1) * 5,))
+        return arr[: n.value * 5].reshape(-1, 5).copy()
+
+    def status(self, stream=None) -> int:
+        st = ctypes.c_uint32(0)
+        _check(load().pkv_status(self.handle, _stream_handle(stream), ctypes.byref(st)), "pkv_status")
+        return st.value
+
+    def read_workspace(self, stream=None):
+        n = ctypes.c_int32(0)
+        _check(load().pkv_read_workspace(self.handle, _stream_handle(stream), None, None, 0, ctypes.byref(n)),
+               "pkv_read_workspace")
+        o = np.zeros((max(n.value, 1), self.G, self.D), np.float32)
+        lse = np.zeros((max(n.value, 1), self.G), np.float32)
+        _check(load().pkv_read_workspace(self.handle, _stream_handle(stream), o.ctypes.data, lse.ctypes.data,
+                                         n.value, ctypes.byref(n)), "pkv_read_workspace")
+        return o[: n.value], lse[: n.value]
+
+    def profile(self, enable: bool = True):
+        _check(load().pkv_profile_enable(self.handle, int(enable)), "pkv_profile_enable")
+
+    def profile_read(self) -> list:
+        ms = (ctypes.c_float * 4)()
+        n = ctypes.c_int32(0)
+        _check(load().pkv_profile_read(self.handle, ms, 4, ctypes.byref(n)), "pkv_profile_read")
+        return [ms[i] for i in range(n.value)]
+
+    def close(self):
+        if getattr(self, "_h", None) is not None and _lib is not None:
+            _lib.pkv_plan_destroy(self._h)
+        self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def plan(seq_lens, block_table, page_size, **kw) -> Plan:
+    return Plan(seq_lens, block_table, page_size, **kw)
+
+
+def _dev_ptr(t, name, dtypes=None):
+    import torch
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtypes is not None and t.dtype not in dtypes:
+        raise TypeError(f"{name}: dtype {t.dtype} not in {dtypes}")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _bf16_types():
+    import torch
+    return (torch.bfloat16, torch.int16, getattr(torch, "uint16", torch.int16))
+
+
+def decode(q, k_pages, v_pages, block_table, seq_lens, plan: Plan, out, lse, stream=None):
+    """pkv_decode: out[b][h] / lse[b][h] for every row and query head."""
+    import torch
+    bf = _bf16_types()
+    rc = load().pkv_decode(_dev_ptr(q, "q", bf), _dev_ptr(k_pages, "k_pages", bf),
+                           _dev_ptr(v_pages, "v_pages", bf), _dev_ptr(block_table, "block_table", (torch.int32,)),
+                           _dev_ptr(seq_lens, "seq_lens", (torch.int32,)), plan.handle,
+                           _dev_ptr(out, "out", (torch.float32,)), _dev_ptr(lse, "lse", (torch.float32,)),
+                           _stream_handle(stream))
+    _check(rc, "pkv_decode")
+
+
+def append(k_new, v_new, k_pages, v_pages, block_table, seq_lens, plan: Plan, stream=None):
+    """pkv_append: one new K/V token per row at position seq_lens[b]; seq_lens[b] += 1."""
+    import torch
+    bf = _bf16_types()
+    rc = load().pkv_append(_dev_ptr(k_new, "k_new", bf), _dev_ptr(v_new, "v_new", bf),
+                           _dev_ptr(k_pages, "k_pages", bf), _dev_ptr(v_pages, "v_pages", bf),
+                           _dev_ptr(block_table, "block_table", (torch.int32,)),
+                           _dev_ptr(seq_lens, "seq_lens", (torch.int32,)), plan.handle, _stream_handle(stream))
+    _check(rc, "pkv_append")
+
+
+class Pool:
+    """Host FIFO page pool (pkv_pool_*)."""
+
+    def __init__(self, free_pages, num_pages: int):
+        pages = _i32(free_pages)
+        h = ctypes.c_void_p()
+        _check(load().pkv_pool_create(_ptr_i32(pages), len(pages), int(num_pages), ctypes.byref(h)),
+               "pkv_pool_create")
+        self._h = h
+
+    def reserve(self, seq_lens, block_table: np.ndarray, page_size: int) -> np.ndarray:
+        """Assigns pages in place in `block_table` (int32, C-contiguous); returns touched rows."""
+        lens = _i32(seq_lens)
+        if block_table.dtype != np.int32 or not block_table.flags.c_contiguous:
+            raise TypeError("block_table must be a C-contiguous int32 array")
+        B, max_pages = block_table.shape
+        rows = np.zeros(max(B, 1), np.int32)
+        n = ctypes.c_int32(0)
+        _check(load().pkv_pool_reserve(self._h, _ptr_i32(lens), _ptr_i32(block_table), B, max_pages,
+                                       int(page_size), _ptr_i32(rows), ctypes.byref(n)), "pkv_pool_reserve")
+        return rows[: n.value].copy()
+
+    def release(self, pages):
+        p = _i32(pages)
+        _check(load().pkv_pool_release(self._h, _ptr_i32(p), len(p)), "pkv_pool_release")
+
+    def free_count(self) -> int:
+        return int(load().pkv_pool_free_count(self._h))
+
+    def close(self):
+        if getattr(self, "_h", None) is not None and _lib is not None:
+            _lib.pkv_pool_destroy(self._h)
+        self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

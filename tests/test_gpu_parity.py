@@ -1,0 +1,187 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle.
+
+Bar: max-abs 2e-3 on out, 1e-4 on LSE; work queues bit-exact against the
+oracle's enumeration; device status word clean.  Covers every route, split
+counts, ragged and edge lengths, every supported (D, G), and the full-size
+workloads.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from paged_kv_decode_block_gb300 import pkv
+from paged_kv_decode_block_gb300 import workloads as wl
+from pkv_testutil import (assert_close, expected_queue, make_plan, oracle_result, run, to_device)
+
+pytestmark = pytest.mark.gpu
+
+ROUTES = ["direct", "split_queue", "split_padded", "persistent"]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    pkv.load()
+
+
+@pytest.mark.parametrize("route", ROUTES)
+@pytest.mark.parametrize("splits", [1, 2, 4])
+def test_tiny_every_route_and_split(route, splits):
+    p = wl.tiny()
+    ref = oracle_result(p)
+    out, lse, plan, _ = run(p, force_mode=route, num_splits=splits)
+    assert_close(out, lse, *ref, what=f"tiny {route} S={splits}")
+    info = plan.info()
+    assert info["mode_name"] == route
+    assert np.array_equal(plan.queue(), expected_queue(p, info))
+    assert plan.status() == 0
+
+
+def test_tiny_split_partials_match_oracle_partials():
+    """The partial kernel's per-tile states equal the oracle's split partials."""
+    p = wl.tiny()
+    _, _, plan, _ = run(p, force_mode="split_queue", num_splits=4)
+    o, lse = plan.read_workspace()
+    q = plan.queue()
+    for slot, (b, kvh, s, pb, pe) in enumerate(q):
+        ro, rl = oracle.partial(p.q, p.k_pages, p.v_pages, p.block_table, p.seq_lens, b, kvh,
+                                pb * p.page_size, pe * p.page_size)
+        assert np.max(np.abs(o[slot] - ro)) <= 2e-3
+        assert np.max(np.abs(lse[slot] - rl)) <= 1e-4
+
+
+EDGE_LENS = [1, 15, 16, 17, 32, 33, 0, 250]
+
+
+@pytest.mark.parametrize("route", ROUTES)
+@pytest.mark.parametrize("splits", [1, 3, 16])
+def test_edge_lengths(route, splits):
+    p = wl.make_problem("edges", EDGE_LENS, Hq=8, Hkv=2, D=128, page_size=16, num_pages=48, seed=21)
+    ref = oracle_result(p)
+    out, lse, plan, _ = run(p, force_mode=route, num_splits=splits)
+    assert_close(out, lse, *ref, what=f"edges {route} S={splits}")
+    assert np.array_equal(plan.queue(), expected_queue(p, plan.info()))
+    assert plan.status() == 0
+
+
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("G", [1, 2, 4, 8])
+def test_every_head_shape(D, G):
+    Hkv = 2
+    p = wl.make_problem(f"shape{D}x{G}", [77, 300, 16], Hq=G * Hkv, Hkv=Hkv, D=D, page_size=16,
+                        num_pages=40, seed=22)
+    ref = oracle_result(p)
+    for route, splits in [("direct", 0), ("split_queue", 5), ("persistent", 3)]:
+        out, lse, _, _ = run(p, force_mode=route, num_splits=splits)
+        assert_close(out, lse, *ref, what=f"D={D} G={G} {route}")
+
+
+@pytest.mark.parametrize("page_size", [32, 64])
+def test_larger_pages(page_size):
+    p = wl.make_problem("pages", [1, 63, 64, 65, 500], Hq=8, Hkv=2, D=128, page_size=page_size,
+                        num_pages=24, seed=23)
+    ref = oracle_result(p)
+    for route in ROUTES:
+        out, lse, _, _ = run(p, force_mode=route, num_splits=3)
+        assert_close(out, lse, *ref, what=f"ps={page_size} {route}")
+
+
+def test_all_rows_empty():
+    p = wl.make_problem("empty", [0, 0, 0], Hq=4, Hkv=1, D=64, page_size=16, num_pages=4, seed=24)
+    for route in ROUTES:
+        out, lse, _, _ = run(p, force_mode=route, num_splits=2)
+        assert np.array_equal(out, np.zeros_like(out)) and np.all(np.isneginf(lse)), route
+
+
+def test_permuted_block_table_same_result():
+    p = wl.mixed()
+    out0, lse0, _, _ = run(p, force_mode="split_queue", num_splits=8)
+    rng = np.random.default_rng(25)
+    perm = rng.permutation(p.num_pages)
+    k2 = np.empty_like(p.k_pages)
+    v2 = np.empty_like(p.v_pages)
+    k2[perm] = p.k_pages
+    v2[perm] = p.v_pages
+    t2 = np.where(p.block_table >= 0, perm[np.maximum(p.block_table, 0)], -1).astype(np.int32)
+    p2 = wl.Problem("mixed_perm", p.q, k2, v2, t2, p.seq_lens, p.page_size)
+    out1, lse1, _, _ = run(p2, force_mode="split_queue", num_splits=8)
+    assert np.array_equal(out0, out1) and np.array_equal(lse0, lse1)
+
+
+def test_deterministic_across_runs():
+    p = wl.mixed()
+    for route in ["persistent", "split_padded"]:
+        dev = to_device(p)
+        plan = make_plan(p, force_mode=route)
+        a = run(p, dev=dev, plan=plan)[:2]
+        a = (a[0].copy(), a[1].copy())
+        b = run(p, dev=dev, plan=plan)[:2]
+        assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1]), route
+
+
+def test_bad_page_id_flags_status_and_poisons():
+    """A table entry outside the pool (the planner is not shown the table) is caught in
+    the kernel: status bit set, output NaN, no access through the bad id."""
+    p = wl.tiny()
+    bad = p.block_table.copy()
+    bad[1, 2] = p.num_pages + 5
+    p_bad = wl.Problem("bad", p.q, p.k_pages, p.v_pages, bad, p.seq_lens, p.page_size)
+    for route in ROUTES:
+        out, lse, plan, _ = run(p_bad, host_table=False, force_mode=route, num_splits=2)
+        assert plan.status() & pkv.DEV_PAGE_OOB, route
+        assert np.all(np.isnan(out[1])), route
+        assert np.all(np.isfinite(out[0])), route
+
+
+def test_plan_mismatch_is_detected():
+    p = wl.tiny()
+    plan = make_plan(p, force_mode="split_queue", num_splits=2)
+    dev = to_device(p)
+    dev["lens"] = torch.tensor([37, 60], dtype=torch.int32, device="cuda")   # not what was planned
+    pkv.decode(dev["q"], dev["k"], dev["v"], dev["table"], dev["lens"], plan, dev["out"], dev["lse"])
+    assert plan.status() & pkv.DEV_PLAN_MISMATCH
+
+
+def test_host_validation_errors():
+    p = wl.tiny()
+    bad = p.block_table.copy()
+    bad[0, 1] = -3
+    with pytest.raises(pkv.PkvError) as e:
+        make_plan(wl.Problem("b", p.q, p.k_pages, p.v_pages, bad, p.seq_lens, p.page_size))
+    assert e.value.code == pkv.EINVAL
+
+
+# --- the full-size workloads ---------------------------------------------------------
+
+@pytest.mark.parametrize("route", ["split_queue", "persistent"])
+def test_batch1_long_32k(route):
+    p = wl.batch1_long()
+    ref = oracle_result(p, nthreads=16)
+    out, lse, plan, _ = run(p, force_mode=route, num_splits=32)
+    assert_close(out, lse, *ref, what=f"batch1_long {route}")
+    info = plan.info()
+    assert info["chunk_pages"] == 64 and info["num_work_items"] == 256
+    assert np.array_equal(plan.queue(), expected_queue(p, info))
+    assert plan.status() == 0
+
+
+@pytest.mark.parametrize("route", ["split_queue", "split_padded", "persistent", "auto"])
+def test_mixed_batch(route):
+    p = wl.mixed()
+    ref = oracle_result(p, nthreads=16)
+    out, lse, plan, _ = run(p, force_mode=route)
+    assert_close(out, lse, *ref, what=f"mixed {route}")
+    assert np.array_equal(plan.queue(), expected_queue(p, plan.info()))
+    assert plan.status() == 0
+
+
+def test_high_batch_policy_chooses_direct():
+    p = wl.high_batch()
+    ref = oracle_result(p, nthreads=16)
+    out, lse, plan, _ = run(p)
+    assert plan.info()["mode_name"] == "direct"
+    assert plan.info()["launches_per_step"] == 1
+    assert_close(out, lse, *ref, what="high_batch")
+    assert plan.status() == 0
