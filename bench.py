@@ -1,0 +1,410 @@
+"""Benchmark: paged GQA decode attention on one GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl pkv|reference]
+
+Default workload: batch-1 long context (1 x 32768 tokens, 32 query / 8 KV heads,
+D 128, 16-token pages scattered over a 4096-page pool, 32 splits).  One step is
+one pkv_decode: the split-partial kernel over the compact queue plus the LSE
+merge kernel.  Metric: KV-read GB/s (KV bytes of the step / device time of the
+step) and µs per step; roofline fraction against the measured HBM copy
+bandwidth.
+
+Timing rules: parity against the fp64 oracle before any timing; W >= 3 warm-up
+steps; L2 flushed (a 2 x L2-size buffer written) before every timed step; each
+step timed with CUDA events on the launching stream; clocks sampled with
+nvidia-smi during the timed region.  Multi-GPU (torchrun, one rank per GPU)
+runs independent replicas of the workload, partitioned by sequence: no
+collective on the data path, a barrier and max-over-ranks timing only.
+
+--impl reference times the fp64 CPU oracle on the host cores on the same
+workload and metric (a bounded sample per step).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "decode-attention µs/step and KV-read GB/s (fraction of GB300 HBM peak)"
+FALLBACK_HBM_GBS = 6800.0
+NOMINAL_HBM_GBS = 7900.0
+PROFILE_DIR = os.path.join(ROOT, "profiles")
+KERNEL_SOURCE = os.path.join(ROOT, "paged_kv_decode_block_gb300", "csrc", "pkv_attention.cu")
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash() -> str:
+    with open(KERNEL_SOURCE, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def profiled_traffic(workload: str):
+    """DRAM bytes per launch of the attention kernel from the committed ncu summary,
+    if it was taken on the current kernel source; else None."""
+    path = os.path.join(PROFILE_DIR, f"attention_{workload}.md")
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
+    m_src = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]{16})", text)
+    m_bytes = re.search(r"dram_bytes_per_launch:\s*([0-9]+)", text)
+    if not m_src or not m_bytes or m_src.group(1) != kernel_source_hash():
+        return None
+    return int(m_bytes.group(1))
+
+
+def smi_index(local: int) -> int:
+    """nvidia-smi index of this rank's GPU (CUDA_VISIBLE_DEVICES may remap it)."""
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+    parts = [x.strip() for x in vis.split(",") if x.strip()]
+    if local < len(parts) and parts[local].isdigit():
+        return int(parts[local])
+    return local
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms in the background."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- workloads
+
+def build_workload(name: str):
+    from paged_kv_decode_block_gb300 import workloads as wl
+    makers = {"batch1_long": (wl.batch1_long, dict(force_mode="split_queue", num_splits=32)),
+              "mixed": (wl.mixed, dict(force_mode="split_queue")),
+              "mixed_padded": (wl.mixed, dict(force_mode="split_padded")),
+              "high_batch": (wl.high_batch, dict()),
+              "tiny": (wl.tiny, dict(force_mode="split_queue", num_splits=4)),
+              "continuous": (wl.continuous, dict(force_mode="persistent", num_splits=1))}
+    make, opts = makers[name]
+    return make(), opts
+
+
+def parity_gate(p, out, lse, nthreads):
+    import oracle
+    ref_out, ref_lse = oracle.decode(p.q, p.k_pages, p.v_pages, p.block_table, p.seq_lens, nthreads=nthreads)
+    err_out = float(np.max(np.abs(out - ref_out)))
+    fin = np.isfinite(ref_lse)
+    err_lse = float(np.max(np.abs(lse[fin] - ref_lse[fin]))) if fin.any() else 0.0
+    ok = err_out <= 2e-3 and err_lse <= 1e-4 and np.array_equal(np.isneginf(lse), np.isneginf(ref_lse))
+    return ok, err_out, err_lse
+
+
+def host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def time_oracle(p, budget_s: float, nthreads: int):
+    """Run full oracle steps until `budget_s` has passed (at least one); seconds per step."""
+    import oracle
+    oracle.load()
+    n, t0 = 0, time.perf_counter()
+    while True:
+        oracle.decode(p.q, p.k_pages, p.v_pages, p.block_table, p.seq_lens, nthreads=nthreads)
+        n += 1
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    return (time.perf_counter() - t0) / n, n
+
+
+# ----------------------------------------------------------------------------- our arm
+
+def run_pkv(args):
+    import torch
+    import torch.distributed as dist
+    from paged_kv_decode_block_gb300 import pkv
+
+    rank, world, local = dist_env()
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pkv.load()
+
+    p, opts = build_workload(args.workload)
+    opts = dict(opts, math=args.math, separate_merge=args.separate_merge, copy=args.copy)
+    q = torch.from_numpy(p.q.view(np.int16)).to(dev)
+    k = torch.from_numpy(p.k_pages.view(np.int16)).to(dev)
+    v = torch.from_numpy(p.v_pages.view(np.int16)).to(dev)
+    table = torch.from_numpy(p.block_table).to(dev)
+    lens = torch.from_numpy(p.seq_lens).to(dev)
+    out = torch.empty((p.B, p.Hq, p.D), dtype=torch.float32, device=dev)
+    lse = torch.empty((p.B, p.Hq), dtype=torch.float32, device=dev)
+    plan = pkv.Plan(p.seq_lens, p.block_table, p.page_size, B=p.B, Hq=p.Hq, Hkv=p.Hkv, D=p.D,
+                    max_pages=p.max_pages, num_pages=p.num_pages, **opts)
+    info = plan.info()
+    stream = torch.cuda.current_stream()
+
+    # correctness gate before any timing
+    pkv.decode(q, k, v, table, lens, plan, out, lse)
+    torch.cuda.synchronize()
+    if plan.status() != 0:
+        raise SystemExit("device status word set on the parity run")
+    ok, err_out, err_lse = parity_gate(p, out.cpu().numpy(), lse.cpu().numpy(), host_cores())
+    log(f"parity vs oracle: max|out|={err_out:.3g} max|lse|={err_lse:.3g} -> {'ok' if ok else 'FAIL'}")
+    if not ok:
+        raise SystemExit("parity gate failed; not timing")
+
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
+    plan.profile(True)
+    for _ in range(args.warmup):
+        flush.zero_()
+        pkv.decode(q, k, v, table, lens, plan, out, lse)
+    torch.cuda.synchronize()
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    kernel_ms = []
+    with ClockSampler(smi_index(local)) as clk:
+        time.sleep(0.3)
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        t_wall0 = time.perf_counter()
+        for i in range(args.steps):
+            flush.zero_()
+            starts[i].record(stream)
+            pkv.decode(q, k, v, table, lens, plan, out, lse)
+            ends[i].record(stream)
+            kernel_ms.append(plan.profile_read())   # waits for this step's kernels
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        t_wall = time.perf_counter() - t_wall0
+        time.sleep(0.3)
+    plan.profile(False)
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    med_ms = statistics.median(step_ms)
+    attn_ms = statistics.mean(km[0] for km in kernel_ms)
+    merge_ms = statistics.mean(km[1] for km in kernel_ms) if info["launches_per_step"] > 1 else 0.0
+
+    if world > 1:
+        t = torch.tensor([med_ms, attn_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        med_ms, attn_ms = float(t[0]), float(t[1])
+
+    kv = info["kv_bytes"]
+    q_bytes = p.B * p.Hq * p.D * 2
+    o_bytes = p.B * p.Hq * (p.D + 1) * 4
+    alg_bytes_attn = kv + q_bytes   # what the attention kernel must read
+    value = kv * world / (med_ms * 1e-3) / 1e9
+    peak, peak_src = hbm_peak()
+    achieved = alg_bytes_attn / (attn_ms * 1e-3) / 1e9
+
+    # end to end through the public API with host buffers: q H2D (pinned), host re-plan
+    # and queue upload, decode, out + lse D2H; wall time per step
+    q_host = torch.from_numpy(p.q.view(np.int16)).pin_memory()
+    out_host = torch.empty(out.shape, dtype=torch.float32).pin_memory()
+    lse_host = torch.empty(lse.shape, dtype=torch.float32).pin_memory()
+    e2e_s = []
+    for i in range(args.warmup + args.steps):
+        flush.zero_()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        q.copy_(q_host, non_blocking=True)
+        plan.update(p.seq_lens)
+        pkv.decode(q, k, v, table, lens, plan, out, lse)
+        out_host.copy_(out, non_blocking=True)
+        lse_host.copy_(lse, non_blocking=True)
+        torch.cuda.synchronize()
+        if i >= args.warmup:
+            e2e_s.append(time.perf_counter() - t0)
+    e2e_med = statistics.median(e2e_s)
+    upload = 4 * (5 * info["num_work_items"] + 2 * p.B) if info["mode"] != pkv.MODE_DIRECT else 0
+    if world > 1:
+        t = torch.tensor([e2e_med], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_med = float(t[0])
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.skip_cpu:
+        cores = host_cores()
+        sec, n = time_oracle(p, args.cpu_budget, cores)
+        cpu = {"value": round(kv / sec / 1e9, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+               "sample": f"{n} full oracle decode step(s) of the same workload (fp64 C, {cores} threads), "
+                         f"{sec * 1e3:.0f} ms per step"}
+
+    clocks = clk.summary()
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(med_ms, 5),
+        "us_per_step": round(med_ms * 1e3, 2), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16 in, fp32 accumulate", "data": "synthetic (seeded, bf16 ~N(0,1))",
+        "config": {"workload": p.name, "batch": p.B, "seq_lens": "32768" if args.workload == "batch1_long"
+                   else f"sum {int(p.seq_lens.sum())}", "q_heads": p.Hq, "kv_heads": p.Hkv,
+                   "head_dim": p.D, "page_size": p.page_size, "num_pages": p.num_pages,
+                   "mode": info["mode_name"], "math": args.math, "copy": args.copy,
+                   "num_splits": info["max_splits"],
+                   "chunk_pages": info["chunk_pages"], "tiles": info["num_work_items"],
+                   "launches_per_step": info["launches_per_step"],
+                   "l2": "flushed before every timed step (2 x L2 bytes written)",
+                   "parallelism": f"replicas x{world} (partition by sequence, no collective)"},
+        "kv_bytes_per_step": kv,
+        "frac_of_nominal_7_9TBs": round(value / NOMINAL_HBM_GBS, 4),
+        "kernel_ms": {"attention": round(attn_ms, 5), "merge": round(merge_ms, 5)},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "peak_source": peak_src,
+                     "kernel": "attention_kernel (split partial over the compact queue)",
+                     "algorithmic_bytes_per_launch": alg_bytes_attn,
+                     "traffic": profiled_traffic(args.workload)},
+        "e2e": {"value": round(kv * world / e2e_med / 1e9, 2), "unit": "GB/s",
+                "us_per_step": round(e2e_med * 1e6, 2), "h2d_bytes_per_step": q_bytes + upload,
+                "d2h_bytes_per_step": o_bytes},
+        "gpu_launches": info["launches_per_step"] * args.steps,
+        "cpu_baseline": cpu,
+        "clocks": {"sm_mhz": clocks["sm_mhz"], "sm_max_mhz": clocks["sm_max_mhz"],
+                   "reasons": clocks["reasons"], "samples": clocks["samples"]},
+        "timed_region_wall_s": round(t_wall, 4),
+        "parity": {"max_abs_out": err_out, "max_abs_lse": err_lse},
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+# ----------------------------------------------------------------------------- reference arm
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    p, _ = build_workload(args.workload)
+    kv = p.kv_bytes()
+    cores = host_cores()
+    budget = max(1.0, args.cpu_budget / max(1, args.steps + args.warmup))
+    for _ in range(args.warmup):
+        time_oracle(p, 0.0, cores)
+    per_step = []
+    for _ in range(args.steps):
+        sec, _n = time_oracle(p, budget, cores)
+        per_step.append(sec)
+    sec = statistics.median(per_step)
+    value = kv / sec / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(sec * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded, bf16 ~N(0,1))",
+        "config": {"workload": p.name, "batch": p.B, "q_heads": p.Hq, "kv_heads": p.Hkv, "head_dim": p.D,
+                   "page_size": p.page_size},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+                         "sample": f"each step = full oracle decode of the workload, repeated for ~{budget:.1f} s"},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--workload", default="batch1_long",
+                    choices=["batch1_long", "mixed", "mixed_padded", "high_batch", "tiny"])
+    ap.add_argument("--impl", default="pkv", choices=["pkv", "reference"])
+    ap.add_argument("--math", default="auto", choices=["auto", "fma", "mma"],
+                    help="block reduction: tensor cores (mma.sync) or CUDA-core FMA")
+    ap.add_argument("--separate-merge", action="store_true", help="merge splits in a second launch")
+    ap.add_argument("--copy", default="auto", choices=["auto", "lsu", "tma"],
+                    help="K/V staging: cp.async from the producer warp, or TMA boxes")
+    ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time for the CPU baseline")
+    ap.add_argument("--skip-cpu", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_pkv(args)
+
+
+if __name__ == "__main__":
+    main()

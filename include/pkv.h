@@ -85,9 +85,9 @@ enum pkv_device_status_bits {
 enum pkv_mode {
     PKV_MODE_AUTO = 0,          /* let the policy choose */
     PKV_MODE_DIRECT = 1,        /* one CTA per (row, KV head); no split, no merge */
-    PKV_MODE_SPLIT_QUEUE = 2,   /* partial kernel over the compact queue + merge kernel */
-    PKV_MODE_SPLIT_PADDED = 3,  /* partial kernel over the padded B*Hkv*S_max grid + merge */
-    PKV_MODE_PERSISTENT = 4     /* SM-sized grid drains the compact queue; fused merge */
+    PKV_MODE_SPLIT_QUEUE = 2,   /* one CTA per compact-queue tile; exact LSE merge of splits */
+    PKV_MODE_SPLIT_PADDED = 3,  /* one CTA per slot of the padded B*Hkv*S_max grid; merge */
+    PKV_MODE_PERSISTENT = 4     /* SM-sized grid drains the compact queue; merge */
 };
 
 typedef struct {
@@ -108,9 +108,26 @@ typedef struct {
     int32_t target_ctas_per_sm;  /* policy: aim for this many tiles per SM (default 2) */
     int32_t min_chunk_pages;     /* policy: smallest split chunk in pages (default 8) */
     int32_t ctas_per_sm;         /* persistent grid = SMs * this (default: occupancy) */
-    int32_t separate_merge;      /* persistent: 1 = merge in its own launch, 0 = fused */
+    int32_t separate_merge;      /* split routes: 1 = merge in its own launch, 0 = the last
+                                    arriving split of each (row, KV head) merges (default) */
     int32_t num_sms;             /* SM count to plan for (default: current device) */
+    int32_t math;                /* pkv_math: block reduction on tensor cores or CUDA cores */
+    int32_t copy;                /* pkv_copy: how K/V pages reach shared memory */
 } pkv_plan_opts;
+
+/* How the producer warp moves K/V blocks into shared memory. */
+enum pkv_copy {
+    PKV_COPY_AUTO = 0,   /* cp.async */
+    PKV_COPY_LSU = 1,    /* cp.async 16-byte copies issued by all 32 producer lanes */
+    PKV_COPY_TMA = 2     /* cp.async.bulk.tensor boxes of 16 tokens x 64 elements */
+};
+
+/* How a 16-token block is reduced (results agree to the stated tolerances). */
+enum pkv_math {
+    PKV_MATH_AUTO = 0,   /* tensor cores */
+    PKV_MATH_FMA = 1,    /* fp32 FMA on CUDA cores */
+    PKV_MATH_MMA = 2     /* mma.sync bf16 x bf16 -> fp32, P split into bf16 hi + lo */
+};
 
 /* One work tile: KV head `kvh` of row `b`, split `split`, pages
  * [page_begin, page_end) of the row (end exclusive). 20 bytes. */

@@ -59,6 +59,8 @@ struct Options {
     int ctas_per_sm = 0;
     int separate_merge = 0;
     int num_sms = 0;
+    int math = PKV_MATH_AUTO;
+    int copy = PKV_COPY_AUTO;
 };
 
 int resolve_options(const pkv_plan_opts* o, Options* r) {
@@ -66,8 +68,11 @@ int resolve_options(const pkv_plan_opts* o, Options* r) {
     if (o->force_mode < PKV_MODE_AUTO || o->force_mode > PKV_MODE_PERSISTENT) return PKV_EINVAL;
     if (o->num_splits < 0 || o->direct_units_per_sm < 0 || o->target_ctas_per_sm < 0 ||
         o->min_chunk_pages < 0 || o->ctas_per_sm < 0 || o->num_sms < 0 || o->separate_merge < 0 ||
-        o->separate_merge > 1)
+        o->separate_merge > 1 || o->math < PKV_MATH_AUTO || o->math > PKV_MATH_MMA || o->copy < PKV_COPY_AUTO ||
+        o->copy > PKV_COPY_TMA)
         return PKV_EINVAL;
+    r->math = o->math;
+    r->copy = o->copy;
     r->force_mode = o->force_mode;
     r->num_splits = o->num_splits;
     if (o->direct_units_per_sm) r->direct_units_per_sm = o->direct_units_per_sm;
@@ -149,6 +154,8 @@ int compute_plan(const pkv_geom& g, int32_t ps, const int32_t* lens, const Optio
     else
         chunk = policy_chunk();
     chunk = std::max<int64_t>(chunk, 1);
+    // an exact merge holds all splits of one (row, KV head) in shared memory
+    chunk = std::max<int64_t>(chunk, ceil_div(p_max, pkv::kMergeCapFloats / G));
     if (mode == PKV_MODE_AUTO) mode = chunk >= p_max ? PKV_MODE_DIRECT : PKV_MODE_SPLIT_QUEUE;
     if (mode == PKV_MODE_DIRECT) chunk = std::max<int64_t>(p_max, 1);
 
@@ -170,6 +177,7 @@ int compute_plan(const pkv_geom& g, int32_t ps, const int32_t* lens, const Optio
         r->grid = B * Hkv;
         r->ws_slots = 0;
     } else if (mode == PKV_MODE_SPLIT_PADDED) {
+        r->s_max = std::max(r->s_max, 1);   // an all-empty batch still gets one (neutral) slot per row
         for (int b = 0; b < B; ++b) {
             r->row_start[b] = b * Hkv * r->s_max;
             r->row_splits[b] = r->s_max;
@@ -183,8 +191,8 @@ int compute_plan(const pkv_geom& g, int32_t ps, const int32_t* lens, const Optio
         }
         r->grid = B * Hkv * r->s_max;
         r->ws_slots = r->grid;
-        r->need_merge = r->s_max != 1;
-        if (r->need_merge) merged_slots = r->grid;
+        r->need_merge = o.separate_merge && r->s_max != 1;
+        if (r->s_max != 1) merged_slots = r->grid;
     } else {   // compact queue: SPLIT_QUEUE and PERSISTENT
         int32_t slot = 0;
         bool any_unfinished = false;
@@ -202,15 +210,13 @@ int compute_plan(const pkv_geom& g, int32_t ps, const int32_t* lens, const Optio
         }
         r->ws_slots = slot;
         const int32_t T = static_cast<int32_t>(r->items.size());
-        if (mode == PKV_MODE_SPLIT_QUEUE) {
-            r->grid = T;
-            r->need_merge = any_unfinished;
-        } else {
+        // rows with no tokens have no tiles; the attention kernel writes their
+        // neutral state (a fused merge) or the merge kernel does (separate)
+        if (mode == PKV_MODE_SPLIT_QUEUE)
+            r->grid = B > 0 ? std::max<int32_t>(T, 1) : 0;
+        else
             r->grid = B > 0 ? std::max(1, std::min<int32_t>(T, num_sms * std::max(1, ctas_per_sm))) : 0;
-            bool any_split = false;
-            for (int b = 0; b < B; ++b) any_split |= r->row_splits[b] > 1;
-            r->need_merge = o.separate_merge && any_split;
-        }
+        r->need_merge = o.separate_merge && any_unfinished;
     }
     r->ws_bytes = merged_slots * G * (D + 1) * 4 * 2;   // written once, read once
     return PKV_OK;
@@ -256,8 +262,9 @@ EncodeTiledFn encode_fn() {
 }
 
 // The pool [num_pages][page_size][Hkv][D] bf16 as a 3-D tensor
-// {D, Hkv, num_pages * page_size} (innermost first); one box is kBlockRows
-// consecutive tokens of one KV head.
+// {D, Hkv, num_pages * page_size} (innermost first); one box is 64 elements
+// (128 B) of kBlockRows consecutive tokens of one KV head, stored with the
+// 128-byte swizzle the kernels' shared-memory addressing expects.
 int encode_pool_map(CUtensorMap* map, const void* pool, const pkv_geom& g, int32_t page_size) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return cuda_fail(cudaErrorNotSupported);
@@ -265,10 +272,10 @@ int encode_pool_map(CUtensorMap* map, const void* pool, const pkv_geom& g, int32
                                 static_cast<cuuint64_t>(g.num_pages) * page_size};
     const cuuint64_t strides[2] = {static_cast<cuuint64_t>(g.head_dim) * 2,
                                    static_cast<cuuint64_t>(g.num_kv_heads) * g.head_dim * 2};
-    const cuuint32_t box[3] = {static_cast<cuuint32_t>(g.head_dim), 1u, static_cast<cuuint32_t>(pkv::kBlockRows)};
+    const cuuint32_t box[3] = {64u, 1u, static_cast<cuuint32_t>(pkv::kBlockRows)};   // 128 B x 16 tokens
     const cuuint32_t estr[3] = {1u, 1u, 1u};
     CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(pool), dims, strides, box, estr,
-                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return cuda_fail(cudaErrorInvalidValue);
     return PKV_OK;
@@ -434,7 +441,9 @@ int pkv_plan(const int32_t* seq_lens_h, const int32_t* block_table_h, int32_t pa
     }
     if (o.num_sms > 0) p->num_sms = o.num_sms;
     const int G = geom->num_q_heads / geom->num_kv_heads;
-    p->ctas_per_sm = o.ctas_per_sm > 0 ? o.ctas_per_sm : std::max(1, pkv::attention_ctas_per_sm(geom->head_dim, G));
+    p->ctas_per_sm = o.ctas_per_sm > 0 ? o.ctas_per_sm
+                                       : std::max(1, pkv::attention_ctas_per_sm(geom->head_dim, G,
+                                                                                o.math != PKV_MATH_FMA));
 
     if ((rc = compute_plan(p->g, page_size, seq_lens_h, o, p->num_sms, p->ctas_per_sm, &p->plan))) {
         delete p;
@@ -541,6 +550,10 @@ int pkv_decode(const void* q, const void* k_pages, const void* v_pages, const in
     a.max_splits = pl.s_max;
     a.num_tiles = static_cast<int32_t>(pl.items.size());
     a.fused_merge = p->opts.separate_merge ? 0 : 1;
+    a.use_mma = p->opts.math != PKV_MATH_FMA;
+    a.copy_lsu = p->opts.copy != PKV_COPY_TMA;
+    a.k_pages = static_cast<const uint16_t*>(k_pages);
+    a.v_pages = static_cast<const uint16_t*>(v_pages);
     a.scale_log2 = static_cast<float>(1.4426950408889634 / sqrt(static_cast<double>(p->g.head_dim)));
     switch (pl.mode) {
         case PKV_MODE_DIRECT: a.route = pkv::kRouteDirect; break;

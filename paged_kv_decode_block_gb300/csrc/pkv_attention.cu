@@ -6,7 +6,7 @@
 //   * one pass over a KV head serves its whole group of G = Hq/Hkv query heads;
 //   * K and V are read in place through the block table ("Layout");
 //   * a split computes the partial online-softmax state of a disjoint page
-//     range and a merge step combines the states exactly ("Sequence Splitting");
+//     range and a merge combines the states exactly ("Sequence Splitting");
 //   * split ranges follow the row's true length; an empty split writes the
 //     neutral state and reads no KV ("Row-Local Bounds");
 //   * tiles come from a compact queue of non-empty (row, KV head, split)
@@ -16,29 +16,37 @@
 // Executor"), with the grid sized to the SM count as in "WPK persistent kernel"
 // (dotwave.ai, "What a persistent kernel is").
 //
-// GB300 design.  Decode attention reads every KV byte once and does about two
-// fp32 FMAs per byte (G = 4), far below the tensor-core balance, so the kernel
-// is built for HBM bandwidth on CUDA cores:
-//   * one CTA per tile: 4 consumer warps + 1 producer warp;
-//   * the producer resolves the block table (32 entries per coalesced load,
-//     prefetched one batch ahead) and streams 16-token blocks of K and V into a
-//     ring of shared-memory stages with TMA (cp.async.bulk.tensor, L2
+// GB300 design.  The kernel streams every KV byte once from HBM:
+//   * one CTA per tile: 4 consumer warps + 2 producer warps;
+//   * the producers resolve the block table (32 entries per coalesced load,
+//     prefetched one batch ahead) and stream 16-token blocks of K and V into
+//     a ring of 10-16 shared-memory stages (about 80-96 KB per CTA, two CTAs
+//     per SM) with TMA (cp.async.bulk.tensor, 128-byte swizzle, L2
 //     evict-first), completion tracked by mbarriers;
-//   * each consumer warp owns every 4th block and keeps its own online-softmax
-//     state (running max m, sum l, fp32 accumulator), so the loop has no
-//     CTA-wide barrier; the four states are merged with the same exact LSE rule
-//     at the end of the tile;
-//   * inside a warp, D/8 lanes cover one 16-byte slice each of a K row; the G
-//     partial dot products are summed with a transposing butterfly (each
-//     exchange halves the values a lane holds), so a row costs log2(D/8)
-//     shuffles per lane instead of G * log2(D/8);
-//   * scores are kept in the log2 domain (q pre-scaled by log2(e)/sqrt(D));
-//     exp2f is CUDA's own function; everything accumulates in fp32.
+//   * each consumer warp owns every 4th block and keeps a private
+//     online-softmax state (running max, sum, fp32 accumulator), so the loop has
+//     no CTA-wide barrier; the four states are merged with the exact LSE rule at
+//     the end of the tile;
+//   * two interchangeable block reductions (template MMA):
+//       - FMA: CUDA cores; D/8 lanes cover a K row in 16-byte slices and the G
+//         dot products are summed by a transposing butterfly;
+//       - MMA: warp-level mma.sync m16n8k16 bf16 with fp32 accumulation for
+//         S^T = K Q^T (16 tokens x the query group, padded to 8 columns) and for
+//         O^T += V^T P^T.  P (in [0,1]) is split into bf16 hi + lo parts that
+//         ride in the padding columns (or a second column tile when G = 8), so
+//         P V keeps about 16 mantissa bits; K and V come from shared memory with
+//         ldmatrix (conflict-free under the swizzle) straight into registers,
+//         and the stage is released before any arithmetic, so stages are held
+//         only briefly and the ring stays full of loads in flight.  This also
+//         cuts the issued instructions per block about six-fold against FMA;
+//   * scores stay in the log2 domain (scale log2(e)/sqrt(D) applied in fp32);
+//     exp2f is CUDA's own function; all accumulation is fp32.
 // Every wait on an mbarrier is bounded (kWaitLimitNs): on expiry the kernel
-// sets PKV_DEV_TIMEOUT in the status word, poisons the tile and carries on.
-// Bad page ids set PKV_DEV_PAGE_OOB and poison the tile; no access is made
-// through them.
+// sets PKV_DEV_TIMEOUT, poisons the tile, stops waiting and drains its own
+// copies before exit.  Bad page ids set PKV_DEV_PAGE_OOB and poison the tile;
+// no access is made through them.
 #include <cuda.h>
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stdint.h>
@@ -49,10 +57,11 @@ namespace pkv {
 namespace {
 
 constexpr int kConsumerWarps = 4;
-constexpr int kThreads = (kConsumerWarps + 1) * 32;
-constexpr int kStages = 8;
+constexpr int kProducerWarps = 2;   // block j is staged by producer warp j % kProducerWarps
+constexpr int kThreads = (kConsumerWarps + kProducerWarps) * 32;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 constexpr unsigned kFull = 0xffffffffu;
+constexpr float kLn2 = 0.69314718055994530942f;
 
 // ------------------------------------------------------------------ PTX helpers
 
@@ -66,6 +75,10 @@ __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
 
 __device__ __forceinline__ void fence_mbar_init() {
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_shared() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
@@ -134,8 +147,65 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, i
         : "memory");
 }
 
+// Non-tensor bulk copy global -> shared (16-byte aligned, size a multiple of 16),
+// completing on `bar`.
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_addr(dst)),
+        "l"(src), "r"(bytes), "r"(smem_addr(bar))
+        : "memory");
+}
+
+// Order this thread's view of global data written through the generic proxy
+// (other CTAs' plain stores) before its own async-proxy (bulk copy) reads.
+__device__ __forceinline__ void fence_proxy_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+// 16-byte asynchronous global -> shared copy through L2 only, with an L2 policy.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint64_t policy) {
+    asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "l"(policy)
+                 : "memory");
+}
+
+// Arrive on `bar` once every cp.async this thread has issued so far has landed
+// (the arrival counts against the barrier's expected count).
+__device__ __forceinline__ void cp_async_arrive_noinc(uint64_t* bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
 __device__ __forceinline__ void named_barrier_sync(int id, int threads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], uint32_t addr) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr)
+                 : "memory");
+}
+
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t (&r)[4], uint32_t addr) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr)
+                 : "memory");
+}
+
+__device__ __forceinline__ void ldsm_x2(uint32_t (&r)[2], uint32_t addr) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0, %1}, [%2];"
+                 : "=r"(r[0]), "=r"(r[1])
+                 : "r"(addr)
+                 : "memory");
+}
+
+// D (16x8 fp32) += A (16x16 bf16, row-major) * B (16x8 bf16, column-major)
+__device__ __forceinline__ void mma_16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
 // 8 packed bf16 (one 16-byte vector) -> 8 floats.  bf16 is the top half of an
@@ -147,6 +217,14 @@ __device__ __forceinline__ void unpack_bf16x8(const uint4& raw, float (&f)[8]) {
         f[2 * i] = __uint_as_float(w[i] << 16);
         f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
     }
+}
+
+// Byte offset, inside one K or V stage, of the 16-byte chunk holding token
+// row's elements [d, d + 8) (d a multiple of 8).  A stage holds D/64 halves of
+// [16 rows][128 B]; TMA's 128-byte swizzle stores chunk c of row r at chunk
+// c ^ (r % 8), so 8 rows read at one chunk index hit 8 distinct bank groups.
+__device__ __forceinline__ uint32_t swz(int row, int d) {
+    return static_cast<uint32_t>((d >> 6) * (kBlockRows * 128) + row * 128 + ((((d & 63) >> 3) ^ (row & 7)) << 4));
 }
 
 // Transposing butterfly over the lanes of one row group.  Starting from N
@@ -180,32 +258,49 @@ struct Butterfly {
 
 template <int D, int G>
 struct Cfg {
+    // FMA form
     static constexpr int L = D / 8;                 // lanes per K/V row (16 B each)
     static constexpr int R = 32 / L;                // rows per warp step
     static constexpr int kSteps = kBlockRows / R;   // warp steps per 16-row block
     static constexpr int HG = L / G;                // lanes holding the same head
-    static constexpr int kStageElems = kBlockRows * D;
-    static constexpr uint32_t kStageBytes = 2u * kStageElems * 2u;  // K + V
+    // both forms
+    static constexpr int kMatBytes = kBlockRows * D * 2;            // one K or V stage
+    static constexpr uint32_t kStageBytes = 2u * kMatBytes;         // K + V
+    // MMA form: P^T column tiles (hi and lo parts share one tile while 2G <= 8)
+    static constexpr int NPV = (2 * G <= 8) ? 1 : 2;
+    // Ring depth: about 80-96 KB of K/V in flight per CTA, two CTAs per SM.
+    static constexpr int kStages = D == 128 ? (G == 8 ? 10 : 12) : 16;
     static_assert(D == 64 || D == 128, "head_dim");
-    static_assert(G >= 1 && G <= L, "group size");
+    static_assert(G >= 1 && G <= 8 && G <= L, "group size");
 };
 
 template <int D, int G>
-struct __align__(128) Smem {
-    uint16_t k[kStages][kBlockRows * D];
-    uint16_t v[kStages][kBlockRows * D];
-    float p[kConsumerWarps][kBlockRows * G];   // softmax weights of the block being reduced
+struct Smem {
+    static constexpr int kStages = Cfg<D, G>::kStages;
+    alignas(1024) uint8_t k[kStages][Cfg<D, G>::kMatBytes];
+    alignas(1024) uint8_t v[kStages][Cfg<D, G>::kMatBytes];
+    alignas(16) uint16_t pt[kConsumerWarps][Cfg<D, G>::NPV * 2 * 8 * 8];   // P^T tiles, bf16 (MMA form)
+    float p[kConsumerWarps][kBlockRows * G];   // softmax weights of the block (FMA form)
     float acc[kConsumerWarps][G * D];          // per-warp states for the end-of-tile merge
     float m[kConsumerWarps][G];
     float l[kConsumerWarps][G];
+    float merge_m[G], merge_inv[G];
+    int merge_nan;
     int poisoned[kConsumerWarps];
     int bad[kStages];
     uint32_t issued[kStages];   // 1 + use index of the last TMA issued into each stage
     int abort;                  // a wait of this CTA ran out: stop waiting, drain, finish
     uint64_t full[kStages];
     uint64_t empty[kStages];
+    uint64_t merge_bar;         // completion of the fused merge's bulk copies
+    uint32_t merge_phase;       // phases of merge_bar used so far
     int tile_slot[2];
 };
+
+template <int D, int G>
+constexpr size_t smem_bytes() {
+    return sizeof(Smem<D, G>) + 1024;   // + room to align the base to 1024 B
+}
 
 struct TileWork {
     int b, kvh;
@@ -215,13 +310,39 @@ struct TileWork {
     int poisoned;      // plan and device lengths disagree
 };
 
-// ------------------------------------------------------------------ tile body
+// ------------------------------------------------------------------ FMA block reduction
 
 template <int D, int G>
-__device__ __forceinline__ void consume_block(const uint16_t* __restrict__ ks, const uint16_t* __restrict__ vs,
-                                              float* __restrict__ ps, int valid, int lane,
-                                              const float (&qf)[G][8], float (&m)[G], float (&l)[G],
-                                              float& m_mine, float (&acc)[G][8]) {
+struct FmaState {
+    float qf[G][8];    // this lane's 8-element slice of every query head, pre-scaled
+    float m[G], l[G];  // running max / sum (log2 domain), warp-uniform
+    float m_mine;      // running max of the head this lane reduces
+    float acc[G][8];   // this lane's slice of the unnormalised output
+};
+
+template <int D, int G>
+__device__ __forceinline__ void fma_init(FmaState<D, G>& st, const AttnParams& p, const TileWork& tw, int lane) {
+    using C = Cfg<D, G>;
+    const int sub = lane % C::L;
+    const uint16_t* qrow = p.q + (static_cast<size_t>(tw.b) * p.Hq + tw.kvh * G) * D + sub * 8;
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+        const uint4 raw = __ldg(reinterpret_cast<const uint4*>(qrow + g * D));
+        unpack_bf16x8(raw, st.qf[g]);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            st.qf[g][e] *= p.scale_log2;
+            st.acc[g][e] = 0.f;
+        }
+        st.m[g] = -INFINITY;
+        st.l[g] = 0.f;
+    }
+    st.m_mine = -INFINITY;
+}
+
+template <int D, int G>
+__device__ __forceinline__ void fma_block(FmaState<D, G>& st, const uint8_t* ks, const uint8_t* vs,
+                                          float* __restrict__ ps, int valid, int lane) {
     using C = Cfg<D, G>;
     const int sub = lane % C::L;
     const int rg = lane / C::L;
@@ -229,66 +350,64 @@ __device__ __forceinline__ void consume_block(const uint16_t* __restrict__ ks, c
 
     float sc[C::kSteps];
 #pragma unroll
-    for (int st = 0; st < C::kSteps; ++st) {
-        const int row = st * C::R + rg;
-        const uint4 raw = *reinterpret_cast<const uint4*>(ks + row * D + sub * 8);
+    for (int s = 0; s < C::kSteps; ++s) {
+        const int row = s * C::R + rg;
+        const uint4 raw = *reinterpret_cast<const uint4*>(ks + swz(row, sub * 8));
         float kf[8];
         unpack_bf16x8(raw, kf);
         float dot[G];
 #pragma unroll
         for (int g = 0; g < G; ++g) {
-            float a = qf[g][0] * kf[0];
+            float a = st.qf[g][0] * kf[0];
 #pragma unroll
-            for (int e = 1; e < 8; ++e) a = fmaf(qf[g][e], kf[e], a);
+            for (int e = 1; e < 8; ++e) a = fmaf(st.qf[g][e], kf[e], a);
             dot[g] = a;
         }
-        const float s = Butterfly<C::L / 2, G>::run(dot, lane);
-        sc[st] = row < valid ? s : -INFINITY;
+        const float sv = Butterfly<C::L / 2, G>::run(dot, lane);
+        sc[s] = row < valid ? sv : -INFINITY;
     }
 
-    // block maximum of my head, then the new running maximum of every head
     float bm = sc[0];
 #pragma unroll
-    for (int st = 1; st < C::kSteps; ++st) bm = fmaxf(bm, sc[st]);
+    for (int s = 1; s < C::kSteps; ++s) bm = fmaxf(bm, sc[s]);
 #pragma unroll
     for (int mask = C::L; mask < 32; mask <<= 1) bm = fmaxf(bm, __shfl_xor_sync(kFull, bm, mask));
     float alpha[G];
 #pragma unroll
     for (int g = 0; g < G; ++g) {
         const float bmg = __shfl_sync(kFull, bm, g * C::HG);
-        const float mn = fmaxf(m[g], bmg);
-        alpha[g] = exp2f(m[g] - mn);   // m = -inf on the first block: alpha = 0
-        m[g] = mn;
+        const float mn = fmaxf(st.m[g], bmg);
+        alpha[g] = exp2f(st.m[g] - mn);   // m = -inf on the first block: alpha = 0
+        st.m[g] = mn;
     }
-    m_mine = fmaxf(m_mine, bm);
+    st.m_mine = fmaxf(st.m_mine, bm);
 
     float pr[C::kSteps];
     float psum = 0.f;
 #pragma unroll
-    for (int st = 0; st < C::kSteps; ++st) {
-        pr[st] = exp2f(sc[st] - m_mine);   // masked rows: exp2(-inf) = 0
-        psum += pr[st];
+    for (int s = 0; s < C::kSteps; ++s) {
+        pr[s] = exp2f(sc[s] - st.m_mine);   // masked rows: exp2(-inf) = 0
+        psum += pr[s];
     }
 #pragma unroll
     for (int mask = C::L; mask < 32; mask <<= 1) psum += __shfl_xor_sync(kFull, psum, mask);
 #pragma unroll
     for (int g = 0; g < G; ++g) {
-        l[g] = l[g] * alpha[g] + __shfl_sync(kFull, psum, g * C::HG);
+        st.l[g] = st.l[g] * alpha[g] + __shfl_sync(kFull, psum, g * C::HG);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) acc[g][e] *= alpha[g];
+        for (int e = 0; e < 8; ++e) st.acc[g][e] *= alpha[g];
     }
 
-    // publish p[row][g] for the whole warp, then accumulate p * V
     if (sub % C::HG == 0) {
 #pragma unroll
-        for (int st = 0; st < C::kSteps; ++st) ps[(st * C::R + rg) * G + my_g] = pr[st];
+        for (int s = 0; s < C::kSteps; ++s) ps[(s * C::R + rg) * G + my_g] = pr[s];
     }
     __syncwarp();
 #pragma unroll
-    for (int st = 0; st < C::kSteps; ++st) {
-        const int row = st * C::R + rg;
+    for (int s = 0; s < C::kSteps; ++s) {
+        const int row = s * C::R + rg;
         if (row < valid) {   // rows past N_b may hold stale, even non-finite, data
-            const uint4 raw = *reinterpret_cast<const uint4*>(vs + row * D + sub * 8);
+            const uint4 raw = *reinterpret_cast<const uint4*>(vs + swz(row, sub * 8));
             float vf[8];
             unpack_bf16x8(raw, vf);
             float pv[G];
@@ -297,11 +416,243 @@ __device__ __forceinline__ void consume_block(const uint16_t* __restrict__ ks, c
 #pragma unroll
             for (int g = 0; g < G; ++g)
 #pragma unroll
-                for (int e = 0; e < 8; ++e) acc[g][e] = fmaf(pv[g], vf[e], acc[g][e]);
+                for (int e = 0; e < 8; ++e) st.acc[g][e] = fmaf(pv[g], vf[e], st.acc[g][e]);
         }
     }
     __syncwarp();
 }
+
+// Publish the warp's state (m, l, unnormalised output) for the end-of-tile merge.
+template <int D, int G>
+__device__ __forceinline__ void fma_publish(FmaState<D, G>& st, Smem<D, G>& sm, int warp, int lane) {
+    using C = Cfg<D, G>;
+    const int sub = lane % C::L;
+#pragma unroll
+    for (int mask = C::L; mask < 32; mask <<= 1)
+#pragma unroll
+        for (int g = 0; g < G; ++g)
+#pragma unroll
+            for (int e = 0; e < 8; ++e) st.acc[g][e] += __shfl_xor_sync(kFull, st.acc[g][e], mask);
+    if (lane < C::L) {
+#pragma unroll
+        for (int g = 0; g < G; ++g)
+#pragma unroll
+            for (int e = 0; e < 8; ++e) sm.acc[warp][g * D + sub * 8 + e] = st.acc[g][e];
+    }
+    if (lane == 0) {
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+            sm.m[warp][g] = st.m[g];
+            sm.l[warp][g] = st.l[g];
+        }
+    }
+}
+
+// ------------------------------------------------------------------ MMA block reduction
+//
+// Fragment layout of mma.m16n8k16 (gid = lane / 4, tig = lane % 4):
+//   A rows gid, gid+8 / cols 2tig(+1), 2tig+8(+1);  B rows (k) 2tig(+1), 2tig+8(+1) / col gid;
+//   C rows gid, gid+8 / cols 2tig, 2tig+1.
+// QK: S^T[token][column] with column n = query head n (n < G, the rest zero).
+// PV: O^T[d][column]: column n < G is head n's hi part; the lo parts sit in
+// columns G..2G-1 (2G <= 8) or in a second column tile (G = 8).
+
+template <int D, int G>
+struct MmaState {
+    uint32_t qb[D / 16][2];                  // B fragments of Q^T
+    float m[2];                              // running max of heads 2tig, 2tig+1 (log2 domain)
+    float l[2];                              // this lane's share of their running sums
+    float o[Cfg<D, G>::NPV][D / 16][4];      // O^T accumulators
+};
+
+template <int D, int G>
+__device__ __forceinline__ void mma_init(MmaState<D, G>& st, const AttnParams& p, const TileWork& tw, int lane) {
+    const int gid = lane >> 2, tig = lane & 3;
+    const uint16_t* qh = p.q + (static_cast<size_t>(tw.b) * p.Hq + tw.kvh * G + (gid < G ? gid : 0)) * D;
+#pragma unroll
+    for (int kt = 0; kt < D / 16; ++kt) {
+        st.qb[kt][0] = gid < G ? __ldg(reinterpret_cast<const uint32_t*>(qh + kt * 16 + 2 * tig)) : 0u;
+        st.qb[kt][1] = gid < G ? __ldg(reinterpret_cast<const uint32_t*>(qh + kt * 16 + 8 + 2 * tig)) : 0u;
+    }
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+        st.m[c] = -INFINITY;
+        st.l[c] = 0.f;
+    }
+#pragma unroll
+    for (int t = 0; t < Cfg<D, G>::NPV; ++t)
+#pragma unroll
+        for (int mt = 0; mt < D / 16; ++mt)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) st.o[t][mt][i] = 0.f;
+}
+
+__device__ __forceinline__ uint16_t bf16_bits(float x) {
+    return __bfloat16_as_ushort(__float2bfloat16_rn(x));
+}
+
+__device__ __forceinline__ float bf16_value(uint16_t b) { return __uint_as_float(static_cast<uint32_t>(b) << 16); }
+
+template <int D, int G>
+__device__ __forceinline__ void mma_block(MmaState<D, G>& st, uint8_t* ks, uint8_t* vs, uint64_t* empty,
+                                          uint16_t* pt, int valid, int lane, float scale_log2) {
+    using C = Cfg<D, G>;
+    const int gid = lane >> 2, tig = lane & 3;
+    const int j = lane >> 3, r8 = lane & 7;
+    const uint32_t ka = smem_addr(ks), va = smem_addr(vs);
+
+    // Rows past N_b may hold stale, even non-finite, data (0 * inf = NaN in P V):
+    // zero them in the stage first.
+    if (valid < kBlockRows) {
+        for (int idx = lane; idx < (kBlockRows - valid) * (D / 8); idx += 32) {
+            const int row = valid + idx / (D / 8);
+            *reinterpret_cast<uint4*>(vs + swz(row, (idx % (D / 8)) * 8)) = make_uint4(0u, 0u, 0u, 0u);
+        }
+        fence_proxy_async_shared();   // the next TMA into this stage is ordered after these writes
+        __syncwarp();
+    }
+    // The whole block moves to registers as mma fragments, and the stage goes
+    // straight back to the producer: a stage is held for a few dozen cycles,
+    // not for the block's arithmetic, so the ring stays full of loads in flight.
+    uint32_t kf[D / 16][4], vf[D / 16][4];
+    {
+        const int row = r8 + 8 * (j & 1);
+        const int tok = r8 + 8 * (j >> 1);
+#pragma unroll
+        for (int kt = 0; kt < D / 16; ++kt) ldsm_x4(kf[kt], ka + swz(row, kt * 16 + 8 * (j >> 1)));
+#pragma unroll
+        for (int mt = 0; mt < D / 16; ++mt) ldsm_x4_trans(vf[mt], va + swz(tok, mt * 16 + 8 * (j & 1)));
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(empty);
+
+    // S^T = K Q^T over D in steps of 16
+    float s[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int kt = 0; kt < D / 16; ++kt) mma_16816(s, kf[kt], st.qb[kt][0], st.qb[kt][1]);
+    const bool r0 = gid < valid, r1 = gid + 8 < valid;
+    s[0] = r0 ? s[0] * scale_log2 : -INFINITY;
+    s[1] = r0 ? s[1] * scale_log2 : -INFINITY;
+    s[2] = r1 ? s[2] * scale_log2 : -INFINITY;
+    s[3] = r1 ? s[3] * scale_log2 : -INFINITY;
+
+    // online softmax for the lane's two columns
+    float bm0 = fmaxf(s[0], s[2]), bm1 = fmaxf(s[1], s[3]);
+#pragma unroll
+    for (int x = 4; x < 32; x <<= 1) {
+        bm0 = fmaxf(bm0, __shfl_xor_sync(kFull, bm0, x));
+        bm1 = fmaxf(bm1, __shfl_xor_sync(kFull, bm1, x));
+    }
+    const float mn0 = fmaxf(st.m[0], bm0), mn1 = fmaxf(st.m[1], bm1);
+    const float al0 = exp2f(st.m[0] - mn0), al1 = exp2f(st.m[1] - mn1);   // first block: 0
+    st.m[0] = mn0;
+    st.m[1] = mn1;
+    const float p0 = exp2f(s[0] - mn0), p1 = exp2f(s[1] - mn1);   // token gid
+    const float p2 = exp2f(s[2] - mn0), p3 = exp2f(s[3] - mn1);   // token gid + 8
+    st.l[0] = st.l[0] * al0 + (p0 + p2);
+    st.l[1] = st.l[1] * al1 + (p1 + p3);
+
+    // P^T into shared memory as bf16 hi/lo parts: pt[tile][half][column][8 tokens]
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+        const int h = 2 * tig + c;
+        if (h < G) {
+            const float pa = c ? p1 : p0, pb = c ? p3 : p2;
+            const uint16_t ha = bf16_bits(pa), hb = bf16_bits(pb);
+            const uint16_t la = bf16_bits(pa - bf16_value(ha)), lb = bf16_bits(pb - bf16_value(hb));
+            constexpr int lt = C::NPV == 1 ? 0 : 1;
+            const int ln = C::NPV == 1 ? G + h : h;
+            pt[((0 * 2 + 0) * 8 + h) * 8 + gid] = ha;
+            pt[((0 * 2 + 1) * 8 + h) * 8 + gid] = hb;
+            pt[((lt * 2 + 0) * 8 + ln) * 8 + gid] = la;
+            pt[((lt * 2 + 1) * 8 + ln) * 8 + gid] = lb;
+        }
+    }
+
+    // rescale O^T by the alpha of the head each of the lane's columns belongs to
+    float a0, a1;
+    if constexpr (G == 1) {
+        a0 = a1 = __shfl_sync(kFull, al0, lane & ~3);
+    } else if constexpr (C::NPV == 1) {
+        const int h0 = (2 * tig) & (G - 1);
+        const int src = (lane & ~3) | (h0 >> 1);
+        a0 = __shfl_sync(kFull, al0, src);
+        a1 = __shfl_sync(kFull, al1, src);
+    } else {
+        a0 = al0;
+        a1 = al1;
+    }
+#pragma unroll
+    for (int t = 0; t < C::NPV; ++t)
+#pragma unroll
+        for (int mt = 0; mt < D / 16; ++mt) {
+            st.o[t][mt][0] *= a0;
+            st.o[t][mt][1] *= a1;
+            st.o[t][mt][2] *= a0;
+            st.o[t][mt][3] *= a1;
+        }
+
+    __syncwarp();
+
+    uint32_t pb[C::NPV][2];
+#pragma unroll
+    for (int t = 0; t < C::NPV; ++t)
+        ldsm_x2(pb[t], smem_addr(pt) + (((t * 2 + ((lane >> 3) & 1)) * 8 + (lane & 7)) * 16));
+
+    // O^T += V^T P^T over D in tiles of 16
+#pragma unroll
+    for (int mt = 0; mt < D / 16; ++mt)
+#pragma unroll
+        for (int t = 0; t < C::NPV; ++t) mma_16816(st.o[t][mt], vf[mt], pb[t][0], pb[t][1]);
+    __syncwarp();   // pt is rewritten by the next block
+}
+
+template <int D, int G>
+__device__ __forceinline__ void mma_publish(MmaState<D, G>& st, Smem<D, G>& sm, int warp, int lane) {
+    using C = Cfg<D, G>;
+    const int gid = lane >> 2, tig = lane & 3;
+#pragma unroll
+    for (int c = 0; c < 2; ++c)
+#pragma unroll
+        for (int x = 4; x < 32; x <<= 1) st.l[c] += __shfl_xor_sync(kFull, st.l[c], x);
+    // fold the lo parts into the hi parts
+#pragma unroll
+    for (int mt = 0; mt < D / 16; ++mt) {
+        float f[4];
+        if constexpr (G == 1) {
+            f[0] = st.o[0][mt][0] + st.o[0][mt][1];
+            f[2] = st.o[0][mt][2] + st.o[0][mt][3];
+            f[1] = f[3] = 0.f;
+        } else if constexpr (C::NPV == 1) {
+            const int src = (lane & ~3) | ((tig + G / 2) & 3);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) f[i] = st.o[0][mt][i] + __shfl_sync(kFull, st.o[0][mt][i], src);
+        } else {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) f[i] = st.o[0][mt][i] + st.o[1][mt][i];
+        }
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+            const int h = 2 * tig + c;
+            if (h < G) {
+                sm.acc[warp][h * D + mt * 16 + gid] = f[c];
+                sm.acc[warp][h * D + mt * 16 + gid + 8] = f[2 + c];
+            }
+        }
+    }
+    if (gid == 0) {
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+            const int h = 2 * tig + c;
+            if (h < G) {
+                sm.m[warp][h] = st.m[c];
+                sm.l[warp][h] = st.l[c];
+            }
+        }
+    }
+}
+
+// ------------------------------------------------------------------ merges
 
 // Write the neutral state (out = 0, lse = -inf) for every query head of row b.
 __device__ void write_neutral_row(const AttnParams& p, int b, int tid, int nthreads) {
@@ -309,56 +660,173 @@ __device__ void write_neutral_row(const AttnParams& p, int b, int tid, int nthre
     for (int i = tid; i < p.Hq; i += nthreads) p.lse[static_cast<size_t>(b) * p.Hq + i] = -INFINITY;
 }
 
-// Exact LSE merge of the `ns` partial states of (b, kvh) into out / lse.
-// Partials come from other CTAs, so they are read through L2 (ld.cg).
+// Exact LSE merge of the `ns` partial states of (b, kvh) into out / lse
+// (M = max_s lse_s, w_s = 2^(lse_s - M) / sum_s 2^(lse_s - M), out = sum_s w_s o_s).
+// Must be called by every thread of the CTA.  Partials come from other CTAs,
+// so they are read through L2 (ld.cg).  `wsm` is shared scratch of
+// kMergeCapFloats floats (the planner keeps ns * G within it).
 template <int D, int G>
-__device__ void merge_unit(const AttnParams& p, int b, int kvh, int ns, int tid, int nthreads) {
+__device__ void merge_unit(const AttnParams& p, int b, int kvh, int ns, float* wsm, float* m_s, float* inv_s,
+                           int* nan_s) {
+    const int tid = threadIdx.x, nthreads = blockDim.x;
     const size_t base = static_cast<size_t>(p.row_start[b]) + static_cast<size_t>(kvh) * ns;
-    for (int idx = tid; idx < G * D; idx += nthreads) {
-        const int g = idx / D, d = idx % D;
-        const int h = kvh * G + g;
+    if (tid == 0) *nan_s = 0;
+    __syncthreads();
+    for (int i = tid; i < ns * G; i += nthreads) {
+        const float ls = __ldcg(p.ws_lse + base * G + i);
+        if (isnan(ls)) *nan_s = 1;
+        wsm[i] = ls;
+    }
+    __syncthreads();
+    if (tid < G) {
+        float M = -INFINITY;
+        for (int s = 0; s < ns; ++s) M = fmaxf(M, wsm[s * G + tid]);
+        float wsum = 0.f;
+        if (M != -INFINITY)
+            for (int s = 0; s < ns; ++s) wsum += exp2f(wsm[s * G + tid] - M);
+        m_s[tid] = M;
+        inv_s[tid] = M != -INFINITY ? 1.f / wsum : 0.f;
+        const float lse2 = M != -INFINITY ? M + log2f(wsum) : -INFINITY;
+        p.lse[static_cast<size_t>(b) * p.Hq + kvh * G + tid] = *nan_s ? NAN : lse2 * kLn2;
+    }
+    __syncthreads();
+    for (int i = tid; i < ns * G; i += nthreads) {
+        const int g = i % G;
+        wsm[i] = m_s[g] != -INFINITY ? exp2f(wsm[i] - m_s[g]) * inv_s[g] : 0.f;
+    }
+    __syncthreads();
+    const bool nan = *nan_s != 0;
+    for (int i = tid; i < G * D / 4; i += nthreads) {
+        const int g = i / (D / 4), d = (i % (D / 4)) * 4;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        const float* src = p.ws_o + (base * G + g) * D + d;
+#pragma unroll 8
+        for (int s = 0; s < ns; ++s) {
+            const float w = wsm[s * G + g];
+            const float4 o = __ldcg(reinterpret_cast<const float4*>(src + static_cast<size_t>(s) * G * D));
+            acc.x = fmaf(w, o.x, acc.x);
+            acc.y = fmaf(w, o.y, acc.y);
+            acc.z = fmaf(w, o.z, acc.z);
+            acc.w = fmaf(w, o.w, acc.w);
+        }
+        if (nan) acc = make_float4(NAN, NAN, NAN, NAN);
+        *reinterpret_cast<float4*>(p.out + (static_cast<size_t>(b) * p.Hq + kvh * G + g) * D + d) = acc;
+    }
+    __syncthreads();
+}
+
+// The fused merge of the last-arriving CTA.  The ns partial outputs of
+// (b, kvh) are contiguous in the workspace, so they come into the CTA's idle
+// stage buffers with bulk asynchronous copies (a chunk of splits at a time)
+// while the threads read the LSEs and form the weights; the sum then runs out
+// of shared memory.  Same arithmetic as merge_unit; all CTA threads call it.
+template <int D, int G>
+__device__ void merge_unit_bulk(Smem<D, G>& sm, const AttnParams& p, int b, int kvh, int ns) {
+    constexpr int kScratch = Cfg<D, G>::kStages * Cfg<D, G>::kMatBytes * 2;   // K and V stages
+    constexpr int kSplitBytes = G * D * 4;
+    const int tid = threadIdx.x, nthreads = blockDim.x;
+    const size_t base = static_cast<size_t>(p.row_start[b]) + static_cast<size_t>(kvh) * ns;
+    uint8_t* scratch = &sm.k[0][0];   // k and v stages are adjacent
+    float* w = reinterpret_cast<float*>(scratch);                  // [ns][G] weights
+    const int w_bytes = (ns * G * 4 + 1023) & ~1023;
+    float* obuf = reinterpret_cast<float*>(scratch + w_bytes);     // [chunk][G][D] partials
+    const int chunk = (kScratch - w_bytes) / kSplitBytes;
+    uint32_t* status = &p.ctr->status;
+
+    auto issue = [&](int s0) {   // thread 0: bulk-copy splits [s0, s0 + chunk) of (b, kvh)
+        const int n = min(chunk, ns - s0);
+        mbar_arrive_expect_tx(&sm.merge_bar, static_cast<uint32_t>(n * kSplitBytes));
+        bulk_load(obuf, p.ws_o + (base + s0) * G * D, static_cast<uint32_t>(n * kSplitBytes), &sm.merge_bar);
+    };
+    if (tid == 0) {
+        sm.merge_nan = 0;
+        fence_proxy_async_global();
+        issue(0);
+    }
+    for (int i = tid; i < ns * G; i += nthreads) w[i] = __ldcg(p.ws_lse + base * G + i);
+    __syncthreads();
+    if (tid < G) {
         float M = -INFINITY;
         bool nan = false;
         for (int s = 0; s < ns; ++s) {
-            const float ls = __ldcg(p.ws_lse + (base + s) * G + g);
-            nan |= isnan(ls);
-            M = fmaxf(M, ls);
+            nan |= isnan(w[s * G + tid]);
+            M = fmaxf(M, w[s * G + tid]);
         }
-        float o = 0.f, lse2 = -INFINITY;
-        if (M != -INFINITY) {
-            float wsum = 0.f, acc = 0.f;
-            for (int s = 0; s < ns; ++s) {
-                const float ls = __ldcg(p.ws_lse + (base + s) * G + g);
-                const float w = exp2f(ls - M);   // neutral split: exp2(-inf) = 0
-                wsum += w;
-                acc = fmaf(w, __ldcg(p.ws_o + ((base + s) * G + g) * D + d), acc);
-            }
-            o = acc / wsum;
-            lse2 = M + log2f(wsum);
-        }
-        if (nan) o = lse2 = NAN;
-        p.out[(static_cast<size_t>(b) * p.Hq + h) * D + d] = o;
-        if (d == 0) p.lse[static_cast<size_t>(b) * p.Hq + h] = lse2 * 0.69314718055994530942f;
+        float wsum = 0.f;
+        if (M != -INFINITY)
+            for (int s = 0; s < ns; ++s) wsum += exp2f(w[s * G + tid] - M);
+        sm.merge_m[tid] = M;
+        sm.merge_inv[tid] = M != -INFINITY ? 1.f / wsum : 0.f;
+        if (nan) sm.merge_nan = 1;
+        const float lse2 = M != -INFINITY ? M + log2f(wsum) : -INFINITY;
+        p.lse[static_cast<size_t>(b) * p.Hq + kvh * G + tid] = nan ? NAN : lse2 * kLn2;
     }
+    __syncthreads();
+    for (int i = tid; i < ns * G; i += nthreads) {
+        const int g = i % G;
+        w[i] = sm.merge_m[g] != -INFINITY ? exp2f(w[i] - sm.merge_m[g]) * sm.merge_inv[g] : 0.f;
+    }
+    constexpr int kOut = G * D / 4;   // float4 outputs of (b, kvh)
+    float4 acc[2] = {make_float4(0.f, 0.f, 0.f, 0.f), make_float4(0.f, 0.f, 0.f, 0.f)};
+    for (int s0 = 0; s0 < ns; s0 += chunk) {
+        const int n = min(chunk, ns - s0);
+        mbar_wait(&sm.merge_bar, sm.merge_phase & 1u, status, nullptr);
+        __syncthreads();   // weights ready; every thread saw this chunk land
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+            const int i = tid + r * nthreads;
+            if (i < kOut) {
+                const int g = i / (D / 4), d = (i % (D / 4)) * 4;
+                for (int s = 0; s < n; ++s) {
+                    const float ws = w[(s0 + s) * G + g];
+                    const float4 o = *reinterpret_cast<const float4*>(obuf + (s * G + g) * D + d);
+                    acc[r].x = fmaf(ws, o.x, acc[r].x);
+                    acc[r].y = fmaf(ws, o.y, acc[r].y);
+                    acc[r].z = fmaf(ws, o.z, acc[r].z);
+                    acc[r].w = fmaf(ws, o.w, acc[r].w);
+                }
+            }
+        }
+        __syncthreads();   // chunk consumed
+        if (tid == 0) {
+            ++sm.merge_phase;
+            if (s0 + chunk < ns) issue(s0 + chunk);
+        }
+    }
+    const bool nan = sm.merge_nan != 0;
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+        const int i = tid + r * nthreads;
+        if (i < kOut) {
+            const int g = i / (D / 4), d = (i % (D / 4)) * 4;
+            *reinterpret_cast<float4*>(p.out + (static_cast<size_t>(b) * p.Hq + kvh * G + g) * D + d) =
+                nan ? make_float4(NAN, NAN, NAN, NAN) : acc[r];
+        }
+    }
+    __syncthreads();
 }
 
-// One tile: producer warp streams blocks, consumer warps reduce them, then the
-// four warp states are merged and written (to out/lse or to the workspace).
-// `pipe` counts blocks this CTA has streamed so far (stage/phase bookkeeping
-// continues across the tiles of a persistent CTA).
-template <int D, int G>
+// ------------------------------------------------------------------ tile
+
+// One tile: the producer warp streams blocks, the consumer warps reduce them,
+// then the four warp states are merged and written (to out/lse, or to the
+// workspace for a split).  `pipe` counts blocks this CTA has streamed before
+// (stage/phase bookkeeping continues across the tiles of a persistent CTA).
+template <int D, int G, bool MMA>
 __device__ void run_tile(Smem<D, G>& sm, const AttnParams& p, const TileWork& tw, uint32_t pipe,
                          const CUtensorMap* kmap, const CUtensorMap* vmap) {
     using C = Cfg<D, G>;
+    constexpr int kStages = C::kStages;
     const int warp = threadIdx.x / 32;
     const int lane = threadIdx.x % 32;
     const int ntok = tw.t1 > tw.t0 ? tw.t1 - tw.t0 : 0;
     const int nblk = (ntok + kBlockRows - 1) / kBlockRows;
     uint32_t* status = &p.ctr->status;
 
-    if (warp == kConsumerWarps) {
-        // ---------------- producer
+    if (warp >= kConsumerWarps) {
+        // ---------------- producers
         if (nblk == 0) return;
+        const int pw = warp - kConsumerWarps;
         const int ps = p.page_size;
         const int first_page = tw.t0 / ps;
         const int last_page = (tw.t1 + ps - 1) / ps;   // exclusive
@@ -376,26 +844,52 @@ __device__ void run_tile(Smem<D, G>& sm, const AttnParams& p, const TileWork& tw
                 const int page_tok0 = (pg0 + i) * ps;
                 const int lo = max(page_tok0, tw.t0);
                 const int hi = min(page_tok0 + ps, tw.t1);
+                const bool page_ok = page >= 0 && page < p.num_pages;
                 for (int tok = lo; tok < hi; tok += kBlockRows, ++j) {
+                    if (j % kProducerWarps != pw) continue;
+                    const uint32_t it = pipe + j;
+                    const int s = it % kStages;
+                    const uint32_t use = it / kStages;
+                    int go = 0;
                     if (lane == 0) {
-                        const uint32_t it = pipe + j;
-                        const int s = it % kStages;
-                        const uint32_t use = it / kStages;
-                        bool go = !sm.abort;
+                        go = !sm.abort;
                         if (go && use > 0) go = mbar_wait(&sm.empty[s], (use - 1) & 1u, status, &sm.abort);
-                        const bool page_ok = page >= 0 && page < p.num_pages;
                         if (!page_ok) atomicOr(status, static_cast<uint32_t>(PKV_DEV_PAGE_OOB));
-                        if (!go || !page_ok) {
-                            sm.bad[s] = 1;
-                            mbar_arrive(&sm.full[s]);
-                        } else {
-                            sm.bad[s] = 0;
-                            sm.issued[s] = use + 1;
+                        go = go && page_ok;
+                        sm.bad[s] = !go;
+                        if (go) sm.issued[s] = use + 1;
+                        if (p.copy_lsu)
+                            mbar_arrive(&sm.full[s]);   // publishes bad[s]; the lanes' copies arrive below
+                        else if (go)
                             mbar_arrive_expect_tx(&sm.full[s], C::kStageBytes);
-                            const int row = page * ps + (tok - page_tok0);
-                            tma_load_3d(sm.k[s], kmap, 0, tw.kvh, row, &sm.full[s], policy);
-                            tma_load_3d(sm.v[s], vmap, 0, tw.kvh, row, &sm.full[s], policy);
+                        else
+                            mbar_arrive(&sm.full[s]);
+                    }
+                    go = __shfl_sync(kFull, go, 0);
+                    const int grow = page * ps + (tok - page_tok0);   // token row inside the pool
+                    if (p.copy_lsu) {
+                        // every lane moves D/16 16-byte chunks of K and as many of V
+                        // into the swizzled stage, then arrives when they have landed
+                        if (go) {
+                            const size_t row0 = (static_cast<size_t>(grow) * p.Hkv + tw.kvh) * D;
+                            const size_t pitch = static_cast<size_t>(p.Hkv) * D;
+                            const uint32_t ks = smem_addr(sm.k[s]), vs = smem_addr(sm.v[s]);
+#pragma unroll
+                            for (int i = 0; i < kBlockRows * (D / 8) / 32; ++i) {
+                                const int q = lane + 32 * i;
+                                const int r = q / (D / 8), c = (q % (D / 8)) * 8;
+                                const size_t off = row0 + r * pitch + c;
+                                cp_async16(ks + swz(r, c), p.k_pages + off, policy);
+                                cp_async16(vs + swz(r, c), p.v_pages + off, policy);
+                            }
                         }
+                        cp_async_arrive_noinc(&sm.full[s]);
+                    } else if (go && lane < 2 * (D / 64)) {
+                        // the block's D/64 K boxes and D/64 V boxes, after lane 0 armed the barrier
+                        const int h = lane % (D / 64);
+                        const bool is_v = lane >= D / 64;
+                        tma_load_3d((is_v ? sm.v[s] : sm.k[s]) + h * (kBlockRows * 128), is_v ? vmap : kmap, h * 64,
+                                    tw.kvh, grow, &sm.full[s], policy);
                     }
                 }
             }
@@ -404,64 +898,41 @@ __device__ void run_tile(Smem<D, G>& sm, const AttnParams& p, const TileWork& tw
     }
 
     // ---------------- consumers
-    const int sub = lane % C::L;
-    float qf[G][8];
-    {
-        const uint16_t* qrow = p.q + (static_cast<size_t>(tw.b) * p.Hq + tw.kvh * G) * D + sub * 8;
-#pragma unroll
-        for (int g = 0; g < G; ++g) {
-            const uint4 raw = __ldg(reinterpret_cast<const uint4*>(qrow + g * D));
-            unpack_bf16x8(raw, qf[g]);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) qf[g][e] *= p.scale_log2;
-        }
-    }
-    float m[G], l[G], acc[G][8];
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
-        m[g] = -INFINITY;
-        l[g] = 0.f;
-#pragma unroll
-        for (int e = 0; e < 8; ++e) acc[g][e] = 0.f;
-    }
-    float m_mine = -INFINITY;
     int poisoned = tw.poisoned;
-
-    for (int j = warp; j < nblk; j += kConsumerWarps) {
-        const uint32_t it = pipe + j;
-        const int s = it % kStages;
-        const bool ok = mbar_wait(&sm.full[s], (it / kStages) & 1u, status, &sm.abort);
-        if (!ok || sm.bad[s]) {
-            poisoned = 1;
-        } else {
-            const int valid = min(kBlockRows, ntok - j * kBlockRows);
-            consume_block<D, G>(sm.k[s], sm.v[s], sm.p[warp], valid, lane, qf, m, l, m_mine, acc);
+    if constexpr (MMA) {
+        MmaState<D, G> st;
+        mma_init<D, G>(st, p, tw, lane);
+        for (int j = warp; j < nblk; j += kConsumerWarps) {
+            const uint32_t it = pipe + j;
+            const int s = it % kStages;
+            const bool ok = mbar_wait(&sm.full[s], (it / kStages) & 1u, status, &sm.abort);
+            if (!ok || sm.bad[s]) {
+                poisoned = 1;
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sm.empty[s]);
+            } else {   // releases the stage itself once the block is in registers
+                mma_block<D, G>(st, sm.k[s], sm.v[s], &sm.empty[s], sm.pt[warp],
+                                min(kBlockRows, ntok - j * kBlockRows), lane, p.scale_log2);
+            }
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&sm.empty[s]);
-    }
-
-    // fold the row groups of the warp, then publish the warp's state
-#pragma unroll
-    for (int mask = C::L; mask < 32; mask <<= 1)
-#pragma unroll
-        for (int g = 0; g < G; ++g)
-#pragma unroll
-            for (int e = 0; e < 8; ++e) acc[g][e] += __shfl_xor_sync(kFull, acc[g][e], mask);
-    if (lane < C::L) {
-#pragma unroll
-        for (int g = 0; g < G; ++g)
-#pragma unroll
-            for (int e = 0; e < 8; ++e) sm.acc[warp][g * D + sub * 8 + e] = acc[g][e];
-    }
-    if (lane == 0) {
-#pragma unroll
-        for (int g = 0; g < G; ++g) {
-            sm.m[warp][g] = m[g];
-            sm.l[warp][g] = l[g];
+        mma_publish<D, G>(st, sm, warp, lane);
+    } else {
+        FmaState<D, G> st;
+        fma_init<D, G>(st, p, tw, lane);
+        for (int j = warp; j < nblk; j += kConsumerWarps) {
+            const uint32_t it = pipe + j;
+            const int s = it % kStages;
+            const bool ok = mbar_wait(&sm.full[s], (it / kStages) & 1u, status, &sm.abort);
+            if (!ok || sm.bad[s])
+                poisoned = 1;
+            else
+                fma_block<D, G>(st, sm.k[s], sm.v[s], sm.p[warp], min(kBlockRows, ntok - j * kBlockRows), lane);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sm.empty[s]);
         }
-        sm.poisoned[warp] = poisoned;
+        fma_publish<D, G>(st, sm, warp, lane);
     }
+    if (lane == 0) sm.poisoned[warp] = poisoned;
     named_barrier_sync(1, kConsumerWarps * 32);
 
     const int tid = threadIdx.x;
@@ -489,11 +960,34 @@ __device__ void run_tile(Smem<D, G>& sm, const AttnParams& p, const TileWork& tw
         if (tw.finalize) {
             const int h = tw.kvh * G + g;
             p.out[(static_cast<size_t>(tw.b) * p.Hq + h) * D + d] = o;
-            if (d == 0) p.lse[static_cast<size_t>(tw.b) * p.Hq + h] = lse2 * 0.69314718055994530942f;
+            if (d == 0) p.lse[static_cast<size_t>(tw.b) * p.Hq + h] = lse2 * kLn2;
         } else {
             p.ws_o[(static_cast<size_t>(tw.slot) * G + g) * D + d] = o;
             if (d == 0) p.ws_lse[static_cast<size_t>(tw.slot) * G + g] = lse2;
         }
+    }
+}
+
+// After a split tile has written its partial: the last split of (b, kvh) to
+// arrive merges all of them (all CTA threads call this).
+template <int D, int G>
+__device__ void merge_if_last(Smem<D, G>& sm, const AttnParams& p, const TileWork& tw, int ns) {
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        const int u = tw.b * p.Hkv + tw.kvh;
+        const uint32_t prev = atomicAdd(&p.arrive[u], 1u);
+        const int last = prev == static_cast<uint32_t>(ns - 1);
+        if (last) p.arrive[u] = 0;   // ready for the next launch
+        sm.tile_slot[1] = last;
+    }
+    __syncthreads();
+    if (sm.tile_slot[1]) {
+        __threadfence();
+        // the stage buffers are idle here and serve as the merge's scratch
+        static_assert(2 * Cfg<D, G>::kStages * Cfg<D, G>::kMatBytes >= kMergeCapFloats * 4 + 2 * G * D * 4,
+                      "merge scratch");
+        merge_unit_bulk<D, G>(sm, p, tw.b, tw.kvh, ns);
     }
 }
 
@@ -502,7 +996,7 @@ __device__ void run_tile(Smem<D, G>& sm, const AttnParams& p, const TileWork& tw
 // Called by one thread once the producer has stopped issuing.
 template <int D, int G>
 __device__ void drain_after_abort(Smem<D, G>& sm, uint32_t* status) {
-    for (int s = 0; s < kStages; ++s)
+    for (int s = 0; s < Cfg<D, G>::kStages; ++s)
         if (sm.issued[s] > 0) mbar_wait_slow(&sm.full[s], (sm.issued[s] - 1) & 1u, status, nullptr);
 }
 
@@ -526,27 +1020,34 @@ __device__ __forceinline__ TileWork tile_from_queue(const AttnParams& p, int t) 
     return tw;
 }
 
-template <int D, int G>
-__global__ void __launch_bounds__(kThreads) attention_kernel(const AttnParams p,
+template <int D, int G, bool MMA>
+__global__ void __launch_bounds__(kThreads, MMA ? 2 : 1) attention_kernel(const AttnParams p,
                                                              const __grid_constant__ CUtensorMap kmap,
                                                              const __grid_constant__ CUtensorMap vmap) {
-    extern __shared__ __align__(128) unsigned char smem_raw[];
-    Smem<D, G>& sm = *reinterpret_cast<Smem<D, G>*>(smem_raw);
+    extern __shared__ uint8_t smem_raw[];
+    Smem<D, G>& sm =
+        *reinterpret_cast<Smem<D, G>*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) {
-            mbar_init(&sm.full[s], 1);
+        for (int s = 0; s < Cfg<D, G>::kStages; ++s) {
+            // LSU copies: 32 producer lanes' cp.async arrivals + lane 0's flag arrival
+            mbar_init(&sm.full[s], p.copy_lsu ? 33 : 1);
             mbar_init(&sm.empty[s], 1);
             sm.issued[s] = 0;
         }
         sm.abort = 0;
+        mbar_init(&sm.merge_bar, 1);
+        sm.merge_phase = 0;
         fence_mbar_init();
     }
     __syncthreads();
 
-    if (p.route == kRoutePersistent) {
+    if (p.route == kRoutePersistent || p.route == kRouteQueue) {
         // rows with no tokens get no tiles: write their neutral state here
         for (int b = blockIdx.x; b < p.B; b += gridDim.x)
             if (p.row_splits[b] == 0) write_neutral_row(p, b, threadIdx.x, blockDim.x);
+    }
+
+    if (p.route == kRoutePersistent) {
         uint32_t pipe = 0;
         while (true) {
             if (threadIdx.x == 0) sm.tile_slot[0] = static_cast<int>(atomicAdd(&p.ctr->next_tile, 1u));
@@ -554,27 +1055,10 @@ __global__ void __launch_bounds__(kThreads) attention_kernel(const AttnParams p,
             const int t = sm.tile_slot[0];
             if (t >= p.num_tiles) break;
             const TileWork tw = tile_from_queue(p, t);
-            run_tile<D, G>(sm, p, tw, pipe, &kmap, &vmap);
+            run_tile<D, G, MMA>(sm, p, tw, pipe, &kmap, &vmap);
             const int ntok = tw.t1 > tw.t0 ? tw.t1 - tw.t0 : 0;
             pipe += (ntok + kBlockRows - 1) / kBlockRows;
-            if (!tw.finalize && p.fused_merge) {
-                // last-arriving split of (b, kvh) merges all of them
-                __threadfence();
-                __syncthreads();
-                if (threadIdx.x == 0) {
-                    const int u = tw.b * p.Hkv + tw.kvh;
-                    const int ns = p.row_splits[tw.b];
-                    const uint32_t prev = atomicAdd(&p.arrive[u], 1u);
-                    const int last = prev == static_cast<uint32_t>(ns - 1);
-                    if (last) p.arrive[u] = 0;   // ready for the next launch
-                    sm.tile_slot[1] = last;
-                }
-                __syncthreads();
-                if (sm.tile_slot[1]) {
-                    __threadfence();
-                    merge_unit<D, G>(p, tw.b, tw.kvh, p.row_splits[tw.b], threadIdx.x, blockDim.x);
-                }
-            }
+            if (!tw.finalize && p.fused_merge) merge_if_last<D, G>(sm, p, tw, p.row_splits[tw.b]);
             __syncthreads();
         }
         if (threadIdx.x == 0) {
@@ -589,6 +1073,7 @@ __global__ void __launch_bounds__(kThreads) attention_kernel(const AttnParams p,
     }
 
     TileWork tw;
+    int ns = 1;
     if (p.route == kRouteDirect) {
         tw.b = blockIdx.x / p.Hkv;
         tw.kvh = blockIdx.x % p.Hkv;
@@ -597,13 +1082,15 @@ __global__ void __launch_bounds__(kThreads) attention_kernel(const AttnParams p,
         tw.slot = 0;
         tw.finalize = 1;
         tw.poisoned = 0;
-        if (tw.t1 > p.max_pages * p.page_size) {   // would read past the table row
+        if (tw.t1 < 0 || tw.t1 > p.max_pages * p.page_size) {   // would read past the table row
             tw.poisoned = 1;
             tw.t1 = 0;
             if (threadIdx.x == 0) atomicOr(&p.ctr->status, static_cast<uint32_t>(PKV_DEV_PLAN_MISMATCH));
         }
     } else if (p.route == kRouteQueue) {
+        if (static_cast<int>(blockIdx.x) >= p.num_tiles) return;   // launched only for the neutral rows
         tw = tile_from_queue(p, blockIdx.x);
+        ns = p.row_splits[tw.b];
     } else {   // padded grid: (b, kvh, s) from the block index, ranges from the device lengths
         const int per_row = p.Hkv * p.max_splits;
         tw.b = blockIdx.x / per_row;
@@ -611,22 +1098,27 @@ __global__ void __launch_bounds__(kThreads) attention_kernel(const AttnParams p,
         const int s = blockIdx.x % p.max_splits;
         const int n = p.seq_lens[tw.b];
         const int pages = (n + p.page_size - 1) / p.page_size;
-        tw.poisoned = pages > p.max_splits * p.chunk_pages || n > p.max_pages * p.page_size;
+        tw.poisoned = n < 0 || pages > p.max_splits * p.chunk_pages || n > p.max_pages * p.page_size;
         if (tw.poisoned && threadIdx.x == 0) atomicOr(&p.ctr->status, static_cast<uint32_t>(PKV_DEV_PLAN_MISMATCH));
-        const int pb = min(s * p.chunk_pages, pages);
-        const int pe = min((s + 1) * p.chunk_pages, pages);
+        const int pb = max(0, min(s * p.chunk_pages, pages));
+        const int pe = max(0, min((s + 1) * p.chunk_pages, pages));
         tw.t0 = pb * p.page_size;
         tw.t1 = tw.poisoned ? tw.t0 : min(pe * p.page_size, n);
         tw.finalize = p.max_splits == 1;
         tw.slot = blockIdx.x;
+        ns = p.max_splits;
     }
-    run_tile<D, G>(sm, p, tw, 0, &kmap, &vmap);
+    run_tile<D, G, MMA>(sm, p, tw, 0, &kmap, &vmap);
     __syncthreads();
+    if (!tw.finalize && p.fused_merge) merge_if_last<D, G>(sm, p, tw, ns);
     if (threadIdx.x == 0 && sm.abort) drain_after_abort<D, G>(sm, &p.ctr->status);
 }
 
 template <int D, int G>
 __global__ void __launch_bounds__(128) merge_kernel(const AttnParams p) {
+    __shared__ float wsm[kMergeCapFloats];
+    __shared__ float m_s[G], inv_s[G];
+    __shared__ int nan_s;
     const int b = blockIdx.x / p.Hkv;
     const int kvh = blockIdx.x % p.Hkv;
     const int ns = p.row_splits[b];
@@ -639,32 +1131,33 @@ __global__ void __launch_bounds__(128) merge_kernel(const AttnParams p) {
         }
         return;
     }
-    merge_unit<D, G>(p, b, kvh, ns, threadIdx.x, blockDim.x);
+    merge_unit<D, G>(p, b, kvh, ns, wsm, m_s, inv_s, &nan_s);
 }
 
-template <int D, int G>
+template <int D, int G, bool MMA>
 cudaError_t launch_attention_t(const AttnParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap, int grid,
                                cudaStream_t stream) {
-    const size_t smem = sizeof(Smem<D, G>);
+    constexpr size_t smem = smem_bytes<D, G>();
     static bool configured = false;
     if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(attention_kernel<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(smem));
+        cudaError_t e = cudaFuncSetAttribute(attention_kernel<D, G, MMA>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
         if (e != cudaSuccess) return e;
         configured = true;
     }
-    attention_kernel<D, G><<<grid, kThreads, smem, stream>>>(p, kmap, vmap);
+    attention_kernel<D, G, MMA><<<grid, kThreads, smem, stream>>>(p, kmap, vmap);
     return cudaGetLastError();
 }
 
-template <int D, int G>
+template <int D, int G, bool MMA>
 int ctas_per_sm_t() {
-    const size_t smem = sizeof(Smem<D, G>);
-    if (cudaFuncSetAttribute(attention_kernel<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    constexpr size_t smem = smem_bytes<D, G>();
+    if (cudaFuncSetAttribute(attention_kernel<D, G, MMA>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem)) != cudaSuccess)
         return 0;
     int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, attention_kernel<D, G>, kThreads, smem) != cudaSuccess)
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, attention_kernel<D, G, MMA>, kThreads, smem) !=
+        cudaSuccess)
         return 0;
     return n;
 }
@@ -675,17 +1168,17 @@ cudaError_t launch_merge_t(const AttnParams& p, cudaStream_t stream) {
     return cudaGetLastError();
 }
 
-#define PKV_DISPATCH(D_, G_, CALL)                                   \
-    switch ((D_) * 16 + (G_)) {                                      \
-        case 64 * 16 + 1: { constexpr int kD = 64, kG = 1; CALL; }   \
-        case 64 * 16 + 2: { constexpr int kD = 64, kG = 2; CALL; }   \
-        case 64 * 16 + 4: { constexpr int kD = 64, kG = 4; CALL; }   \
-        case 64 * 16 + 8: { constexpr int kD = 64, kG = 8; CALL; }   \
-        case 128 * 16 + 1: { constexpr int kD = 128, kG = 1; CALL; } \
-        case 128 * 16 + 2: { constexpr int kD = 128, kG = 2; CALL; } \
-        case 128 * 16 + 4: { constexpr int kD = 128, kG = 4; CALL; } \
-        case 128 * 16 + 8: { constexpr int kD = 128, kG = 8; CALL; } \
-        default: break;                                              \
+#define PKV_DISPATCH(D_, G_, ...)                                           \
+    switch ((D_) * 16 + (G_)) {                                             \
+        case 64 * 16 + 1: { constexpr int kD = 64, kG = 1; __VA_ARGS__; }   \
+        case 64 * 16 + 2: { constexpr int kD = 64, kG = 2; __VA_ARGS__; }   \
+        case 64 * 16 + 4: { constexpr int kD = 64, kG = 4; __VA_ARGS__; }   \
+        case 64 * 16 + 8: { constexpr int kD = 64, kG = 8; __VA_ARGS__; }   \
+        case 128 * 16 + 1: { constexpr int kD = 128, kG = 1; __VA_ARGS__; } \
+        case 128 * 16 + 2: { constexpr int kD = 128, kG = 2; __VA_ARGS__; } \
+        case 128 * 16 + 4: { constexpr int kD = 128, kG = 4; __VA_ARGS__; } \
+        case 128 * 16 + 8: { constexpr int kD = 128, kG = 8; __VA_ARGS__; } \
+        default: break;                                                     \
     }
 
 }  // namespace
@@ -695,15 +1188,17 @@ bool shape_supported(int D, int G) {
     return false;
 }
 
-int attention_ctas_per_sm(int D, int G) {
-    PKV_DISPATCH(D, G, return (ctas_per_sm_t<kD, kG>()));
+int attention_ctas_per_sm(int D, int G, bool mma) {
+    PKV_DISPATCH(D, G, return mma ? ctas_per_sm_t<kD, kG, true>() : ctas_per_sm_t<kD, kG, false>());
     return 0;
 }
 
 cudaError_t launch_attention(const AttnParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap, int grid,
                              cudaStream_t stream) {
     const int G = p.Hq / p.Hkv;
-    PKV_DISPATCH(p.D, G, return (launch_attention_t<kD, kG>(p, kmap, vmap, grid, stream)));
+    PKV_DISPATCH(p.D, G,
+                 return p.use_mma ? launch_attention_t<kD, kG, true>(p, kmap, vmap, grid, stream)
+                                  : launch_attention_t<kD, kG, false>(p, kmap, vmap, grid, stream));
     return cudaErrorInvalidValue;
 }
 

@@ -14,6 +14,10 @@ namespace pkv {
 // page_size / kBlockRows stages; page_size must be a multiple of it.
 constexpr int kBlockRows = 16;
 
+// Shared-memory scratch (floats) of one exact LSE merge: the planner keeps
+// splits-per-(row, KV head) * G within it.
+constexpr int kMergeCapFloats = 4096;
+
 // Device-side bookkeeping of a plan (zeroed once at creation; kernels that
 // change it put it back before they exit, so no host reset is needed between
 // launches or graph replays).
@@ -33,6 +37,8 @@ enum Route : int32_t {
 
 struct AttnParams {
     const uint16_t* q;            // bf16 [B][Hq][D]
+    const uint16_t* k_pages;      // bf16 [num_pages][page_size][Hkv][D]
+    const uint16_t* v_pages;
     const int32_t* block_table;   // [B][max_pages]
     const int32_t* seq_lens;      // [B]
     const pkv_work_item* queue;   // [num_tiles] for queue / persistent routes
@@ -47,13 +53,15 @@ struct AttnParams {
     int32_t B, Hq, Hkv, D, page_size, max_pages, num_pages;
     int32_t chunk_pages, max_splits, num_tiles;
     int32_t route;
-    int32_t fused_merge;          // persistent route: last arriving split merges
+    int32_t fused_merge;          // split tiles: the last arriving split of (b, kvh) merges
+    int32_t use_mma;              // block reduction on tensor cores (mma.sync) instead of FMA
+    int32_t copy_lsu;             // stage K/V with cp.async from the producer warp instead of TMA
     float scale_log2;             // log2(e) / sqrt(D)
 };
 
 // Attention launch: one of the four routes.  kmap / vmap are TMA descriptors
 // of the K and V pools viewed as [page_size * num_pages][Hkv][D] (innermost D),
-// box {D, 1, kBlockRows}.
+// box {64, 1, kBlockRows}, 128-byte swizzle.
 cudaError_t launch_attention(const AttnParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap,
                              int grid, cudaStream_t stream);
 cudaError_t launch_merge(const AttnParams& p, cudaStream_t stream);
@@ -62,7 +70,7 @@ cudaError_t launch_append(const uint16_t* k_new, const uint16_t* v_new, uint16_t
                           int B, int Hkv, int D, int page_size, int max_pages, int num_pages,
                           uint32_t* status, cudaStream_t stream);
 // Resident CTAs per SM of the attention kernel for this (D, G); 0 if unsupported.
-int attention_ctas_per_sm(int D, int G);
+int attention_ctas_per_sm(int D, int G, bool mma);
 bool shape_supported(int D, int G);
 
 }  // namespace pkv

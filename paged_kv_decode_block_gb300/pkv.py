@@ -19,6 +19,8 @@ MODE_AUTO, MODE_DIRECT, MODE_SPLIT_QUEUE, MODE_SPLIT_PADDED, MODE_PERSISTENT = r
 MODE_NAMES = {MODE_AUTO: "auto", MODE_DIRECT: "direct", MODE_SPLIT_QUEUE: "split_queue",
               MODE_SPLIT_PADDED: "split_padded", MODE_PERSISTENT: "persistent"}
 MODES = {v: k for k, v in MODE_NAMES.items()}
+MATH = {"auto": 0, "fma": 1, "mma": 2}
+COPY = {"auto": 0, "lsu": 1, "tma": 2}
 
 OK, EINVAL, ENOMEM, ECUDA, EUNSUPPORTED, EDEVICE, ENOSPACE = range(7)
 DEV_PAGE_OOB, DEV_PLAN_MISMATCH, DEV_TIMEOUT, DEV_ROW_FULL = 1, 2, 4, 8
@@ -34,7 +36,8 @@ class PlanOpts(ctypes.Structure):
     _fields_ = [("force_mode", ctypes.c_int32), ("num_splits", ctypes.c_int32),
                 ("direct_units_per_sm", ctypes.c_int32), ("target_ctas_per_sm", ctypes.c_int32),
                 ("min_chunk_pages", ctypes.c_int32), ("ctas_per_sm", ctypes.c_int32),
-                ("separate_merge", ctypes.c_int32), ("num_sms", ctypes.c_int32)]
+                ("separate_merge", ctypes.c_int32), ("num_sms", ctypes.c_int32),
+                ("math", ctypes.c_int32), ("copy", ctypes.c_int32)]
 
 
 class WorkItem(ctypes.Structure):
@@ -126,12 +129,17 @@ def _ptr_i32(a):
 
 
 def _opts(force_mode=MODE_AUTO, num_splits=0, direct_units_per_sm=0, target_ctas_per_sm=0,
-          min_chunk_pages=0, ctas_per_sm=0, separate_merge=False, num_sms=0) -> PlanOpts:
+          min_chunk_pages=0, ctas_per_sm=0, separate_merge=False, num_sms=0, math="auto",
+          copy="auto") -> PlanOpts:
     if isinstance(force_mode, str):
         force_mode = MODES[force_mode]
+    if isinstance(math, str):
+        math = MATH[math]
+    if isinstance(copy, str):
+        copy = COPY[copy]
     return PlanOpts(int(force_mode), int(num_splits), int(direct_units_per_sm),
                     int(target_ctas_per_sm), int(min_chunk_pages), int(ctas_per_sm),
-                    int(bool(separate_merge)), int(num_sms))
+                    int(bool(separate_merge)), int(num_sms), int(math), int(copy))
 
 
 def _geom(B, Hq, Hkv, D, max_pages, num_pages) -> Geom:

@@ -17,6 +17,7 @@ from pkv_testutil import (assert_close, expected_queue, make_plan, oracle_result
 pytestmark = pytest.mark.gpu
 
 ROUTES = ["direct", "split_queue", "split_padded", "persistent"]
+MATHS = ["fma", "mma"]
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -26,23 +27,25 @@ def _cuda():
     pkv.load()
 
 
+@pytest.mark.parametrize("math", MATHS)
 @pytest.mark.parametrize("route", ROUTES)
 @pytest.mark.parametrize("splits", [1, 2, 4])
-def test_tiny_every_route_and_split(route, splits):
+def test_tiny_every_route_and_split(route, splits, math):
     p = wl.tiny()
     ref = oracle_result(p)
-    out, lse, plan, _ = run(p, force_mode=route, num_splits=splits)
-    assert_close(out, lse, *ref, what=f"tiny {route} S={splits}")
+    out, lse, plan, _ = run(p, force_mode=route, num_splits=splits, math=math)
+    assert_close(out, lse, *ref, what=f"tiny {route} S={splits} {math}")
     info = plan.info()
     assert info["mode_name"] == route
     assert np.array_equal(plan.queue(), expected_queue(p, info))
     assert plan.status() == 0
 
 
-def test_tiny_split_partials_match_oracle_partials():
+@pytest.mark.parametrize("math", MATHS)
+def test_tiny_split_partials_match_oracle_partials(math):
     """The partial kernel's per-tile states equal the oracle's split partials."""
     p = wl.tiny()
-    _, _, plan, _ = run(p, force_mode="split_queue", num_splits=4)
+    _, _, plan, _ = run(p, force_mode="split_queue", num_splits=4, math=math)
     o, lse = plan.read_workspace()
     q = plan.queue()
     for slot, (b, kvh, s, pb, pe) in enumerate(q):
@@ -55,27 +58,42 @@ def test_tiny_split_partials_match_oracle_partials():
 EDGE_LENS = [1, 15, 16, 17, 32, 33, 0, 250]
 
 
+@pytest.mark.parametrize("math", MATHS)
 @pytest.mark.parametrize("route", ROUTES)
 @pytest.mark.parametrize("splits", [1, 3, 16])
-def test_edge_lengths(route, splits):
+def test_edge_lengths(route, splits, math):
     p = wl.make_problem("edges", EDGE_LENS, Hq=8, Hkv=2, D=128, page_size=16, num_pages=48, seed=21)
     ref = oracle_result(p)
-    out, lse, plan, _ = run(p, force_mode=route, num_splits=splits)
-    assert_close(out, lse, *ref, what=f"edges {route} S={splits}")
+    out, lse, plan, _ = run(p, force_mode=route, num_splits=splits, math=math)
+    assert_close(out, lse, *ref, what=f"edges {route} S={splits} {math}")
     assert np.array_equal(plan.queue(), expected_queue(p, plan.info()))
     assert plan.status() == 0
 
 
+@pytest.mark.parametrize("math", MATHS)
 @pytest.mark.parametrize("D", [64, 128])
 @pytest.mark.parametrize("G", [1, 2, 4, 8])
-def test_every_head_shape(D, G):
+def test_every_head_shape(D, G, math):
     Hkv = 2
     p = wl.make_problem(f"shape{D}x{G}", [77, 300, 16], Hq=G * Hkv, Hkv=Hkv, D=D, page_size=16,
                         num_pages=40, seed=22)
     ref = oracle_result(p)
     for route, splits in [("direct", 0), ("split_queue", 5), ("persistent", 3)]:
-        out, lse, _, _ = run(p, force_mode=route, num_splits=splits)
-        assert_close(out, lse, *ref, what=f"D={D} G={G} {route}")
+        out, lse, _, _ = run(p, force_mode=route, num_splits=splits, math=math)
+        assert_close(out, lse, *ref, what=f"D={D} G={G} {route} {math}")
+
+
+@pytest.mark.parametrize("route", ["split_queue", "split_padded", "persistent"])
+def test_separate_merge_launch(route):
+    """The merge as its own kernel gives the same result as the fused last-arriver merge."""
+    p = wl.make_problem("sepmerge", EDGE_LENS, Hq=8, Hkv=2, D=128, page_size=16, num_pages=48, seed=26)
+    ref = oracle_result(p)
+    out, lse, plan, _ = run(p, force_mode=route, num_splits=4, separate_merge=True)
+    assert plan.info()["launches_per_step"] == 2
+    assert_close(out, lse, *ref, what=f"separate merge {route}")
+    out2, lse2, plan2, _ = run(p, force_mode=route, num_splits=4)
+    assert plan2.info()["launches_per_step"] == 1
+    assert np.array_equal(out, out2) and np.array_equal(lse, lse2)
 
 
 @pytest.mark.parametrize("page_size", [32, 64])
@@ -155,24 +173,36 @@ def test_host_validation_errors():
 
 # --- the full-size workloads ---------------------------------------------------------
 
-@pytest.mark.parametrize("route", ["split_queue", "persistent"])
-def test_batch1_long_32k(route):
+@pytest.fixture(scope="module")
+def batch1_long_ref():
     p = wl.batch1_long()
-    ref = oracle_result(p, nthreads=16)
-    out, lse, plan, _ = run(p, force_mode=route, num_splits=32)
-    assert_close(out, lse, *ref, what=f"batch1_long {route}")
+    return p, oracle_result(p, nthreads=16)
+
+
+@pytest.fixture(scope="module")
+def mixed_ref():
+    p = wl.mixed()
+    return p, oracle_result(p, nthreads=16)
+
+
+@pytest.mark.parametrize("math", MATHS)
+@pytest.mark.parametrize("route", ["split_queue", "persistent"])
+def test_batch1_long_32k(route, math, batch1_long_ref):
+    p, ref = batch1_long_ref
+    out, lse, plan, _ = run(p, force_mode=route, num_splits=32, math=math)
+    assert_close(out, lse, *ref, what=f"batch1_long {route} {math}")
     info = plan.info()
     assert info["chunk_pages"] == 64 and info["num_work_items"] == 256
     assert np.array_equal(plan.queue(), expected_queue(p, info))
     assert plan.status() == 0
 
 
+@pytest.mark.parametrize("math", MATHS)
 @pytest.mark.parametrize("route", ["split_queue", "split_padded", "persistent", "auto"])
-def test_mixed_batch(route):
-    p = wl.mixed()
-    ref = oracle_result(p, nthreads=16)
-    out, lse, plan, _ = run(p, force_mode=route)
-    assert_close(out, lse, *ref, what=f"mixed {route}")
+def test_mixed_batch(route, math, mixed_ref):
+    p, ref = mixed_ref
+    out, lse, plan, _ = run(p, force_mode=route, math=math)
+    assert_close(out, lse, *ref, what=f"mixed {route} {math}")
     assert np.array_equal(plan.queue(), expected_queue(p, plan.info()))
     assert plan.status() == 0
 
@@ -180,8 +210,10 @@ def test_mixed_batch(route):
 def test_high_batch_policy_chooses_direct():
     p = wl.high_batch()
     ref = oracle_result(p, nthreads=16)
-    out, lse, plan, _ = run(p)
-    assert plan.info()["mode_name"] == "direct"
-    assert plan.info()["launches_per_step"] == 1
-    assert_close(out, lse, *ref, what="high_batch")
-    assert plan.status() == 0
+    dev = to_device(p)
+    for math in MATHS:
+        out, lse, plan, _ = run(p, dev=dev, math=math)
+        assert plan.info()["mode_name"] == "direct"
+        assert plan.info()["launches_per_step"] == 1
+        assert_close(out, lse, *ref, what=f"high_batch {math}")
+        assert plan.status() == 0
