@@ -261,6 +261,35 @@ int pkv_pool_release(pkv_pool_t pool, const int32_t *pages, int32_t count);
 int32_t pkv_pool_free_count(pkv_pool_t pool);
 void pkv_pool_destroy(pkv_pool_t pool);
 
+/*
+ * pkv_decode_static: decode attention for callers that cannot allocate device
+ * memory.  The PersistentKV summary has no counterpart; this is a deployment
+ * variant.  Code that runs inside another framework's memory budget, real-time
+ * loops that must not touch the allocator, and hosts that forbid cudaMalloc
+ * after start-up cannot build a plan (pkv_plan allocates).  This call needs
+ * none: it runs the padded split route with fused merge and keeps its split
+ * workspace, arrival counters and status word in one fixed device array of
+ * PKV_STATIC_SCRATCH_BYTES that the library declares at file scope (every GPU
+ * that loads the library holds it until the process exits).  It calls no
+ * allocating routine.
+ *   q, k_pages, v_pages, block_table_d, seq_lens_d, out, lse: as in pkv_decode
+ *   max_seq_len  host upper bound on every seq_lens_d[b]; rows longer than it
+ *                are poisoned with NaN
+ *   num_splits   S; chunk C = ceil(ceil(max_seq_len / page_size) / S) pages
+ * Needs B * Hkv * S_max * G * (D + 1) * 4 bytes of workspace plus a few KB of
+ * counters within PKV_STATIC_SCRATCH_BYTES; larger problems get PKV_ENOSPACE.
+ * The first call on a device (with that device current) looks the array's
+ * device address up with cudaGetSymbolAddress; make that first call before any
+ * stream capture.  All calls on a device share the array and it keeps the last
+ * call's contents (counters are cleared on `stream` by each call), so calls
+ * that overlap on the GPU race: keep them ordered on one stream.  Device-side
+ * faults poison outputs with NaN; there is no status read-back.
+ */
+#define PKV_STATIC_SCRATCH_BYTES (8u * 1024u * 1024u)
+int pkv_decode_static(const void *q, const void *k_pages, const void *v_pages, const int32_t *block_table_d,
+                      const int32_t *seq_lens_d, int32_t page_size, const pkv_geom *geom, int32_t max_seq_len,
+                      int32_t num_splits, float *out, float *lse, pkv_stream_t stream);
+
 const char *pkv_strerror(int code);
 /* The CUDA error code behind the last PKV_ECUDA on this thread (0 if none). */
 int pkv_last_cuda_error(void);

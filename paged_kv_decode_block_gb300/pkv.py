@@ -83,6 +83,7 @@ SIGNATURES = {
     "pkv_pool_release": (ctypes.c_int, [_P, _I32P, _I32]),
     "pkv_pool_free_count": (ctypes.c_int32, [_P]),
     "pkv_pool_destroy": (None, [_P]),
+    "pkv_decode_static": (ctypes.c_int, [_P, _P, _P, _P, _P, _I32, ctypes.POINTER(Geom), _I32, _I32, _P, _P, _P]),
     "pkv_strerror": (ctypes.c_char_p, [ctypes.c_int]),
     "pkv_last_cuda_error": (ctypes.c_int, []),
 }
@@ -278,6 +279,25 @@ def decode(q, k_pages, v_pages, block_table, seq_lens, plan: Plan, out, lse, str
                            _dev_ptr(out, "out", (torch.float32,)), _dev_ptr(lse, "lse", (torch.float32,)),
                            _stream_handle(stream))
     _check(rc, "pkv_decode")
+
+
+STATIC_SCRATCH_BYTES = 8 * 1024 * 1024
+
+
+def decode_static(q, k_pages, v_pages, block_table, seq_lens, out, lse, *, page_size, max_seq_len,
+                  num_splits, num_pages, stream=None):
+    """pkv_decode_static: decode attention that allocates nothing (see include/pkv.h)."""
+    import torch
+    bf = _bf16_types()
+    B, Hq, D = q.shape
+    g = _geom(B, Hq, k_pages.shape[2], D, block_table.shape[1], num_pages)
+    rc = load().pkv_decode_static(_dev_ptr(q, "q", bf), _dev_ptr(k_pages, "k_pages", bf),
+                                  _dev_ptr(v_pages, "v_pages", bf),
+                                  _dev_ptr(block_table, "block_table", (torch.int32,)),
+                                  _dev_ptr(seq_lens, "seq_lens", (torch.int32,)), int(page_size), ctypes.byref(g),
+                                  int(max_seq_len), int(num_splits), _dev_ptr(out, "out", (torch.float32,)),
+                                  _dev_ptr(lse, "lse", (torch.float32,)), _stream_handle(stream))
+    _check(rc, "pkv_decode_static")
 
 
 def append(k_new, v_new, k_pages, v_pages, block_table, seq_lens, plan: Plan, stream=None):
