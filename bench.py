@@ -350,6 +350,139 @@ def run_pkv(args):
         dist.destroy_process_group()
 
 
+# ----------------------------------------------------------------------------- continuous sessions
+
+def run_continuous(args):
+    """56 sessions; every step appends one K/V token per session (a fresh page from
+    the pool when one fills), re-plans on the host and decodes with the persistent
+    queue kernel.  Device time per step covers append + host re-plan + decode (the
+    GPU waits while the host plans, as a serving loop would); wall time adds the
+    host-side pool work and a synchronise.  Each step reads ~1 GB of KV, far more
+    than L2, so no flush is needed between steps."""
+    import torch
+    from paged_kv_decode_block_gb300 import pkv
+    from paged_kv_decode_block_gb300 import workloads as wl
+    from paged_kv_decode_block_gb300.session import ContinuousSessions
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    pkv.load()
+    steps = args.steps
+    total = args.warmup + steps
+    p = wl.continuous(steps=total)
+    sess = ContinuousSessions(p, force_mode="persistent", num_splits=1, math=args.math, copy=args.copy)
+    rng = np.random.default_rng(wl.HELD_OUT_SEED + 1)
+    toks = [wl.new_tokens(rng, p.B, p.Hkv, p.D) for _ in range(total)]
+    k_new = torch.from_numpy(np.stack([t[0] for t in toks]).view(np.int16)).cuda()
+    v_new = torch.from_numpy(np.stack([t[1] for t in toks]).view(np.int16)).cuda()
+    stream = torch.cuda.current_stream()
+
+    # correctness gate on the first step
+    sess.step(k_new[0], v_new[0])
+    torch.cuda.synchronize()
+    if sess.plan.status() != 0:
+        raise SystemExit("device status word set on the parity step")
+    import oracle
+    table0 = sess.table_h.numpy().copy()
+    k0, v0, lens0 = oracle.append(toks[0][0], toks[0][1], p.k_pages, p.v_pages, table0, p.seq_lens)
+    ref_out, ref_lse = oracle.decode(p.q, k0, v0, table0, lens0, nthreads=host_cores())
+    del k0, v0
+    err_out = float(np.max(np.abs(sess.out.cpu().numpy() - ref_out)))
+    err_lse = float(np.max(np.abs(sess.lse.cpu().numpy() - ref_lse)))
+    log(f"parity vs oracle (step 0): max|out|={err_out:.3g} max|lse|={err_lse:.3g}")
+    if err_out > 2e-3 or err_lse > 1e-4:
+        raise SystemExit("parity gate failed; not timing")
+
+    for i in range(1, args.warmup):
+        sess.step(k_new[i], v_new[i])
+    torch.cuda.synchronize()
+    sess.plan.profile(True)
+    dev_us, wall_us, kv, attn_ms = [], [], [], []
+    with ClockSampler(smi_index(local)) as clk:
+        time.sleep(0.3)
+        torch.cuda.synchronize()
+        t_region = time.perf_counter()
+        for i in range(args.warmup, total):
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            t0 = time.perf_counter()
+            a.record(stream)
+            sess.step(k_new[i], v_new[i])
+            b.record(stream)
+            b.synchronize()
+            wall_us.append((time.perf_counter() - t0) * 1e6)
+            dev_us.append(a.elapsed_time(b) * 1e3)
+            attn_ms.append(sess.plan.profile_read()[0])
+            kv.append(sess.kv_bytes())
+        t_region = time.perf_counter() - t_region
+        time.sleep(0.3)
+    sess.plan.profile(False)
+    kv_total = float(np.sum(kv))
+    value = kv_total / (np.sum(dev_us) * 1e-6) / 1e9
+    peak, peak_src = hbm_peak()
+    achieved = float(np.mean([(k + p.B * p.Hq * p.D * 2) / (t * 1e-3) / 1e9 for k, t in zip(kv, attn_ms)]))
+    clocks = clk.summary()
+
+    # end to end: new tokens and q from pinned host memory each step, outputs back to the host
+    kh = torch.from_numpy(np.stack([t[0] for t in toks[:8]]).view(np.int16)).pin_memory()
+    vh = torch.from_numpy(np.stack([t[1] for t in toks[:8]]).view(np.int16)).pin_memory()
+    qh = torch.from_numpy(p.q.view(np.int16)).pin_memory()
+    oh = torch.empty(sess.out.shape, dtype=torch.float32).pin_memory()
+    lh = torch.empty(sess.lse.shape, dtype=torch.float32).pin_memory()
+    kd, vd = torch.empty_like(k_new[0]), torch.empty_like(v_new[0])
+    e2e = []
+    for i in range(min(8, steps)):
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        kd.copy_(kh[i], non_blocking=True)
+        vd.copy_(vh[i], non_blocking=True)
+        sess.q.copy_(qh, non_blocking=True)
+        sess.step(kd, vd)
+        oh.copy_(sess.out, non_blocking=True)
+        lh.copy_(sess.lse, non_blocking=True)
+        torch.cuda.synchronize()
+        e2e.append(time.perf_counter() - t0)
+    e2e_med = statistics.median(e2e)
+
+    info = sess.plan.info()
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": steps,
+        "warmup": args.warmup, "ms_per_step": round(statistics.median(dev_us) / 1e3, 5),
+        "us_per_step": {"device_p50": round(float(np.percentile(dev_us, 50)), 2),
+                        "device_p99": round(float(np.percentile(dev_us, 99)), 2),
+                        "wall_p50": round(float(np.percentile(wall_us, 50)), 2),
+                        "wall_p99": round(float(np.percentile(wall_us, 99)), 2)},
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16 in, fp32 accumulate", "data": "synthetic (seeded, bf16 ~N(0,1))",
+        "config": {"workload": p.name, "sessions": p.B, "seq_lens": "U[1024, 8192] + appended",
+                   "q_heads": p.Hq, "kv_heads": p.Hkv, "head_dim": p.D, "page_size": p.page_size,
+                   "num_pages": p.num_pages, "mode": info["mode_name"], "math": args.math, "copy": args.copy,
+                   "tiles": info["num_work_items"], "grid_ctas": info["grid_ctas"],
+                   "launches_per_step": 1 + info["launches_per_step"],
+                   "l2": "not flushed: each step reads ~1 GB of KV, far above L2",
+                   "step": "append + host re-plan + persistent decode"},
+        "kv_bytes_per_step": int(np.mean(kv)),
+        "kernel_ms": {"attention_mean": round(float(np.mean(attn_ms)), 5)},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "peak_source": peak_src,
+                     "kernel": "attention_kernel (persistent queue drain)",
+                     "algorithmic_bytes_per_launch": int(np.mean(kv)) + p.B * p.Hq * p.D * 2,
+                     "traffic": profiled_traffic(args.workload)},
+        "e2e": {"value": round(float(np.mean(kv)) / e2e_med / 1e9, 2), "unit": "GB/s",
+                "us_per_step": round(e2e_med * 1e6, 2),
+                "h2d_bytes_per_step": 2 * p.B * p.Hkv * p.D * 2 + p.B * p.Hq * p.D * 2,
+                "d2h_bytes_per_step": p.B * p.Hq * (p.D + 1) * 4},
+        "gpu_launches": (1 + info["launches_per_step"]) * steps,
+        "cpu_baseline": None,
+        "clocks": {"sm_mhz": clocks["sm_mhz"], "sm_max_mhz": clocks["sm_max_mhz"],
+                   "reasons": clocks["reasons"], "samples": clocks["samples"]},
+        "timed_region_wall_s": round(t_region, 4),
+        "parity": {"max_abs_out": err_out, "max_abs_lse": err_lse, "checked_step": 0},
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
 # ----------------------------------------------------------------------------- reference arm
 
 def run_reference(args):
@@ -388,7 +521,7 @@ def main():
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--workload", default="batch1_long",
-                    choices=["batch1_long", "mixed", "mixed_padded", "high_batch", "tiny"])
+                    choices=["batch1_long", "mixed", "mixed_padded", "high_batch", "tiny", "continuous"])
     ap.add_argument("--impl", default="pkv", choices=["pkv", "reference"])
     ap.add_argument("--math", default="auto", choices=["auto", "fma", "mma"],
                     help="block reduction: tensor cores (mma.sync) or CUDA-core FMA")
@@ -402,6 +535,8 @@ def main():
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":
         run_reference(args)
+    elif args.workload == "continuous":
+        run_continuous(args)
     else:
         run_pkv(args)
 

@@ -16,14 +16,17 @@ from __future__ import annotations
 import numpy as np
 
 
-def append(k_new, v_new, k_pages, v_pages, block_table, seq_lens):
-    """Returns updated copies (k_pages, v_pages, seq_lens).
+def append(k_new, v_new, k_pages, v_pages, block_table, seq_lens, inplace=False):
+    """Returns (k_pages, v_pages, seq_lens) after the append: updated copies, or the
+    given arrays themselves updated in place when inplace=True (for long runs over
+    large pools).
 
     k_new, v_new: [B][Hkv][D]; pages: [NP][ps][Hkv][D]; block_table [B][max_pages].
     Raises ValueError when a row has no room or its page id is out of range."""
-    k_pages = np.array(k_pages, copy=True)
-    v_pages = np.array(v_pages, copy=True)
-    seq_lens = np.array(seq_lens, dtype=np.int32, copy=True)
+    if not inplace:
+        k_pages = np.array(k_pages, copy=True)
+        v_pages = np.array(v_pages, copy=True)
+        seq_lens = np.array(seq_lens, dtype=np.int32, copy=True)
     num_pages, page_size = k_pages.shape[0], k_pages.shape[1]
     for b in range(seq_lens.shape[0]):
         pos = int(seq_lens[b])

@@ -5,9 +5,9 @@ dotwave.ai: a fixed cohort of sessions advancing together; its page arenas are
 fixed pools, "What has to exist instead"):
   1. host: the page pool hands a fresh page to every row whose next token starts
      a page (pkv_pool_reserve); the changed block table goes to the device;
-  2. device: pkv_append writes each row's new K/V token and bumps seq_lens;
-  3. host: the plan is rebuilt for the new lengths (pkv_plan_update, same
-     buffers, so device addresses stay fixed);
+  2. host: the plan is rebuilt for the lengths after the append
+     (pkv_plan_update, same buffers, so device addresses stay fixed);
+  3. device: pkv_append writes each row's new K/V token and bumps seq_lens;
   4. device: pkv_decode runs attention for every row.
 This module only sequences those C-ABI calls and keeps the host mirrors of the
 lengths and the table; all arithmetic runs in the library's kernels.
@@ -40,6 +40,7 @@ class ContinuousSessions:
                              max_pages=p.max_pages, num_pages=p.num_pages, **plan_opts)
         self._table_copied = torch.cuda.Event()
         self._table_copied.record()
+        torch.cuda.synchronize()
 
     def step(self, k_new: torch.Tensor, v_new: torch.Tensor, q: torch.Tensor | None = None, stream=None):
         """Append one token per row, then decode.  k_new/v_new: device bf16 [B][Hkv][D]."""
@@ -50,9 +51,11 @@ class ContinuousSessions:
             with torch.cuda.stream(s):
                 self.table_d.copy_(self.table_h, non_blocking=True)
                 self._table_copied.record(s)
-        pkv.append(k_new, v_new, self.k, self.v, self.table_d, self.lens_d, self.plan, stream=s)
+        # plan for the lengths after the append before launching anything, so that
+        # append and decode reach the GPU back to back
         self.lens_h += 1
         self.plan.update(self.lens_h)
+        pkv.append(k_new, v_new, self.k, self.v, self.table_d, self.lens_d, self.plan, stream=s)
         pkv.decode(self.q if q is None else q, self.k, self.v, self.table_d, self.lens_d, self.plan,
                    self.out, self.lse, stream=s)
         return len(rows)

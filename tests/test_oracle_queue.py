@@ -119,3 +119,16 @@ def test_append_rejects_full_row():
     kn, vn = wl.new_tokens(np.random.default_rng(0), 1, 1, 8)
     with pytest.raises(ValueError):
         oracle.append(kn, vn, p.k_pages, p.v_pages, p.block_table, p.seq_lens)
+
+
+def test_append_in_place_equals_copying_append():
+    p = wl.make_problem("inplace", [15, 16, 3], Hq=2, Hkv=1, D=8, page_size=16, num_pages=6,
+                        max_pages=2, seed=9)
+    table = p.block_table.copy()
+    table[1, 1] = p.free_pages[0]
+    kn, vn = wl.new_tokens(np.random.default_rng(10), 3, 1, 8)
+    k2, v2, l2 = oracle.append(kn, vn, p.k_pages, p.v_pages, table, p.seq_lens)
+    k3, v3, l3 = p.k_pages.copy(), p.v_pages.copy(), p.seq_lens.copy()
+    r = oracle.append(kn, vn, k3, v3, table, l3, inplace=True)
+    assert r[0] is k3 and r[1] is v3 and r[2] is l3
+    assert np.array_equal(k2, k3) and np.array_equal(v2, v3) and np.array_equal(l2, l3)
