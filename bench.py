@@ -209,6 +209,8 @@ def run_pkv(args):
 
     p, opts = build_workload(args.workload)
     opts = dict(opts, math=args.math, separate_merge=args.separate_merge, copy=args.copy)
+    if args.num_splits is not None:
+        opts["num_splits"] = args.num_splits
     q = torch.from_numpy(p.q.view(np.int16)).to(dev)
     k = torch.from_numpy(p.k_pages.view(np.int16)).to(dev)
     v = torch.from_numpy(p.v_pages.view(np.int16)).to(dev)
@@ -526,6 +528,8 @@ def main():
     ap.add_argument("--math", default="auto", choices=["auto", "fma", "mma"],
                     help="block reduction: tensor cores (mma.sync) or CUDA-core FMA")
     ap.add_argument("--separate-merge", action="store_true", help="merge splits in a second launch")
+    ap.add_argument("--num-splits", type=int, default=None,
+                    help="override the workload's split count (0 = the planner's policy)")
     ap.add_argument("--copy", default="auto", choices=["auto", "lsu", "tma"],
                     help="K/V staging: cp.async from the producer warp, or TMA boxes")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time for the CPU baseline")

@@ -13,7 +13,8 @@
 //     28-SM GPU; here they are restated in SM units: a batch whose B * Hkv
 //     (row, KV head) units already fill `direct_units_per_sm` CTAs per SM runs
 //     the single-pass DIRECT kernel (the summary's high-batch route), anything
-//     smaller is split so that the tiles fill `target_ctas_per_sm` CTAs per SM.
+//     smaller is split into the smallest page chunks whose tiles still fit one
+//     wave of `target_ctas_per_sm` CTAs per SM.
 // Split rule (the summary states none exactly): boundaries on pages, one chunk
 // of C pages per plan, row b gets S_b = ceil(P_b / C) splits, split s covers
 // pages [s*C, min((s+1)*C, P_b)); a requested split count S gives
@@ -139,10 +140,21 @@ int compute_plan(const pkv_geom& g, int32_t ps, const int32_t* lens, const Optio
     }
     const int64_t units = static_cast<int64_t>(B) * Hkv;
     const bool big_batch = units >= static_cast<int64_t>(o.direct_units_per_sm) * num_sms;
+    // Smallest chunk (most parallelism) whose tiles still fit one wave of
+    // target_ctas_per_sm CTAs per SM: ceil() per row adds up to one tile per
+    // (row, KV head) beyond Hkv * P_total / C, and a second, mostly empty wave
+    // would cost as much as the first.
     auto policy_chunk = [&]() -> int64_t {
         if (big_batch) return std::max<int64_t>(p_max, 1);
         const int64_t target = std::max<int64_t>(1, static_cast<int64_t>(o.target_ctas_per_sm) * num_sms);
-        return std::max<int64_t>(o.min_chunk_pages, ceil_div(Hkv * p_total, target));
+        int64_t c = std::max<int64_t>(o.min_chunk_pages, ceil_div(Hkv * p_total, target));
+        while (c < p_max) {
+            int64_t tiles = 0;
+            for (int b = 0; b < B; ++b) tiles += Hkv * ceil_div(pages[b], c);
+            if (tiles <= target) break;
+            ++c;
+        }
+        return c;
     };
 
     int64_t chunk;

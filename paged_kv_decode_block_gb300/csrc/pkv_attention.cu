@@ -745,21 +745,30 @@ __device__ void merge_unit_bulk(Smem<D, G>& sm, const AttnParams& p, int b, int 
     }
     for (int i = tid; i < ns * G; i += nthreads) w[i] = __ldcg(p.ws_lse + base * G + i);
     __syncthreads();
-    if (tid < G) {
+    // per head: max and sum over the splits, one warp per head
+    const int warp = tid / 32, lane = tid % 32;
+    for (int g = warp; g < G; g += nthreads / 32) {
         float M = -INFINITY;
         bool nan = false;
-        for (int s = 0; s < ns; ++s) {
-            nan |= isnan(w[s * G + tid]);
-            M = fmaxf(M, w[s * G + tid]);
+        for (int s = lane; s < ns; s += 32) {
+            nan |= isnan(w[s * G + g]);
+            M = fmaxf(M, w[s * G + g]);
         }
+#pragma unroll
+        for (int x = 16; x > 0; x >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, x));
+        nan = __any_sync(kFull, nan);
         float wsum = 0.f;
         if (M != -INFINITY)
-            for (int s = 0; s < ns; ++s) wsum += exp2f(w[s * G + tid] - M);
-        sm.merge_m[tid] = M;
-        sm.merge_inv[tid] = M != -INFINITY ? 1.f / wsum : 0.f;
-        if (nan) sm.merge_nan = 1;
-        const float lse2 = M != -INFINITY ? M + log2f(wsum) : -INFINITY;
-        p.lse[static_cast<size_t>(b) * p.Hq + kvh * G + tid] = nan ? NAN : lse2 * kLn2;
+            for (int s = lane; s < ns; s += 32) wsum += exp2f(w[s * G + g] - M);
+#pragma unroll
+        for (int x = 16; x > 0; x >>= 1) wsum += __shfl_xor_sync(kFull, wsum, x);
+        if (lane == 0) {
+            sm.merge_m[g] = M;
+            sm.merge_inv[g] = M != -INFINITY ? 1.f / wsum : 0.f;
+            if (nan) sm.merge_nan = 1;
+            const float lse2 = M != -INFINITY ? M + log2f(wsum) : -INFINITY;
+            p.lse[static_cast<size_t>(b) * p.Hq + kvh * G + g] = nan ? NAN : lse2 * kLn2;
+        }
     }
     __syncthreads();
     for (int i = tid; i < ns * G; i += nthreads) {
@@ -972,18 +981,23 @@ __device__ void run_tile(Smem<D, G>& sm, const AttnParams& p, const TileWork& tw
 // arrive merges all of them (all CTA threads call this).
 template <int D, int G>
 __device__ void merge_if_last(Smem<D, G>& sm, const AttnParams& p, const TileWork& tw, int ns) {
-    __threadfence();
+    // The CTA's partial is written; after the barrier, thread 0's fence makes those
+    // writes visible device-wide before its arrival is counted (release), and after
+    // the arrival its fence orders the other splits' writes before our reads (acquire).
     __syncthreads();
     if (threadIdx.x == 0) {
         const int u = tw.b * p.Hkv + tw.kvh;
+        __threadfence();
         const uint32_t prev = atomicAdd(&p.arrive[u], 1u);
         const int last = prev == static_cast<uint32_t>(ns - 1);
-        if (last) p.arrive[u] = 0;   // ready for the next launch
+        if (last) {
+            p.arrive[u] = 0;   // ready for the next launch
+            __threadfence();
+        }
         sm.tile_slot[1] = last;
     }
     __syncthreads();
     if (sm.tile_slot[1]) {
-        __threadfence();
         // the stage buffers are idle here and serve as the merge's scratch
         static_assert(2 * Cfg<D, G>::kStages * Cfg<D, G>::kMatBytes >= kMergeCapFloats * 4 + 2 * G * D * 4,
                       "merge scratch");

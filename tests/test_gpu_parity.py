@@ -93,7 +93,11 @@ def test_separate_merge_launch(route):
     assert_close(out, lse, *ref, what=f"separate merge {route}")
     out2, lse2, plan2, _ = run(p, force_mode=route, num_splits=4)
     assert plan2.info()["launches_per_step"] == 1
-    assert np.array_equal(out, out2) and np.array_equal(lse, lse2)
+    assert_close(out2, lse2, *ref, what=f"fused merge {route}")
+    # the two merges sum in different orders; they agree far inside the tolerance
+    assert np.max(np.abs(out - out2)) <= 1e-5
+    fin = np.isfinite(lse)
+    assert np.array_equal(fin, np.isfinite(lse2)) and np.max(np.abs(lse[fin] - lse2[fin])) <= 1e-5
 
 
 @pytest.mark.parametrize("page_size", [32, 64])
