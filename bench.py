@@ -55,6 +55,17 @@ def dist_env():
     return rank, world, local
 
 
+def reduce_max(values, dist, device):
+    """Element-wise maximum of a list of floats over all ranks (the slowest rank
+    sets the time of a multi-GPU step); returns the list unchanged on one rank."""
+    if dist is None or not dist.is_available() or not dist.is_initialized() or dist.get_world_size() == 1:
+        return list(values)
+    import torch
+    t = torch.tensor(list(values), dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t.cpu()]
+
+
 def hbm_peak():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -267,10 +278,7 @@ def run_pkv(args):
     attn_ms = statistics.mean(km[0] for km in kernel_ms)
     merge_ms = statistics.mean(km[1] for km in kernel_ms) if info["launches_per_step"] > 1 else 0.0
 
-    if world > 1:
-        t = torch.tensor([med_ms, attn_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        med_ms, attn_ms = float(t[0]), float(t[1])
+    med_ms, attn_ms = reduce_max([med_ms, attn_ms], dist, dev)
 
     kv = info["kv_bytes"]
     q_bytes = p.B * p.Hq * p.D * 2
@@ -300,10 +308,7 @@ def run_pkv(args):
             e2e_s.append(time.perf_counter() - t0)
     e2e_med = statistics.median(e2e_s)
     upload = 4 * (5 * info["num_work_items"] + 2 * p.B) if info["mode"] != pkv.MODE_DIRECT else 0
-    if world > 1:
-        t = torch.tensor([e2e_med], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_med = float(t[0])
+    e2e_med = reduce_max([e2e_med], dist, dev)[0]
 
     cpu = None
     if rank == 0 and world == 1 and not args.skip_cpu:
@@ -385,7 +390,7 @@ def run_continuous(args):
     if sess.plan.status() != 0:
         raise SystemExit("device status word set on the parity step")
     import oracle
-    table0 = sess.table_h.numpy().copy()
+    table0 = sess.table_h.copy()
     k0, v0, lens0 = oracle.append(toks[0][0], toks[0][1], p.k_pages, p.v_pages, table0, p.seq_lens)
     ref_out, ref_lse = oracle.decode(p.q, k0, v0, table0, lens0, nthreads=host_cores())
     del k0, v0

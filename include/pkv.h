@@ -153,6 +153,7 @@ typedef struct {
 
 typedef struct pkv_plan_s *pkv_plan_t;
 typedef struct pkv_pool_s *pkv_pool_t;
+typedef struct pkv_session_s *pkv_session_t;
 
 /*
  * Build a plan: validate the problem, run the policy, enumerate the work tiles
@@ -289,6 +290,32 @@ void pkv_pool_destroy(pkv_pool_t pool);
 int pkv_decode_static(const void *q, const void *k_pages, const void *v_pages, const int32_t *block_table_d,
                       const int32_t *seq_lens_d, int32_t page_size, const pkv_geom *geom, int32_t max_seq_len,
                       int32_t num_splits, float *out, float *lse, pkv_stream_t stream);
+
+/*
+ * Continuous sessions: B rows that each grow by one token per step, advanced
+ * together (the cohort of "WPK persistent kernel", dotwave.ai, "What has to
+ * exist instead": fixed arenas, sessions advanced every beat).
+ *   pkv_session_create   binds a plan (its geometry and options), a page pool,
+ *                        the caller's device table and lengths; copies the host
+ *                        lengths and table into pinned mirrors owned by the
+ *                        session
+ *   pkv_session_step     one step on `stream`: the pool hands a page to every row
+ *                        whose next token starts one and only those table entries
+ *                        are copied to the device; the plan is rebuilt for the
+ *                        lengths after the append; then pkv_append (k_new, v_new
+ *                        device bf16 [B][Hkv][D]) and pkv_decode (q, out, lse) are
+ *                        enqueued back to back.  PKV_ENOSPACE when the pool or a
+ *                        row runs out (nothing is enqueued then)
+ *   pkv_session_lengths / pkv_session_table   copy the host mirrors out
+ * The session does not own the plan, the pool or any device memory.
+ */
+int pkv_session_create(pkv_plan_t plan, pkv_pool_t pool, const int32_t *seq_lens_h, const int32_t *block_table_h,
+                       int32_t *block_table_d, int32_t *seq_lens_d, pkv_session_t *session);
+int pkv_session_step(pkv_session_t session, const void *k_new, const void *v_new, void *k_pages, void *v_pages,
+                     const void *q, float *out, float *lse, pkv_stream_t stream);
+int pkv_session_lengths(pkv_session_t session, int32_t *seq_lens_h);
+int pkv_session_table(pkv_session_t session, int32_t *block_table_h);
+void pkv_session_destroy(pkv_session_t session);
 
 const char *pkv_strerror(int code);
 /* The CUDA error code behind the last PKV_ECUDA on this thread (0 if none). */

@@ -715,3 +715,115 @@ int32_t pkv_pool_free_count(pkv_pool_t pool) { return pool ? static_cast<int32_t
 void pkv_pool_destroy(pkv_pool_t pool) { delete pool; }
 
 }  // extern "C"
+
+// ------------------------------------------------------------------ continuous sessions
+//
+// A cohort of rows that each grow by one token per step, advanced together as
+// the resident program of "WPK persistent kernel" (dotwave.ai) advances its
+// sessions each beat.  One step: the pool hands a page to every row whose next
+// token starts one (only those table entries travel to the device), the plan
+// is rebuilt for the lengths after the append, then append and decode are
+// enqueued back to back.  Host mirrors of lengths and table live in pinned
+// memory; the device table and lengths belong to the caller.
+
+struct pkv_session_s {
+    pkv_plan_t plan = nullptr;
+    pkv_pool_t pool = nullptr;
+    int32_t* lens_h = nullptr;    // pinned [B]
+    int32_t* table_h = nullptr;   // pinned [B][max_pages]
+    int32_t* rows = nullptr;      // [B] scratch for the pool's touched rows
+    int32_t* table_d = nullptr;
+    int32_t* lens_d = nullptr;
+    cudaEvent_t copied = nullptr;   // last table-entry upload has read the mirror
+    bool copy_pending = false;
+};
+
+namespace {
+void session_free(pkv_session_s* s) {
+    if (!s) return;
+    if (s->copy_pending) cudaEventSynchronize(s->copied);
+    cudaFreeHost(s->lens_h);
+    cudaFreeHost(s->table_h);
+    delete[] s->rows;
+    if (s->copied) cudaEventDestroy(s->copied);
+    delete s;
+}
+}  // namespace
+
+extern "C" {
+
+int pkv_session_create(pkv_plan_t plan, pkv_pool_t pool, const int32_t* seq_lens_h, const int32_t* block_table_h,
+                       int32_t* block_table_d, int32_t* seq_lens_d, pkv_session_t* session) {
+    if (!session) return PKV_EINVAL;
+    *session = nullptr;
+    if (!plan || !pool || !block_table_d || !seq_lens_d || (plan->g.batch > 0 && (!seq_lens_h || !block_table_h)))
+        return PKV_EINVAL;
+    const int B = plan->g.batch;
+    const size_t table_n = static_cast<size_t>(B) * plan->g.max_pages_per_seq;
+    int rc = validate_rows(plan->g, plan->page_size, seq_lens_h, block_table_h);
+    if (rc) return rc;
+    pkv_session_s* s = new (std::nothrow) pkv_session_s;
+    if (!s) return PKV_ENOMEM;
+    s->plan = plan;
+    s->pool = pool;
+    s->table_d = block_table_d;
+    s->lens_d = seq_lens_d;
+    s->rows = new (std::nothrow) int32_t[std::max(B, 1)];
+    if (!s->rows || cudaMallocHost(&s->lens_h, sizeof(int32_t) * std::max(B, 1)) != cudaSuccess ||
+        cudaMallocHost(&s->table_h, sizeof(int32_t) * std::max<size_t>(table_n, 1)) != cudaSuccess ||
+        cudaEventCreateWithFlags(&s->copied, cudaEventDisableTiming) != cudaSuccess) {
+        session_free(s);
+        return PKV_ENOMEM;
+    }
+    if (B > 0) {
+        memcpy(s->lens_h, seq_lens_h, sizeof(int32_t) * B);
+        memcpy(s->table_h, block_table_h, sizeof(int32_t) * table_n);
+    }
+    *session = s;
+    return PKV_OK;
+}
+
+int pkv_session_step(pkv_session_t s, const void* k_new, const void* v_new, void* k_pages, void* v_pages,
+                     const void* q, float* out, float* lse, pkv_stream_t stream) {
+    if (!s) return PKV_EINVAL;
+    const pkv_geom& g = s->plan->g;
+    const int B = g.batch, ps = s->plan->page_size, mp = g.max_pages_per_seq;
+    if (B == 0) return PKV_OK;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (s->copy_pending) {
+        PKV_CUDA(cudaEventSynchronize(s->copied));
+        s->copy_pending = false;
+    }
+    int32_t n_rows = 0;
+    int rc = pkv_pool_reserve(s->pool, s->lens_h, s->table_h, B, mp, ps, s->rows, &n_rows);
+    if (rc) return rc;
+    for (int32_t i = 0; i < n_rows; ++i) {
+        const size_t at = static_cast<size_t>(s->rows[i]) * mp + s->lens_h[s->rows[i]] / ps;
+        PKV_CUDA(cudaMemcpyAsync(s->table_d + at, s->table_h + at, sizeof(int32_t), cudaMemcpyHostToDevice, st));
+    }
+    if (n_rows > 0) {
+        PKV_CUDA(cudaEventRecord(s->copied, st));
+        s->copy_pending = true;
+    }
+    for (int b = 0; b < B; ++b) ++s->lens_h[b];
+    if ((rc = pkv_plan_update(s->plan, s->lens_h, nullptr))) return rc;
+    if ((rc = pkv_append(k_new, v_new, k_pages, v_pages, s->table_d, s->lens_d, s->plan, stream))) return rc;
+    return pkv_decode(q, k_pages, v_pages, s->table_d, s->lens_d, s->plan, out, lse, stream);
+}
+
+int pkv_session_lengths(pkv_session_t s, int32_t* seq_lens_h) {
+    if (!s || !seq_lens_h) return PKV_EINVAL;
+    memcpy(seq_lens_h, s->lens_h, sizeof(int32_t) * s->plan->g.batch);
+    return PKV_OK;
+}
+
+int pkv_session_table(pkv_session_t s, int32_t* block_table_h) {
+    if (!s || !block_table_h) return PKV_EINVAL;
+    memcpy(block_table_h, s->table_h, sizeof(int32_t) * static_cast<size_t>(s->plan->g.batch) *
+                                          s->plan->g.max_pages_per_seq);
+    return PKV_OK;
+}
+
+void pkv_session_destroy(pkv_session_t s) { session_free(s); }
+
+}  // extern "C"

@@ -84,6 +84,11 @@ SIGNATURES = {
     "pkv_pool_free_count": (ctypes.c_int32, [_P]),
     "pkv_pool_destroy": (None, [_P]),
     "pkv_decode_static": (ctypes.c_int, [_P, _P, _P, _P, _P, _I32, ctypes.POINTER(Geom), _I32, _I32, _P, _P, _P]),
+    "pkv_session_create": (ctypes.c_int, [_P, _P, _I32P, _I32P, _P, _P, ctypes.POINTER(ctypes.c_void_p)]),
+    "pkv_session_step": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, _P, _P]),
+    "pkv_session_lengths": (ctypes.c_int, [_P, _I32P]),
+    "pkv_session_table": (ctypes.c_int, [_P, _I32P]),
+    "pkv_session_destroy": (None, [_P]),
     "pkv_strerror": (ctypes.c_char_p, [ctypes.c_int]),
     "pkv_last_cuda_error": (ctypes.c_int, []),
 }
@@ -343,6 +348,53 @@ class Pool:
     def close(self):
         if getattr(self, "_h", None) is not None and _lib is not None:
             _lib.pkv_pool_destroy(self._h)
+        self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+class Session:
+    """Continuous sessions (pkv_session_*): every step appends one token per row and
+    decodes.  The plan, pool and device tensors must outlive the session."""
+
+    def __init__(self, plan: Plan, pool: Pool, seq_lens, block_table, block_table_d, seq_lens_d):
+        lens = _i32(seq_lens)
+        table = _i32(block_table)
+        self.B, self.max_pages = table.shape
+        self._keep = (plan, pool, block_table_d, seq_lens_d)
+        h = ctypes.c_void_p()
+        _check(load().pkv_session_create(plan.handle, pool._h, _ptr_i32(lens), _ptr_i32(table),
+                                         _dev_ptr(block_table_d, "block_table_d"),
+                                         _dev_ptr(seq_lens_d, "seq_lens_d"), ctypes.byref(h)),
+               "pkv_session_create")
+        self._h = h
+
+    def step(self, k_new, v_new, k_pages, v_pages, q, out, lse, stream=None):
+        bf = _bf16_types()
+        import torch
+        rc = load().pkv_session_step(self._h, _dev_ptr(k_new, "k_new", bf), _dev_ptr(v_new, "v_new", bf),
+                                     _dev_ptr(k_pages, "k_pages", bf), _dev_ptr(v_pages, "v_pages", bf),
+                                     _dev_ptr(q, "q", bf), _dev_ptr(out, "out", (torch.float32,)),
+                                     _dev_ptr(lse, "lse", (torch.float32,)), _stream_handle(stream))
+        _check(rc, "pkv_session_step")
+
+    def lengths(self) -> np.ndarray:
+        out = np.zeros(self.B, np.int32)
+        _check(load().pkv_session_lengths(self._h, _ptr_i32(out)), "pkv_session_lengths")
+        return out
+
+    def table(self) -> np.ndarray:
+        out = np.zeros((self.B, self.max_pages), np.int32)
+        _check(load().pkv_session_table(self._h, _ptr_i32(out)), "pkv_session_table")
+        return out
+
+    def close(self):
+        if getattr(self, "_h", None) is not None and _lib is not None:
+            _lib.pkv_session_destroy(self._h)
         self._h = None
 
     def __del__(self):

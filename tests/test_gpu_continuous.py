@@ -53,7 +53,8 @@ def test_continuous_sessions(math):
         oracle.append(kn, vn, k_h, v_h, table_h, lens_h, inplace=True)
         if step in CHECK_STEPS:
             torch.cuda.synchronize()
-            assert np.array_equal(sess.table_h.numpy(), table_h), step
+            assert np.array_equal(sess.table_h, table_h), step
+            assert np.array_equal(sess.lens_h, lens_h), step
             assert np.array_equal(sess.lens_d.cpu().numpy(), lens_h), step
             ref_out, ref_lse = oracle.decode(p.q, k_h, v_h, table_h, lens_h, nthreads=16)
             assert_close(sess.out.cpu().numpy(), sess.lse.cpu().numpy(), ref_out, ref_lse,
