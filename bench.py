@@ -222,6 +222,8 @@ def run_pkv(args):
     opts = dict(opts, math=args.math, separate_merge=args.separate_merge, copy=args.copy)
     if args.num_splits is not None:
         opts["num_splits"] = args.num_splits
+    if args.mode is not None:
+        opts["force_mode"] = args.mode
     q = torch.from_numpy(p.q.view(np.int16)).to(dev)
     k = torch.from_numpy(p.k_pages.view(np.int16)).to(dev)
     v = torch.from_numpy(p.v_pages.view(np.int16)).to(dev)
@@ -376,8 +378,10 @@ def run_continuous(args):
     pkv.load()
     steps = args.steps
     total = args.warmup + steps
-    p = wl.continuous(steps=total)
-    sess = ContinuousSessions(p, force_mode="persistent", num_splits=1, math=args.math, copy=args.copy)
+    e2e_steps = min(8, steps)
+    p = wl.continuous(steps=total + e2e_steps)   # room for every appended token, e2e steps included
+    splits = 1 if args.num_splits is None else args.num_splits
+    sess = ContinuousSessions(p, force_mode="persistent", num_splits=splits, math=args.math, copy=args.copy)
     rng = np.random.default_rng(wl.HELD_OUT_SEED + 1)
     toks = [wl.new_tokens(rng, p.B, p.Hkv, p.D) for _ in range(total)]
     k_new = torch.from_numpy(np.stack([t[0] for t in toks]).view(np.int16)).cuda()
@@ -438,7 +442,7 @@ def run_continuous(args):
     lh = torch.empty(sess.lse.shape, dtype=torch.float32).pin_memory()
     kd, vd = torch.empty_like(k_new[0]), torch.empty_like(v_new[0])
     e2e = []
-    for i in range(min(8, steps)):
+    for i in range(e2e_steps):
         torch.cuda.synchronize()
         t0 = time.perf_counter()
         kd.copy_(kh[i], non_blocking=True)
@@ -464,7 +468,8 @@ def run_continuous(args):
         "config": {"workload": p.name, "sessions": p.B, "seq_lens": "U[1024, 8192] + appended",
                    "q_heads": p.Hq, "kv_heads": p.Hkv, "head_dim": p.D, "page_size": p.page_size,
                    "num_pages": p.num_pages, "mode": info["mode_name"], "math": args.math, "copy": args.copy,
-                   "tiles": info["num_work_items"], "grid_ctas": info["grid_ctas"],
+                   "num_splits": info["max_splits"], "tiles": info["num_work_items"],
+                   "grid_ctas": info["grid_ctas"],
                    "launches_per_step": 1 + info["launches_per_step"],
                    "l2": "not flushed: each step reads ~1 GB of KV, far above L2",
                    "step": "append + host re-plan + persistent decode"},
@@ -533,6 +538,8 @@ def main():
     ap.add_argument("--math", default="auto", choices=["auto", "fma", "mma"],
                     help="block reduction: tensor cores (mma.sync) or CUDA-core FMA")
     ap.add_argument("--separate-merge", action="store_true", help="merge splits in a second launch")
+    ap.add_argument("--mode", default=None, choices=["auto", "direct", "split_queue", "split_padded", "persistent"],
+                    help="override the workload's route")
     ap.add_argument("--num-splits", type=int, default=None,
                     help="override the workload's split count (0 = the planner's policy)")
     ap.add_argument("--copy", default="auto", choices=["auto", "lsu", "tma"],

@@ -125,6 +125,7 @@ struct Plan {
     int64_t kv_bytes = 0, ws_bytes = 0, table_bytes = 0;
     std::vector<pkv_work_item> items;   // queue (or padded grid / direct tiles, for inspection)
     std::vector<int32_t> row_start, row_splits;
+    std::vector<int32_t> order;         // persistent route: queue indices, longest tile first
 };
 
 int compute_plan(const pkv_geom& g, int32_t ps, const int32_t* lens, const Options& o, int num_sms,
@@ -229,6 +230,14 @@ int compute_plan(const pkv_geom& g, int32_t ps, const int32_t* lens, const Optio
         else
             r->grid = B > 0 ? std::max(1, std::min<int32_t>(T, num_sms * std::max(1, ctas_per_sm))) : 0;
         r->need_merge = o.separate_merge && any_unfinished;
+        // The persistent grid hands tiles out in this order: longest first (ties in
+        // queue order), so that the long tiles do not start last and set the tail.
+        r->order.resize(T);
+        for (int32_t t = 0; t < T; ++t) r->order[t] = t;
+        if (mode == PKV_MODE_PERSISTENT)
+            std::stable_sort(r->order.begin(), r->order.end(), [&](int32_t a, int32_t b) {
+                return r->items[a].page_end - r->items[a].page_begin > r->items[b].page_end - r->items[b].page_begin;
+            });
     }
     r->ws_bytes = merged_slots * G * (D + 1) * 4 * 2;   // written once, read once
     return PKV_OK;
@@ -361,7 +370,7 @@ int stage(pkv_plan_s* p) {
         cudaFree(p->dev_buf);
         p->host_buf = nullptr;
         p->dev_buf = nullptr;
-        const size_t bytes = (cap * 5 + 2 * static_cast<size_t>(B)) * sizeof(int32_t);
+        const size_t bytes = (cap * 6 + 2 * static_cast<size_t>(B)) * sizeof(int32_t);
         if (cudaMallocHost(&p->host_buf, bytes) != cudaSuccess) return PKV_ENOMEM;
         if (cudaMalloc(&p->dev_buf, bytes) != cudaSuccess) return PKV_ENOMEM;
         p->buf_cap_items = cap;
@@ -378,7 +387,7 @@ int stage(pkv_plan_s* p) {
         if (cudaMalloc(&p->ws_lse, cap * G * sizeof(float)) != cudaSuccess) return PKV_ENOMEM;
         p->ws_cap_slots = cap;
     }
-    // host staging: the queue, then row_start, then row_splits
+    // host staging: the queue, then row_start, row_splits, then the hand-out order
     int32_t* h = p->host_buf;
     memcpy(h, pl.items.data(), items * sizeof(pkv_work_item));
     int32_t* rs = h + p->buf_cap_items * 5;
@@ -386,7 +395,8 @@ int stage(pkv_plan_s* p) {
         memcpy(rs, pl.row_start.data(), B * sizeof(int32_t));
         memcpy(rs + B, pl.row_splits.data(), B * sizeof(int32_t));
     }
-    p->upload_bytes = (p->buf_cap_items * 5 + 2 * static_cast<size_t>(B)) * sizeof(int32_t);
+    if (!pl.order.empty()) memcpy(rs + 2 * B, pl.order.data(), pl.order.size() * sizeof(int32_t));
+    p->upload_bytes = (p->buf_cap_items * 6 + 2 * static_cast<size_t>(B)) * sizeof(int32_t);
     p->dirty = pl.mode != PKV_MODE_DIRECT;
     return PKV_OK;
 }
@@ -545,6 +555,7 @@ int pkv_decode(const void* q, const void* k_pages, const void* v_pages, const in
     a.queue = reinterpret_cast<const pkv_work_item*>(p->dev_buf);
     a.row_start = p->dev_buf + p->buf_cap_items * 5;
     a.row_splits = a.row_start + p->g.batch;
+    a.order = pl.mode == PKV_MODE_PERSISTENT ? a.row_splits + p->g.batch : nullptr;
     a.out = out;
     a.lse = lse;
     a.ws_o = p->ws_o;

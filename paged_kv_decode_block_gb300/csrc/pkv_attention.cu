@@ -1068,7 +1068,7 @@ __global__ void __launch_bounds__(kThreads, MMA ? 2 : 1) attention_kernel(const 
             __syncthreads();
             const int t = sm.tile_slot[0];
             if (t >= p.num_tiles) break;
-            const TileWork tw = tile_from_queue(p, t);
+            const TileWork tw = tile_from_queue(p, p.order ? p.order[t] : t);
             run_tile<D, G, MMA>(sm, p, tw, pipe, &kmap, &vmap);
             const int ntok = tw.t1 > tw.t0 ? tw.t1 - tw.t0 : 0;
             pipe += (ntok + kBlockRows - 1) / kBlockRows;

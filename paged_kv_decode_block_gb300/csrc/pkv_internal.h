@@ -44,6 +44,7 @@ struct AttnParams {
     const pkv_work_item* queue;   // [num_tiles] for queue / persistent routes
     const int32_t* row_start;     // [B] workspace slot of (b, kvh 0, split 0)
     const int32_t* row_splits;    // [B] slots per (b, kvh); 1 = tile finalises in place
+    const int32_t* order;         // persistent route: queue index of the t-th tile handed out (or null)
     float* out;                   // [B][Hq][D]
     float* lse;                   // [B][Hq]
     float* ws_o;                  // [slots][G][D] normalised partial outputs
