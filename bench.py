@@ -379,7 +379,7 @@ def run_continuous(args):
     steps = args.steps
     total = args.warmup + steps
     e2e_steps = min(8, steps)
-    p = wl.continuous(steps=total + e2e_steps)   # room for every appended token, e2e steps included
+    p = wl.continuous(steps=total + e2e_steps + 1)   # room for every appended token (e2e and profiling steps too)
     splits = 1 if args.num_splits is None else args.num_splits
     sess = ContinuousSessions(p, force_mode="persistent", num_splits=splits, math=args.math, copy=args.copy)
     rng = np.random.default_rng(wl.HELD_OUT_SEED + 1)
@@ -404,30 +404,61 @@ def run_continuous(args):
     if err_out > 2e-3 or err_lse > 1e-4:
         raise SystemExit("parity gate failed; not timing")
 
+    if args.device_plan or args.graph:
+        sess.session.device_plan()
+    kbuf = torch.empty_like(k_new[0])
+    vbuf = torch.empty_like(v_new[0])
+    graph = None
+
+    def one_step(i):
+        if graph is None:
+            sess.step(k_new[i], v_new[i])
+        else:   # the captured step reads its tokens from fixed buffers
+            kbuf.copy_(k_new[i])
+            vbuf.copy_(v_new[i])
+            graph.replay()
+
     for i in range(1, args.warmup):
-        sess.step(k_new[i], v_new[i])
+        one_step(i)
     torch.cuda.synchronize()
-    sess.plan.profile(True)
+    if args.graph:
+        side = torch.cuda.Stream()
+        side.wait_stream(stream)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(side):
+            with torch.cuda.graph(graph, stream=side):
+                sess.step(kbuf, vbuf)
+        stream.wait_stream(side)
+        # capturing enqueued nothing; the lengths still match the host's count
+    lens0 = sess.lens_h.astype(np.int64).sum()
+    sess.plan.profile(not args.graph)
     dev_us, wall_us, kv, attn_ms = [], [], [], []
     with ClockSampler(smi_index(local)) as clk:
         time.sleep(0.3)
         torch.cuda.synchronize()
         t_region = time.perf_counter()
-        for i in range(args.warmup, total):
+        for n, i in enumerate(range(args.warmup, total)):
             a = torch.cuda.Event(enable_timing=True)
             b = torch.cuda.Event(enable_timing=True)
             t0 = time.perf_counter()
             a.record(stream)
-            sess.step(k_new[i], v_new[i])
+            one_step(i)
             b.record(stream)
             b.synchronize()
             wall_us.append((time.perf_counter() - t0) * 1e6)
             dev_us.append(a.elapsed_time(b) * 1e3)
-            attn_ms.append(sess.plan.profile_read()[0])
-            kv.append(sess.kv_bytes())
+            if not args.graph:
+                attn_ms.append(sess.plan.profile_read()[0])
+            kv.append(int(lens0 + (n + 1) * p.B) * p.Hkv * p.D * 4)
         t_region = time.perf_counter() - t_region
         time.sleep(0.3)
     sess.plan.profile(False)
+    if args.graph:   # kernel time of the attention launch, from one more profiled eager step
+        sess.plan.profile(True)
+        torch.cuda.synchronize()
+        sess.step(k_new[total - 1], v_new[total - 1])
+        attn_ms = [sess.plan.profile_read()[0]] * len(kv)
+        sess.plan.profile(False)
     kv_total = float(np.sum(kv))
     value = kv_total / (np.sum(dev_us) * 1e-6) / 1e9
     peak, peak_src = hbm_peak()
@@ -470,9 +501,11 @@ def run_continuous(args):
                    "num_pages": p.num_pages, "mode": info["mode_name"], "math": args.math, "copy": args.copy,
                    "num_splits": info["max_splits"], "tiles": info["num_work_items"],
                    "grid_ctas": info["grid_ctas"],
-                   "launches_per_step": 1 + info["launches_per_step"],
+                   "launches_per_step": 1 + info["launches_per_step"] + (1 if args.device_plan or args.graph else 0),
                    "l2": "not flushed: each step reads ~1 GB of KV, far above L2",
-                   "step": "append + host re-plan + persistent decode"},
+                   "step": ("CUDA-graph replay of device plan + append + persistent decode" if args.graph else
+                            "device plan + append + persistent decode" if args.device_plan else
+                            "append + host re-plan + persistent decode")},
         "kv_bytes_per_step": int(np.mean(kv)),
         "kernel_ms": {"attention_mean": round(float(np.mean(attn_ms)), 5)},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
@@ -484,7 +517,7 @@ def run_continuous(args):
                 "us_per_step": round(e2e_med * 1e6, 2),
                 "h2d_bytes_per_step": 2 * p.B * p.Hkv * p.D * 2 + p.B * p.Hq * p.D * 2,
                 "d2h_bytes_per_step": p.B * p.Hq * (p.D + 1) * 4},
-        "gpu_launches": (1 + info["launches_per_step"]) * steps,
+        "gpu_launches": (1 + info["launches_per_step"] + (1 if args.device_plan or args.graph else 0)) * steps,
         "cpu_baseline": None,
         "clocks": {"sm_mhz": clocks["sm_mhz"], "sm_max_mhz": clocks["sm_max_mhz"],
                    "reasons": clocks["reasons"], "samples": clocks["samples"]},
@@ -544,6 +577,10 @@ def main():
                     help="override the workload's split count (0 = the planner's policy)")
     ap.add_argument("--copy", default="auto", choices=["auto", "lsu", "tma"],
                     help="K/V staging: cp.async from the producer warp, or TMA boxes")
+    ap.add_argument("--device-plan", action="store_true",
+                    help="continuous: plan each step on the device (pkv_session_device_plan)")
+    ap.add_argument("--graph", action="store_true",
+                    help="continuous: device-planned step captured once in a CUDA graph and replayed")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time for the CPU baseline")
     ap.add_argument("--skip-cpu", action="store_true")
     args = ap.parse_args()

@@ -317,6 +317,26 @@ int pkv_session_lengths(pkv_session_t session, int32_t *seq_lens_h);
 int pkv_session_table(pkv_session_t session, int32_t *block_table_h);
 void pkv_session_destroy(pkv_session_t session);
 
+/*
+ * Switch a session to device-planned steps (the plan must use the persistent
+ * route).  Allocates the device free list (the pool's remaining pages move to
+ * it, in order), the device plan buffers and a workspace for the largest plan
+ * the table allows; synchronises `stream`.  Afterwards every pkv_session_step
+ * only enqueues work: a one-CTA planner kernel (page allocation in row order,
+ * queue in (b, kvh, s) order, longest-first hand-out order; see
+ * paged_kv_decode_block_gb300/csrc/pkv_devplan.cu), the append, and the
+ * persistent decode over the device-built plan -- no host work and no host
+ * data per step, so a step can be captured once in a CUDA graph and replayed.
+ * The split chunk is fixed at this call (one split per row stays one split).
+ * pkv_session_lengths / pkv_session_table then read the device copies
+ * (synchronising the device).  Up to 2048 rows.
+ */
+int pkv_session_device_plan(pkv_session_t session, pkv_stream_t stream);
+/* Copy the last device-built plan: its tiles in queue order and the hand-out
+ * order (synchronises the device).  *count receives the tile count. */
+int pkv_session_device_queue(pkv_session_t session, pkv_work_item *items, int32_t *order, int32_t capacity,
+                             int32_t *count);
+
 const char *pkv_strerror(int code);
 /* The CUDA error code behind the last PKV_ECUDA on this thread (0 if none). */
 int pkv_last_cuda_error(void);

@@ -22,7 +22,7 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libpkv.so")
 INCLUDE = os.path.join(ROOT, "include")
 
-CUDA_SOURCES = ["pkv_attention.cu", "pkv_append.cu", "pkv_static.cu"]
+CUDA_SOURCES = ["pkv_attention.cu", "pkv_append.cu", "pkv_static.cu", "pkv_devplan.cu"]
 CXX_SOURCES = ["pkv_api.cpp"]
 HEADERS = ["pkv_internal.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

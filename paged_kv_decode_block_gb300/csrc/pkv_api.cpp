@@ -516,9 +516,26 @@ int pkv_plan_queue(pkv_plan_t p, pkv_work_item* items, int32_t capacity, int32_t
     return PKV_OK;
 }
 
-int pkv_decode(const void* q, const void* k_pages, const void* v_pages, const int32_t* block_table_d,
-               const int32_t* seq_lens_d, pkv_plan_t p, float* out, float* lse, pkv_stream_t stream) {
-    if (!p) return PKV_EINVAL;
+}  // extern "C"
+
+namespace {
+
+// A plan built on the device for one step (see pkv_devplan.cu) instead of by
+// the host planner: queue, row table, hand-out order and tile count all live
+// in device memory, written by the planner kernel earlier on the stream.
+struct DevicePlan {
+    const pkv_work_item* queue;
+    const int32_t* row_start;
+    const int32_t* row_splits;
+    const int32_t* order;
+    const int32_t* tiles;
+    int32_t chunk;
+    int32_t max_splits;
+};
+
+int enqueue_decode(pkv_plan_t p, const void* q, const void* k_pages, const void* v_pages,
+                   const int32_t* block_table_d, const int32_t* seq_lens_d, float* out, float* lse, cudaStream_t s,
+                   const DevicePlan* dp) {
     if (p->g.batch == 0) return PKV_OK;
     if (!q || !k_pages || !v_pages || !block_table_d || !seq_lens_d || !out || !lse) return PKV_EINVAL;
     if (!aligned16(q) || !aligned16(k_pages) || !aligned16(v_pages) || !aligned16(out) ||
@@ -528,9 +545,8 @@ int pkv_decode(const void* q, const void* k_pages, const void* v_pages, const in
     int dev = -1;
     PKV_CUDA(cudaGetDevice(&dev));
     if (dev != p->device) return PKV_EINVAL;
-    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
 
-    if (p->dirty) {
+    if (p->dirty && !dp) {
         PKV_CUDA(cudaMemcpyAsync(p->dev_buf, p->host_buf, p->upload_bytes, cudaMemcpyHostToDevice, s));
         PKV_CUDA(cudaEventRecord(p->upload_done, s));
         p->upload_recorded = true;
@@ -556,6 +572,7 @@ int pkv_decode(const void* q, const void* k_pages, const void* v_pages, const in
     a.row_start = p->dev_buf + p->buf_cap_items * 5;
     a.row_splits = a.row_start + p->g.batch;
     a.order = pl.mode == PKV_MODE_PERSISTENT ? a.row_splits + p->g.batch : nullptr;
+    a.tiles_d = nullptr;
     a.out = out;
     a.lse = lse;
     a.ws_o = p->ws_o;
@@ -584,6 +601,21 @@ int pkv_decode(const void* q, const void* k_pages, const void* v_pages, const in
         case PKV_MODE_SPLIT_PADDED: a.route = pkv::kRoutePadded; break;
         default: a.route = pkv::kRoutePersistent; break;
     }
+    int grid = pl.grid;
+    bool need_merge = pl.need_merge;
+    if (dp) {   // persistent route over a device-built plan; the grid is the full SM-sized one
+        a.route = pkv::kRoutePersistent;
+        a.queue = dp->queue;
+        a.row_start = dp->row_start;
+        a.row_splits = dp->row_splits;
+        a.order = dp->order;
+        a.tiles_d = dp->tiles;
+        a.chunk_pages = dp->chunk;
+        a.max_splits = dp->max_splits;
+        a.fused_merge = 1;
+        grid = p->num_sms * std::max(1, p->ctas_per_sm);
+        need_merge = false;
+    }
 
     if (p->profile) {
         for (auto& ev : p->ev)
@@ -591,18 +623,29 @@ int pkv_decode(const void* q, const void* k_pages, const void* v_pages, const in
         PKV_CUDA(cudaEventRecord(p->ev[0], s));
     }
     int n = 0;
-    if (pl.grid > 0) {
-        PKV_CUDA(pkv::launch_attention(a, p->kmap, p->vmap, pl.grid, s));
+    if (grid > 0) {
+        PKV_CUDA(pkv::launch_attention(a, p->kmap, p->vmap, grid, s));
         ++n;
         if (p->profile) PKV_CUDA(cudaEventRecord(p->ev[n], s));
     }
-    if (pl.need_merge) {
+    if (need_merge) {
         PKV_CUDA(pkv::launch_merge(a, s));
         ++n;
         if (p->profile) PKV_CUDA(cudaEventRecord(p->ev[n], s));
     }
     p->ev_launches = n;
     return PKV_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int pkv_decode(const void* q, const void* k_pages, const void* v_pages, const int32_t* block_table_d,
+               const int32_t* seq_lens_d, pkv_plan_t p, float* out, float* lse, pkv_stream_t stream) {
+    if (!p) return PKV_EINVAL;
+    return enqueue_decode(p, q, k_pages, v_pages, block_table_d, seq_lens_d, out, lse,
+                          reinterpret_cast<cudaStream_t>(stream), nullptr);
 }
 
 int pkv_append(const void* k_new, const void* v_new, void* k_pages, void* v_pages, const int32_t* block_table_d,
@@ -747,12 +790,24 @@ struct pkv_session_s {
     int32_t* lens_d = nullptr;
     cudaEvent_t copied = nullptr;   // last table-entry upload has read the mirror
     bool copy_pending = false;
+    // device-planned steps (pkv_session_device_plan)
+    bool device_mode = false;
+    int32_t* dev_free = nullptr;        // free page ids, handed out in order
+    uint32_t* dev_free_state = nullptr; // {next index, pages left}
+    int32_t free_cap = 0;
+    int32_t* dev_plan = nullptr;        // [queue_cap * 5][B][B][queue_cap][1]
+    int32_t queue_cap = 0;
+    int32_t chunk = 0;
+    int32_t max_splits = 0;
 };
 
 namespace {
 void session_free(pkv_session_s* s) {
     if (!s) return;
     if (s->copy_pending) cudaEventSynchronize(s->copied);
+    cudaFree(s->dev_free);
+    cudaFree(s->dev_free_state);
+    cudaFree(s->dev_plan);
     cudaFreeHost(s->lens_h);
     cudaFreeHost(s->table_h);
     delete[] s->rows;
@@ -794,6 +849,91 @@ int pkv_session_create(pkv_plan_t plan, pkv_pool_t pool, const int32_t* seq_lens
     return PKV_OK;
 }
 
+int pkv_session_device_plan(pkv_session_t s, pkv_stream_t stream) {
+    if (!s) return PKV_EINVAL;
+    if (s->device_mode) return PKV_OK;
+    pkv_plan_s* p = s->plan;
+    const pkv_geom& g = p->g;
+    const int B = g.batch, Hkv = g.num_kv_heads, G = g.num_q_heads / g.num_kv_heads;
+    if (p->plan.mode != PKV_MODE_PERSISTENT || B > pkv::kDevPlanMaxRows) return PKV_EUNSUPPORTED;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (s->copy_pending) {
+        PKV_CUDA(cudaEventSynchronize(s->copied));
+        s->copy_pending = false;
+    }
+    // one split per row stays one split however long the rows grow
+    const int32_t chunk = p->opts.num_splits == 1 ? g.max_pages_per_seq : p->plan.chunk;
+    const int32_t s_max = static_cast<int32_t>(ceil_div(g.max_pages_per_seq, chunk));
+    if (static_cast<int64_t>(s_max) * G > pkv::kMergeCapFloats) return PKV_EUNSUPPORTED;
+    const int64_t cap = static_cast<int64_t>(B) * Hkv * s_max;
+    if (cap > INT32_MAX / 8) return PKV_EUNSUPPORTED;
+    // workspace for the largest plan the table allows
+    if (static_cast<size_t>(cap) > p->ws_cap_slots) {
+        cudaFree(p->ws_o);
+        cudaFree(p->ws_lse);
+        p->ws_o = nullptr;
+        p->ws_lse = nullptr;
+        if (cudaMalloc(&p->ws_o, cap * G * g.head_dim * sizeof(float)) != cudaSuccess) return PKV_ENOMEM;
+        if (cudaMalloc(&p->ws_lse, cap * G * sizeof(float)) != cudaSuccess) return PKV_ENOMEM;
+        p->ws_cap_slots = cap;
+    }
+    std::vector<int32_t> pages(s->pool->free_list.begin(), s->pool->free_list.end());
+    const size_t plan_ints = static_cast<size_t>(cap) * 6 + 2 * static_cast<size_t>(B) + 1;
+    if (cudaMalloc(&s->dev_plan, plan_ints * sizeof(int32_t)) != cudaSuccess ||
+        cudaMalloc(&s->dev_free, std::max<size_t>(pages.size(), 1) * sizeof(int32_t)) != cudaSuccess ||
+        cudaMalloc(&s->dev_free_state, 2 * sizeof(uint32_t)) != cudaSuccess)
+        return PKV_ENOMEM;
+    const uint32_t state[2] = {0u, static_cast<uint32_t>(pages.size())};
+    PKV_CUDA(cudaMemcpyAsync(s->dev_free, pages.data(), pages.size() * sizeof(int32_t), cudaMemcpyHostToDevice, st));
+    PKV_CUDA(cudaMemcpyAsync(s->dev_free_state, state, sizeof(state), cudaMemcpyHostToDevice, st));
+    PKV_CUDA(cudaStreamSynchronize(st));   // the host vectors above go out of scope
+    s->pool->free_list.clear();            // those pages now belong to the device allocator
+    s->free_cap = static_cast<int32_t>(std::max<size_t>(pages.size(), 1));
+    s->queue_cap = static_cast<int32_t>(cap);
+    s->chunk = chunk;
+    s->max_splits = s_max;
+    s->device_mode = true;
+    return PKV_OK;
+}
+
+namespace {
+int session_step_device(pkv_session_t s, const void* k_new, const void* v_new, void* k_pages, void* v_pages,
+                        const void* q, float* out, float* lse, cudaStream_t st) {
+    pkv_plan_s* p = s->plan;
+    const pkv_geom& g = p->g;
+    const int B = g.batch;
+    int32_t* q_items = s->dev_plan;
+    int32_t* row_start = q_items + static_cast<size_t>(s->queue_cap) * 5;
+    int32_t* row_splits = row_start + B;
+    int32_t* order = row_splits + B;
+    int32_t* tiles = order + s->queue_cap;
+    pkv::DevPlanParams dp{};
+    dp.lens = s->lens_d;
+    dp.table = s->table_d;
+    dp.free_list = s->dev_free;
+    dp.free_state = s->dev_free_state;
+    dp.free_cap = s->free_cap;
+    dp.queue = reinterpret_cast<pkv_work_item*>(q_items);
+    dp.row_start = row_start;
+    dp.row_splits = row_splits;
+    dp.order = order;
+    dp.tiles = tiles;
+    dp.queue_cap = s->queue_cap;
+    dp.status = &p->ctr->status;
+    dp.B = B;
+    dp.Hkv = g.num_kv_heads;
+    dp.page_size = p->page_size;
+    dp.max_pages = g.max_pages_per_seq;
+    dp.chunk = s->chunk;
+    PKV_CUDA(pkv::launch_plan_step(dp, st));
+    int rc = pkv_append(k_new, v_new, k_pages, v_pages, s->table_d, s->lens_d, p, reinterpret_cast<pkv_stream_t>(st));
+    if (rc) return rc;
+    const DevicePlan plan{reinterpret_cast<const pkv_work_item*>(q_items), row_start, row_splits, order, tiles,
+                          s->chunk, s->max_splits};
+    return enqueue_decode(p, q, k_pages, v_pages, s->table_d, s->lens_d, out, lse, st, &plan);
+}
+}  // namespace
+
 int pkv_session_step(pkv_session_t s, const void* k_new, const void* v_new, void* k_pages, void* v_pages,
                      const void* q, float* out, float* lse, pkv_stream_t stream) {
     if (!s) return PKV_EINVAL;
@@ -801,6 +941,7 @@ int pkv_session_step(pkv_session_t s, const void* k_new, const void* v_new, void
     const int B = g.batch, ps = s->plan->page_size, mp = g.max_pages_per_seq;
     if (B == 0) return PKV_OK;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (s->device_mode) return session_step_device(s, k_new, v_new, k_pages, v_pages, q, out, lse, st);
     if (s->copy_pending) {
         PKV_CUDA(cudaEventSynchronize(s->copied));
         s->copy_pending = false;
@@ -824,14 +965,43 @@ int pkv_session_step(pkv_session_t s, const void* k_new, const void* v_new, void
 
 int pkv_session_lengths(pkv_session_t s, int32_t* seq_lens_h) {
     if (!s || !seq_lens_h) return PKV_EINVAL;
-    memcpy(seq_lens_h, s->lens_h, sizeof(int32_t) * s->plan->g.batch);
+    const size_t bytes = sizeof(int32_t) * s->plan->g.batch;
+    if (s->device_mode) {   // the device holds the truth; synchronises the device
+        PKV_CUDA(cudaDeviceSynchronize());
+        PKV_CUDA(cudaMemcpy(seq_lens_h, s->lens_d, bytes, cudaMemcpyDeviceToHost));
+    } else {
+        memcpy(seq_lens_h, s->lens_h, bytes);
+    }
     return PKV_OK;
 }
 
 int pkv_session_table(pkv_session_t s, int32_t* block_table_h) {
     if (!s || !block_table_h) return PKV_EINVAL;
-    memcpy(block_table_h, s->table_h, sizeof(int32_t) * static_cast<size_t>(s->plan->g.batch) *
-                                          s->plan->g.max_pages_per_seq);
+    const size_t bytes = sizeof(int32_t) * static_cast<size_t>(s->plan->g.batch) * s->plan->g.max_pages_per_seq;
+    if (s->device_mode) {
+        PKV_CUDA(cudaDeviceSynchronize());
+        PKV_CUDA(cudaMemcpy(block_table_h, s->table_d, bytes, cudaMemcpyDeviceToHost));
+    } else {
+        memcpy(block_table_h, s->table_h, bytes);
+    }
+    return PKV_OK;
+}
+
+int pkv_session_device_queue(pkv_session_t s, pkv_work_item* items, int32_t* order, int32_t capacity,
+                             int32_t* count) {
+    if (!s || !count) return PKV_EINVAL;
+    if (!s->device_mode) return PKV_EINVAL;
+    PKV_CUDA(cudaDeviceSynchronize());
+    const int32_t* tiles = s->dev_plan + static_cast<size_t>(s->queue_cap) * 6 + 2 * s->plan->g.batch;
+    int32_t n = 0;
+    PKV_CUDA(cudaMemcpy(&n, tiles, sizeof(int32_t), cudaMemcpyDeviceToHost));
+    *count = n;
+    const int32_t m = std::min(n, capacity);
+    if (items && m > 0)
+        PKV_CUDA(cudaMemcpy(items, s->dev_plan, sizeof(pkv_work_item) * m, cudaMemcpyDeviceToHost));
+    if (order && m > 0)
+        PKV_CUDA(cudaMemcpy(order, s->dev_plan + static_cast<size_t>(s->queue_cap) * 5 + 2 * s->plan->g.batch,
+                            sizeof(int32_t) * m, cudaMemcpyDeviceToHost));
     return PKV_OK;
 }
 

@@ -1062,12 +1062,13 @@ __global__ void __launch_bounds__(kThreads, MMA ? 2 : 1) attention_kernel(const 
     }
 
     if (p.route == kRoutePersistent) {
+        const int num_tiles = p.tiles_d ? *p.tiles_d : p.num_tiles;   // a device-planned step sets it
         uint32_t pipe = 0;
         while (true) {
             if (threadIdx.x == 0) sm.tile_slot[0] = static_cast<int>(atomicAdd(&p.ctr->next_tile, 1u));
             __syncthreads();
             const int t = sm.tile_slot[0];
-            if (t >= p.num_tiles) break;
+            if (t >= num_tiles) break;
             const TileWork tw = tile_from_queue(p, p.order ? p.order[t] : t);
             run_tile<D, G, MMA>(sm, p, tw, pipe, &kmap, &vmap);
             const int ntok = tw.t1 > tw.t0 ? tw.t1 - tw.t0 : 0;

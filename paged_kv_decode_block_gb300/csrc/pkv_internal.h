@@ -45,6 +45,7 @@ struct AttnParams {
     const int32_t* row_start;     // [B] workspace slot of (b, kvh 0, split 0)
     const int32_t* row_splits;    // [B] slots per (b, kvh); 1 = tile finalises in place
     const int32_t* order;         // persistent route: queue index of the t-th tile handed out (or null)
+    const int32_t* tiles_d;       // persistent route: tile count in device memory (overrides num_tiles)
     float* out;                   // [B][Hq][D]
     float* lse;                   // [B][Hq]
     float* ws_o;                  // [slots][G][D] normalised partial outputs
@@ -59,6 +60,27 @@ struct AttnParams {
     int32_t copy_lsu;             // stage K/V with cp.async from the producer warp instead of TMA
     float scale_log2;             // log2(e) / sqrt(D)
 };
+
+// Device planner of a continuous-decoding step (pkv_devplan.cu): page
+// allocation from a device free list, then the plan for the lengths after the
+// append, all on the GPU.
+constexpr int kDevPlanMaxRows = 2048;
+struct DevPlanParams {
+    const int32_t* lens;        // [B] lengths before the append
+    int32_t* table;             // [B][max_pages] device block table (entries filled in)
+    const int32_t* free_list;   // [free_cap] free page ids, handed out in order
+    uint32_t* free_state;       // {next index into free_list, pages still free}
+    int32_t free_cap;
+    pkv_work_item* queue;       // [queue_cap]
+    int32_t* row_start;         // [B]
+    int32_t* row_splits;        // [B]
+    int32_t* order;             // [queue_cap] hand-out order, longest tile first
+    int32_t* tiles;             // [1] tiles in this step's queue
+    int32_t queue_cap;
+    uint32_t* status;
+    int32_t B, Hkv, page_size, max_pages, chunk;
+};
+cudaError_t launch_plan_step(const DevPlanParams& p, cudaStream_t stream);
 
 // Attention launch: one of the four routes.  kmap / vmap are TMA descriptors
 // of the K and V pools viewed as [page_size * num_pages][Hkv][D] (innermost D),

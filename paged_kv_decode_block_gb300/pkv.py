@@ -89,6 +89,8 @@ SIGNATURES = {
     "pkv_session_lengths": (ctypes.c_int, [_P, _I32P]),
     "pkv_session_table": (ctypes.c_int, [_P, _I32P]),
     "pkv_session_destroy": (None, [_P]),
+    "pkv_session_device_plan": (ctypes.c_int, [_P, _P]),
+    "pkv_session_device_queue": (ctypes.c_int, [_P, ctypes.POINTER(WorkItem), _I32P, _I32, _I32P]),
     "pkv_strerror": (ctypes.c_char_p, [ctypes.c_int]),
     "pkv_last_cuda_error": (ctypes.c_int, []),
 }
@@ -391,6 +393,21 @@ class Session:
         out = np.zeros((self.B, self.max_pages), np.int32)
         _check(load().pkv_session_table(self._h, _ptr_i32(out)), "pkv_session_table")
         return out
+
+    def device_plan(self, stream=None):
+        """Switch to device-planned (graph-capturable) steps."""
+        _check(load().pkv_session_device_plan(self._h, _stream_handle(stream)), "pkv_session_device_plan")
+
+    def device_queue(self):
+        """(tiles int32 [n][5], hand-out order int32 [n]) of the last device-built plan."""
+        n = ctypes.c_int32(0)
+        _check(load().pkv_session_device_queue(self._h, None, None, 0, ctypes.byref(n)), "pkv_session_device_queue")
+        items = (WorkItem * max(n.value, 1))()
+        order = np.zeros(max(n.value, 1), np.int32)
+        _check(load().pkv_session_device_queue(self._h, items, _ptr_i32(order), n.value, ctypes.byref(n)),
+               "pkv_session_device_queue")
+        arr = np.ctypeslib.as_array(ctypes.cast(items, _I32P), shape=(max(n.value, 1) * 5,))
+        return arr[: n.value * 5].reshape(-1, 5).copy(), order[: n.value].copy()
 
     def close(self):
         if getattr(self, "_h", None) is not None and _lib is not None:
