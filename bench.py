@@ -248,7 +248,11 @@ def run_pkv(args):
 
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
-    plan.profile(True)
+    # With one launch per step the step's own events bracket exactly that kernel;
+    # extra per-kernel events (needed only for two launches) would add their own
+    # latency to every timed step.
+    per_kernel_events = info["launches_per_step"] > 1
+    plan.profile(per_kernel_events)
     for _ in range(args.warmup):
         flush.zero_()
         pkv.decode(q, k, v, table, lens, plan, out, lse)
@@ -268,7 +272,8 @@ def run_pkv(args):
             starts[i].record(stream)
             pkv.decode(q, k, v, table, lens, plan, out, lse)
             ends[i].record(stream)
-            kernel_ms.append(plan.profile_read())   # waits for this step's kernels
+            if per_kernel_events:
+                kernel_ms.append(plan.profile_read())   # waits for this step's kernels
         torch.cuda.synchronize()
         if world > 1:
             dist.barrier()
@@ -277,8 +282,12 @@ def run_pkv(args):
     plan.profile(False)
     step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     med_ms = statistics.median(step_ms)
-    attn_ms = statistics.mean(km[0] for km in kernel_ms)
-    merge_ms = statistics.mean(km[1] for km in kernel_ms) if info["launches_per_step"] > 1 else 0.0
+    if per_kernel_events:
+        attn_ms = statistics.mean(km[0] for km in kernel_ms)
+        merge_ms = statistics.mean(km[1] for km in kernel_ms)
+    else:
+        attn_ms = statistics.mean(step_ms)
+        merge_ms = 0.0
 
     med_ms, attn_ms = reduce_max([med_ms, attn_ms], dist, dev)
 

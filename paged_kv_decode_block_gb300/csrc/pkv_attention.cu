@@ -295,6 +295,7 @@ struct Smem {
     uint64_t merge_bar;         // completion of the fused merge's bulk copies
     uint32_t merge_phase;       // phases of merge_bar used so far
     int tile_slot[2];
+    int tile_fin, tile_splits;  // the finished tile's finalize flag and split count
 };
 
 template <int D, int G>
@@ -305,10 +306,19 @@ constexpr size_t smem_bytes() {
 struct TileWork {
     int b, kvh;
     int t0, t1;        // token range [t0, t1) of row b (clipped to N_b)
+    int t_stream;      // tokens [t0, t_stream) are streamed (whole planned pages for queue tiles)
+    int split, page_begin, page_end;
     int slot;          // workspace slot (split tiles)
     int finalize;      // 1: write out/lse directly
+    int splits;        // splits of (b, kvh)
     int poisoned;      // plan and device lengths disagree
+    int lazy;          // t1 / slot / finalize / splits / poisoned still to be read (tile_finish)
 };
+
+__device__ __forceinline__ int stream_blocks(const TileWork& tw) {
+    const int n = tw.t_stream > tw.t0 ? tw.t_stream - tw.t0 : 0;
+    return (n + kBlockRows - 1) / kBlockRows;
+}
 
 // ------------------------------------------------------------------ FMA block reduction
 
@@ -817,19 +827,54 @@ __device__ void merge_unit_bulk(Smem<D, G>& sm, const AttnParams& p, int b, int 
 
 // ------------------------------------------------------------------ tile
 
+// Tile of a queue entry: only the entry itself, so the producers can start
+// streaming its planned pages at once (all of them are in the row's table).
+__device__ __forceinline__ TileWork tile_from_item(const AttnParams& p, int t) {
+    const pkv_work_item it = p.queue[t];
+    TileWork tw;
+    tw.b = it.b;
+    tw.kvh = it.kvh;
+    tw.split = it.split;
+    tw.page_begin = it.page_begin;
+    tw.page_end = it.page_end;
+    tw.t0 = it.page_begin * p.page_size;
+    tw.t_stream = it.page_end * p.page_size;
+    tw.t1 = tw.t_stream;
+    tw.slot = 0;
+    tw.finalize = 0;
+    tw.splits = 0;
+    tw.poisoned = 0;
+    tw.lazy = 1;
+    return tw;
+}
+
+// The rest of a queue tile: the row's length clips the token range, and the
+// plan is checked against it (a mismatch poisons the tile and flags it).
+__device__ __forceinline__ void tile_finish(const AttnParams& p, TileWork& tw) {
+    const int n = p.seq_lens[tw.b];
+    const int pages = (n + p.page_size - 1) / p.page_size;
+    tw.splits = p.row_splits[tw.b];
+    const int want_end = min((tw.split + 1) * p.chunk_pages, pages);
+    tw.poisoned = (tw.page_begin != tw.split * p.chunk_pages || tw.page_end != want_end) ? 1 : 0;
+    if (tw.poisoned && threadIdx.x == 0) atomicOr(&p.ctr->status, static_cast<uint32_t>(PKV_DEV_PLAN_MISMATCH));
+    tw.t1 = tw.poisoned ? tw.t0 : min(tw.t_stream, n);
+    tw.finalize = tw.splits == 1;
+    tw.slot = p.row_start[tw.b] + tw.kvh * tw.splits + tw.split;
+    tw.lazy = 0;
+}
+
 // One tile: the producer warp streams blocks, the consumer warps reduce them,
 // then the four warp states are merged and written (to out/lse, or to the
 // workspace for a split).  `pipe` counts blocks this CTA has streamed before
 // (stage/phase bookkeeping continues across the tiles of a persistent CTA).
 template <int D, int G, bool MMA>
-__device__ void run_tile(Smem<D, G>& sm, const AttnParams& p, const TileWork& tw, uint32_t pipe,
+__device__ void run_tile(Smem<D, G>& sm, const AttnParams& p, TileWork tw, uint32_t pipe,
                          const CUtensorMap* kmap, const CUtensorMap* vmap) {
     using C = Cfg<D, G>;
     constexpr int kStages = C::kStages;
     const int warp = threadIdx.x / 32;
     const int lane = threadIdx.x % 32;
-    const int ntok = tw.t1 > tw.t0 ? tw.t1 - tw.t0 : 0;
-    const int nblk = (ntok + kBlockRows - 1) / kBlockRows;
+    const int nblk = stream_blocks(tw);
     uint32_t* status = &p.ctr->status;
 
     if (warp >= kConsumerWarps) {
@@ -838,7 +883,7 @@ __device__ void run_tile(Smem<D, G>& sm, const AttnParams& p, const TileWork& tw
         const int pw = warp - kConsumerWarps;
         const int ps = p.page_size;
         const int first_page = tw.t0 / ps;
-        const int last_page = (tw.t1 + ps - 1) / ps;   // exclusive
+        const int last_page = (tw.t_stream + ps - 1) / ps;   // exclusive
         const int32_t* bt_row = p.block_table + static_cast<size_t>(tw.b) * p.max_pages;
         const uint64_t policy = l2_evict_first_policy();
         int j = 0;   // block index within the tile
@@ -852,7 +897,7 @@ __device__ void run_tile(Smem<D, G>& sm, const AttnParams& p, const TileWork& tw
                 const int page = __shfl_sync(kFull, ids, i);
                 const int page_tok0 = (pg0 + i) * ps;
                 const int lo = max(page_tok0, tw.t0);
-                const int hi = min(page_tok0 + ps, tw.t1);
+                const int hi = min(page_tok0 + ps, tw.t_stream);
                 const bool page_ok = page >= 0 && page < p.num_pages;
                 for (int tok = lo; tok < hi; tok += kBlockRows, ++j) {
                     if (j % kProducerWarps != pw) continue;
@@ -907,6 +952,14 @@ __device__ void run_tile(Smem<D, G>& sm, const AttnParams& p, const TileWork& tw
     }
 
     // ---------------- consumers
+    // (queue tiles: the lengths and row table are read here, while the producers
+    // already stream the planned pages)
+    if (tw.lazy) tile_finish(p, tw);
+    if (threadIdx.x == 0) {
+        sm.tile_fin = tw.finalize;
+        sm.tile_splits = tw.splits;
+    }
+    const int ntok = tw.t1 > tw.t0 ? tw.t1 - tw.t0 : 0;
     int poisoned = tw.poisoned;
     if constexpr (MMA) {
         MmaState<D, G> st;
@@ -915,13 +968,13 @@ __device__ void run_tile(Smem<D, G>& sm, const AttnParams& p, const TileWork& tw
             const uint32_t it = pipe + j;
             const int s = it % kStages;
             const bool ok = mbar_wait(&sm.full[s], (it / kStages) & 1u, status, &sm.abort);
-            if (!ok || sm.bad[s]) {
-                poisoned = 1;
+            const int valid = min(kBlockRows, ntok - j * kBlockRows);
+            if (!ok || sm.bad[s] || valid <= 0) {   // nothing to reduce (or past the row's end)
+                if (!ok || sm.bad[s]) poisoned = 1;
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&sm.empty[s]);
             } else {   // releases the stage itself once the block is in registers
-                mma_block<D, G>(st, sm.k[s], sm.v[s], &sm.empty[s], sm.pt[warp],
-                                min(kBlockRows, ntok - j * kBlockRows), lane, p.scale_log2);
+                mma_block<D, G>(st, sm.k[s], sm.v[s], &sm.empty[s], sm.pt[warp], valid, lane, p.scale_log2);
             }
         }
         mma_publish<D, G>(st, sm, warp, lane);
@@ -932,10 +985,11 @@ __device__ void run_tile(Smem<D, G>& sm, const AttnParams& p, const TileWork& tw
             const uint32_t it = pipe + j;
             const int s = it % kStages;
             const bool ok = mbar_wait(&sm.full[s], (it / kStages) & 1u, status, &sm.abort);
+            const int valid = min(kBlockRows, ntok - j * kBlockRows);
             if (!ok || sm.bad[s])
                 poisoned = 1;
-            else
-                fma_block<D, G>(st, sm.k[s], sm.v[s], sm.p[warp], min(kBlockRows, ntok - j * kBlockRows), lane);
+            else if (valid > 0)
+                fma_block<D, G>(st, sm.k[s], sm.v[s], sm.p[warp], valid, lane);
             __syncwarp();
             if (lane == 0) mbar_arrive(&sm.empty[s]);
         }
@@ -980,13 +1034,13 @@ __device__ void run_tile(Smem<D, G>& sm, const AttnParams& p, const TileWork& tw
 // After a split tile has written its partial: the last split of (b, kvh) to
 // arrive merges all of them (all CTA threads call this).
 template <int D, int G>
-__device__ void merge_if_last(Smem<D, G>& sm, const AttnParams& p, const TileWork& tw, int ns) {
+__device__ void merge_if_last(Smem<D, G>& sm, const AttnParams& p, int b, int kvh, int ns) {
     // The CTA's partial is written; after the barrier, thread 0's fence makes those
     // writes visible device-wide before its arrival is counted (release), and after
     // the arrival its fence orders the other splits' writes before our reads (acquire).
     __syncthreads();
     if (threadIdx.x == 0) {
-        const int u = tw.b * p.Hkv + tw.kvh;
+        const int u = b * p.Hkv + kvh;
         __threadfence();
         const uint32_t prev = atomicAdd(&p.arrive[u], 1u);
         const int last = prev == static_cast<uint32_t>(ns - 1);
@@ -1001,7 +1055,7 @@ __device__ void merge_if_last(Smem<D, G>& sm, const AttnParams& p, const TileWor
         // the stage buffers are idle here and serve as the merge's scratch
         static_assert(2 * Cfg<D, G>::kStages * Cfg<D, G>::kMatBytes >= kMergeCapFloats * 4 + 2 * G * D * 4,
                       "merge scratch");
-        merge_unit_bulk<D, G>(sm, p, tw.b, tw.kvh, ns);
+        merge_unit_bulk<D, G>(sm, p, b, kvh, ns);
     }
 }
 
@@ -1012,26 +1066,6 @@ template <int D, int G>
 __device__ void drain_after_abort(Smem<D, G>& sm, uint32_t* status) {
     for (int s = 0; s < Cfg<D, G>::kStages; ++s)
         if (sm.issued[s] > 0) mbar_wait_slow(&sm.full[s], (sm.issued[s] - 1) & 1u, status, nullptr);
-}
-
-// Tile of a queue entry, with the plan checked against the device lengths.
-__device__ __forceinline__ TileWork tile_from_queue(const AttnParams& p, int t) {
-    const pkv_work_item it = p.queue[t];
-    TileWork tw;
-    tw.b = it.b;
-    tw.kvh = it.kvh;
-    const int n = p.seq_lens[it.b];
-    const int pages = (n + p.page_size - 1) / p.page_size;
-    const int splits = p.row_splits[it.b];
-    const int want_end = min((it.split + 1) * p.chunk_pages, pages);
-    tw.poisoned = (it.page_begin != it.split * p.chunk_pages || it.page_end != want_end) ? 1 : 0;
-    if (tw.poisoned && threadIdx.x == 0) atomicOr(&p.ctr->status, static_cast<uint32_t>(PKV_DEV_PLAN_MISMATCH));
-    tw.t0 = it.page_begin * p.page_size;
-    tw.t1 = min(it.page_end * p.page_size, n);
-    if (tw.poisoned) tw.t1 = tw.t0;   // read nothing through a plan that does not fit
-    tw.finalize = splits == 1;
-    tw.slot = p.row_start[it.b] + it.kvh * splits + it.split;
-    return tw;
 }
 
 template <int D, int G, bool MMA>
@@ -1069,11 +1103,11 @@ __global__ void __launch_bounds__(kThreads, MMA ? 2 : 1) attention_kernel(const 
             __syncthreads();
             const int t = sm.tile_slot[0];
             if (t >= num_tiles) break;
-            const TileWork tw = tile_from_queue(p, p.order ? p.order[t] : t);
+            const TileWork tw = tile_from_item(p, p.order ? p.order[t] : t);
             run_tile<D, G, MMA>(sm, p, tw, pipe, &kmap, &vmap);
-            const int ntok = tw.t1 > tw.t0 ? tw.t1 - tw.t0 : 0;
-            pipe += (ntok + kBlockRows - 1) / kBlockRows;
-            if (!tw.finalize && p.fused_merge) merge_if_last<D, G>(sm, p, tw, p.row_splits[tw.b]);
+            pipe += stream_blocks(tw);
+            __syncthreads();
+            if (!sm.tile_fin && p.fused_merge) merge_if_last<D, G>(sm, p, tw.b, tw.kvh, sm.tile_splits);
             __syncthreads();
         }
         if (threadIdx.x == 0) {
@@ -1088,7 +1122,8 @@ __global__ void __launch_bounds__(kThreads, MMA ? 2 : 1) attention_kernel(const 
     }
 
     TileWork tw;
-    int ns = 1;
+    tw.lazy = 0;
+    tw.split = tw.page_begin = tw.page_end = 0;
     if (p.route == kRouteDirect) {
         tw.b = blockIdx.x / p.Hkv;
         tw.kvh = blockIdx.x % p.Hkv;
@@ -1096,16 +1131,17 @@ __global__ void __launch_bounds__(kThreads, MMA ? 2 : 1) attention_kernel(const 
         tw.t1 = p.seq_lens[tw.b];
         tw.slot = 0;
         tw.finalize = 1;
+        tw.splits = 1;
         tw.poisoned = 0;
         if (tw.t1 < 0 || tw.t1 > p.max_pages * p.page_size) {   // would read past the table row
             tw.poisoned = 1;
             tw.t1 = 0;
             if (threadIdx.x == 0) atomicOr(&p.ctr->status, static_cast<uint32_t>(PKV_DEV_PLAN_MISMATCH));
         }
+        tw.t_stream = tw.t1;
     } else if (p.route == kRouteQueue) {
         if (static_cast<int>(blockIdx.x) >= p.num_tiles) return;   // launched only for the neutral rows
-        tw = tile_from_queue(p, blockIdx.x);
-        ns = p.row_splits[tw.b];
+        tw = tile_from_item(p, blockIdx.x);
     } else {   // padded grid: (b, kvh, s) from the block index, ranges from the device lengths
         const int per_row = p.Hkv * p.max_splits;
         tw.b = blockIdx.x / per_row;
@@ -1119,13 +1155,14 @@ __global__ void __launch_bounds__(kThreads, MMA ? 2 : 1) attention_kernel(const 
         const int pe = max(0, min((s + 1) * p.chunk_pages, pages));
         tw.t0 = pb * p.page_size;
         tw.t1 = tw.poisoned ? tw.t0 : min(pe * p.page_size, n);
+        tw.t_stream = tw.t1;
         tw.finalize = p.max_splits == 1;
+        tw.splits = p.max_splits;
         tw.slot = blockIdx.x;
-        ns = p.max_splits;
     }
     run_tile<D, G, MMA>(sm, p, tw, 0, &kmap, &vmap);
     __syncthreads();
-    if (!tw.finalize && p.fused_merge) merge_if_last<D, G>(sm, p, tw, ns);
+    if (!sm.tile_fin && p.fused_merge) merge_if_last<D, G>(sm, p, tw.b, tw.kvh, sm.tile_splits);
     if (threadIdx.x == 0 && sm.abort) drain_after_abort<D, G>(sm, &p.ctr->status);
 }
 
