@@ -167,6 +167,44 @@ def continuous(seed: int = HELD_OUT_SEED, steps: int = 200, sessions: int = 56) 
                         notes=f"{steps} steps of append + decode")
 
 
+# --- the trace families of the PersistentKV summary (Methodology section 3) ---------------
+#
+# The summary names Bucketed, Bimodal, Uniform and Zipf-like traces "designed to isolate
+# context length, active batch size, and length raggedness" but publishes none of their
+# parameters.  These are the readings taken here (lengths in tokens, at most 32768):
+#   uniform   N ~ U[512, 32768]
+#   bimodal   each row short, N ~ U[256, 2048], or long, N ~ U[16384, 32768], with p = 1/2
+#   zipf      N = 512 * k with k Zipf(1.3) distributed, truncated to k <= 64
+#   bucketed  N drawn from the buckets {1024, 4096, 16384, 32768}
+TRACE_KINDS = ("uniform", "bimodal", "zipf", "bucketed")
+
+
+def trace_lengths(kind: str, batch: int, rng: np.random.Generator) -> np.ndarray:
+    if kind == "uniform":
+        n = rng.integers(512, 32768, size=batch, endpoint=True)
+    elif kind == "bimodal":
+        long_rows = rng.random(batch) < 0.5
+        n = np.where(long_rows, rng.integers(16384, 32768, size=batch, endpoint=True),
+                     rng.integers(256, 2048, size=batch, endpoint=True))
+    elif kind == "zipf":
+        k = rng.zipf(1.3, size=batch)
+        n = 512 * np.minimum(k, 64)
+    elif kind == "bucketed":
+        n = rng.choice(np.array([1024, 4096, 16384, 32768]), size=batch)
+    else:
+        raise ValueError(kind)
+    return np.asarray(n, dtype=np.int32)
+
+
+def trace(kind: str, batch: int, seed: int = HELD_OUT_SEED) -> Problem:
+    """A trace-family batch: 32/8 heads, D 128, 16-token pages, pool 1.25 x the pages in use."""
+    rng = np.random.default_rng(seed)
+    lens = trace_lengths(kind, batch, rng)
+    pages = int(sum(-(-int(n) // 16) for n in lens))
+    return make_problem(f"{kind}_b{batch}", lens, Hq=32, Hkv=8, D=128, page_size=16,
+                        num_pages=int(math.ceil(pages * 1.25)), rng=rng)
+
+
 WORKLOADS = {
     "tiny": tiny,
     "batch1_long": batch1_long,

@@ -208,3 +208,34 @@ def test_strerror_covers_every_code():
     for code in range(7):
         assert lib.pkv_strerror(code).decode() not in ("", "unknown error")
     assert lib.pkv_strerror(99).decode() == "unknown error"
+
+
+@pytest.mark.parametrize("kind", ["uniform", "bimodal", "zipf", "bucketed"])
+def test_trace_lengths_follow_their_recipes(kind):
+    rng = np.random.default_rng(wl.CALIBRATION_SEED)
+    n = wl.trace_lengths(kind, 4000, rng)
+    assert n.dtype == np.int32 and n.min() >= 256 and n.max() <= 32768
+    if kind == "uniform":
+        assert n.min() >= 512 and abs(n.mean() - (512 + 32768) / 2) < 600
+    elif kind == "bimodal":
+        short, long_ = n[n <= 2048], n[n >= 16384]
+        assert len(short) + len(long_) == len(n) and abs(len(short) / len(n) - 0.5) < 0.05
+    elif kind == "zipf":
+        from scipy.special import zeta
+        assert np.all(n % 512 == 0) and n.max() == 32768
+        assert abs(np.mean(n == 512) - 1 / zeta(1.3)) < 0.02   # P(k = 1) of Zipf(1.3)
+    else:
+        assert set(n.tolist()) == {1024, 4096, 16384, 32768}
+    again = wl.trace_lengths(kind, 4000, np.random.default_rng(wl.CALIBRATION_SEED))
+    assert np.array_equal(n, again)
+
+
+def test_policy_on_trace_families_never_picks_direct_below_one_wave():
+    for kind in ["uniform", "bimodal", "zipf", "bucketed"]:
+        for B in (1, 4, 8):
+            lens = wl.trace_lengths(kind, B, np.random.default_rng(wl.HELD_OUT_SEED))
+            p = _geom_problem(lens, Hq=32, Hkv=8, D=128)
+            info, q = _dry(p)
+            if max(lens) > 16 * 8:
+                assert info["mode_name"] == "split_queue", (kind, B)
+                assert info["num_work_items"] <= 2 * NUM_SMS
