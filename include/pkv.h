@@ -235,6 +235,17 @@ int pkv_status(pkv_plan_t plan, pkv_stream_t stream, uint32_t *status);
 int pkv_read_workspace(pkv_plan_t plan, pkv_stream_t stream, float *o_h, float *lse_h,
                        int32_t capacity, int32_t *count);
 
+/*
+ * Failure-detection self-test of the kernels' bounded waits: one thread waits,
+ * with the pipeline's own wait routine and a limit of `limit_ns` (at most 2 s),
+ * on an mbarrier phase that nothing completes.  The wait must give up, set
+ * PKV_DEV_TIMEOUT in *status_h and raise its CTA's abort flag, after which a
+ * second wait returns at once.  result_h[3] = {first wait succeeded, abort flag
+ * raised, second wait succeeded}.  Synchronises the device; no GPU fault or
+ * hang is involved, the context stays usable.
+ */
+int pkv_selftest_wait(int64_t limit_ns, uint32_t *status_h, int32_t *result_h);
+
 /* Per-launch timing.  While enabled, pkv_decode brackets each kernel it
  * launches with CUDA events; pkv_profile_read waits for them and returns the
  * durations in milliseconds of the last pkv_decode's launches, in launch order. */

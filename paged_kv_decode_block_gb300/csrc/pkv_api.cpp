@@ -685,6 +685,25 @@ int pkv_read_workspace(pkv_plan_t p, pkv_stream_t stream, float* o_h, float* lse
     return PKV_OK;
 }
 
+int pkv_selftest_wait(int64_t limit_ns, uint32_t* status_h, int32_t* result_h) {
+    if (limit_ns <= 0 || limit_ns > 2000000000 || !status_h || !result_h) return PKV_EINVAL;
+    uint32_t* status = nullptr;
+    int* result = nullptr;
+    if (cudaMalloc(&status, sizeof(uint32_t)) != cudaSuccess) return PKV_ENOMEM;
+    if (cudaMalloc(&result, 3 * sizeof(int)) != cudaSuccess) {
+        cudaFree(status);
+        return PKV_ENOMEM;
+    }
+    cudaError_t e = cudaMemset(status, 0, sizeof(uint32_t));
+    if (e == cudaSuccess) e = pkv::launch_wait_selftest(status, static_cast<uint64_t>(limit_ns), result, nullptr);
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    if (e == cudaSuccess) e = cudaMemcpy(status_h, status, sizeof(uint32_t), cudaMemcpyDeviceToHost);
+    if (e == cudaSuccess) e = cudaMemcpy(result_h, result, 3 * sizeof(int), cudaMemcpyDeviceToHost);
+    cudaFree(status);
+    cudaFree(result);
+    return e == cudaSuccess ? PKV_OK : cuda_fail(e);
+}
+
 int pkv_profile_enable(pkv_plan_t p, int32_t enable) {
     if (!p) return PKV_EINVAL;
     p->profile = enable != 0;

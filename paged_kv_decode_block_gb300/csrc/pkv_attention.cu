@@ -112,13 +112,13 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
 // kWaitLimitNs.  On expiry: flag the status word, raise the CTA's abort flag
 // (later waits of the CTA then return at once) and return false.
 __device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity, uint32_t* status,
-                                            volatile int* abort) {
+                                            volatile int* abort, uint64_t limit_ns = kWaitLimitNs) {
     if (abort && *abort) return false;
     const uint64_t start = globaltimer_ns();
     while (true) {
         for (int i = 0; i < 64; ++i)
             if (mbar_try_wait(bar, parity)) return true;
-        if (globaltimer_ns() - start > kWaitLimitNs) {
+        if (globaltimer_ns() - start > limit_ns) {
             atomicOr(status, static_cast<uint32_t>(PKV_DEV_TIMEOUT));
             if (abort) *abort = 1;
             return false;
@@ -1233,7 +1233,29 @@ cudaError_t launch_merge_t(const AttnParams& p, cudaStream_t stream) {
         default: break;                                                     \
     }
 
+// Self-test of the bounded wait: one thread waits on an mbarrier phase that
+// nothing completes, through the same wait the pipeline uses, with a short
+// limit; the wait must give up, flag PKV_DEV_TIMEOUT and raise the abort flag.
+__global__ void wait_selftest_kernel(uint32_t* status, uint64_t limit_ns, int* result) {
+    __shared__ uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x != 0) return;
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    fence_mbar_init();
+    const bool ok = mbar_wait_slow(&bar, 0, status, &abort_flag, limit_ns);   // phase 0 never completes
+    const bool again = mbar_wait_slow(&bar, 0, status, &abort_flag, limit_ns);  // after an abort: at once
+    result[0] = ok ? 1 : 0;
+    result[1] = abort_flag;
+    result[2] = again ? 1 : 0;
+}
+
 }  // namespace
+
+cudaError_t launch_wait_selftest(uint32_t* status, uint64_t limit_ns, int* result, cudaStream_t stream) {
+    wait_selftest_kernel<<<1, 32, 0, stream>>>(status, limit_ns, result);
+    return cudaGetLastError();
+}
 
 bool shape_supported(int D, int G) {
     PKV_DISPATCH(D, G, (void)kD; (void)kG; return true);

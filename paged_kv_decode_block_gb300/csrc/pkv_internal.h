@@ -92,6 +92,9 @@ cudaError_t launch_append(const uint16_t* k_new, const uint16_t* v_new, uint16_t
                           uint16_t* v_pages, const int32_t* block_table, int32_t* seq_lens,
                           int B, int Hkv, int D, int page_size, int max_pages, int num_pages,
                           uint32_t* status, cudaStream_t stream);
+// Bounded-wait self-test (see pkv_selftest_wait): result[3] = {wait returned true,
+// abort flag raised, second wait returned true}.
+cudaError_t launch_wait_selftest(uint32_t* status, uint64_t limit_ns, int* result, cudaStream_t stream);
 // Resident CTAs per SM of the attention kernel for this (D, G); 0 if unsupported.
 int attention_ctas_per_sm(int D, int G, bool mma);
 bool shape_supported(int D, int G);

@@ -91,6 +91,7 @@ SIGNATURES = {
     "pkv_session_destroy": (None, [_P]),
     "pkv_session_device_plan": (ctypes.c_int, [_P, _P]),
     "pkv_session_device_queue": (ctypes.c_int, [_P, ctypes.POINTER(WorkItem), _I32P, _I32, _I32P]),
+    "pkv_selftest_wait": (ctypes.c_int, [_I64, _U32P, _I32P]),
     "pkv_strerror": (ctypes.c_char_p, [ctypes.c_int]),
     "pkv_last_cuda_error": (ctypes.c_int, []),
 }
@@ -419,3 +420,11 @@ class Session:
             self.close()
         except Exception:
             pass
+
+
+def selftest_wait(limit_ns: int = 50_000_000):
+    """pkv_selftest_wait: returns (status bits, [first wait ok, abort raised, second wait ok])."""
+    st = ctypes.c_uint32(0)
+    res = (ctypes.c_int32 * 3)()
+    _check(load().pkv_selftest_wait(int(limit_ns), ctypes.byref(st), res), "pkv_selftest_wait")
+    return st.value, list(res)

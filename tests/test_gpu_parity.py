@@ -27,14 +27,18 @@ def _cuda():
     pkv.load()
 
 
+COPIES = ["lsu", "tma"]
+
+
+@pytest.mark.parametrize("copy", COPIES)
 @pytest.mark.parametrize("math", MATHS)
 @pytest.mark.parametrize("route", ROUTES)
 @pytest.mark.parametrize("splits", [1, 2, 4])
-def test_tiny_every_route_and_split(route, splits, math):
+def test_tiny_every_route_and_split(route, splits, math, copy):
     p = wl.tiny()
     ref = oracle_result(p)
-    out, lse, plan, _ = run(p, force_mode=route, num_splits=splits, math=math)
-    assert_close(out, lse, *ref, what=f"tiny {route} S={splits} {math}")
+    out, lse, plan, _ = run(p, force_mode=route, num_splits=splits, math=math, copy=copy)
+    assert_close(out, lse, *ref, what=f"tiny {route} S={splits} {math} {copy}")
     info = plan.info()
     assert info["mode_name"] == route
     assert np.array_equal(plan.queue(), expected_queue(p, info))
@@ -58,14 +62,15 @@ def test_tiny_split_partials_match_oracle_partials(math):
 EDGE_LENS = [1, 15, 16, 17, 32, 33, 0, 250]
 
 
+@pytest.mark.parametrize("copy", COPIES)
 @pytest.mark.parametrize("math", MATHS)
 @pytest.mark.parametrize("route", ROUTES)
 @pytest.mark.parametrize("splits", [1, 3, 16])
-def test_edge_lengths(route, splits, math):
+def test_edge_lengths(route, splits, math, copy):
     p = wl.make_problem("edges", EDGE_LENS, Hq=8, Hkv=2, D=128, page_size=16, num_pages=48, seed=21)
     ref = oracle_result(p)
-    out, lse, plan, _ = run(p, force_mode=route, num_splits=splits, math=math)
-    assert_close(out, lse, *ref, what=f"edges {route} S={splits} {math}")
+    out, lse, plan, _ = run(p, force_mode=route, num_splits=splits, math=math, copy=copy)
+    assert_close(out, lse, *ref, what=f"edges {route} S={splits} {math} {copy}")
     assert np.array_equal(plan.queue(), expected_queue(p, plan.info()))
     assert plan.status() == 0
 
@@ -100,14 +105,15 @@ def test_separate_merge_launch(route):
     assert np.array_equal(fin, np.isfinite(lse2)) and np.max(np.abs(lse[fin] - lse2[fin])) <= 1e-5
 
 
+@pytest.mark.parametrize("copy", COPIES)
 @pytest.mark.parametrize("page_size", [32, 64])
-def test_larger_pages(page_size):
+def test_larger_pages(page_size, copy):
     p = wl.make_problem("pages", [1, 63, 64, 65, 500], Hq=8, Hkv=2, D=128, page_size=page_size,
                         num_pages=24, seed=23)
     ref = oracle_result(p)
     for route in ROUTES:
-        out, lse, _, _ = run(p, force_mode=route, num_splits=3)
-        assert_close(out, lse, *ref, what=f"ps={page_size} {route}")
+        out, lse, _, _ = run(p, force_mode=route, num_splits=3, copy=copy)
+        assert_close(out, lse, *ref, what=f"ps={page_size} {route} {copy}")
 
 
 def test_all_rows_empty():
@@ -150,8 +156,8 @@ def test_bad_page_id_flags_status_and_poisons():
     bad = p.block_table.copy()
     bad[1, 2] = p.num_pages + 5
     p_bad = wl.Problem("bad", p.q, p.k_pages, p.v_pages, bad, p.seq_lens, p.page_size)
-    for route in ROUTES:
-        out, lse, plan, _ = run(p_bad, host_table=False, force_mode=route, num_splits=2)
+    for route, copy in [(r, c) for r in ROUTES for c in COPIES]:
+        out, lse, plan, _ = run(p_bad, host_table=False, force_mode=route, num_splits=2, copy=copy)
         assert plan.status() & pkv.DEV_PAGE_OOB, route
         assert np.all(np.isnan(out[1])), route
         assert np.all(np.isfinite(out[0])), route
@@ -189,12 +195,12 @@ def mixed_ref():
     return p, oracle_result(p, nthreads=16)
 
 
-@pytest.mark.parametrize("math", MATHS)
+@pytest.mark.parametrize("math,copy", [("fma", "lsu"), ("mma", "lsu"), ("mma", "tma")])
 @pytest.mark.parametrize("route", ["split_queue", "persistent"])
-def test_batch1_long_32k(route, math, batch1_long_ref):
+def test_batch1_long_32k(route, math, copy, batch1_long_ref):
     p, ref = batch1_long_ref
-    out, lse, plan, _ = run(p, force_mode=route, num_splits=32, math=math)
-    assert_close(out, lse, *ref, what=f"batch1_long {route} {math}")
+    out, lse, plan, _ = run(p, force_mode=route, num_splits=32, math=math, copy=copy)
+    assert_close(out, lse, *ref, what=f"batch1_long {route} {math} {copy}")
     info = plan.info()
     assert info["chunk_pages"] == 64 and info["num_work_items"] == 256
     assert np.array_equal(plan.queue(), expected_queue(p, info))
