@@ -147,27 +147,24 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, i
         : "memory");
 }
 
-// Non-tensor bulk copy global -> shared (16-byte aligned, size a multiple of 16),
-// completing on `bar`.
-__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-            smem_addr(dst)),
-        "l"(src), "r"(bytes), "r"(smem_addr(bar))
-        : "memory");
-}
-
-// Order this thread's view of global data written through the generic proxy
-// (other CTAs' plain stores) before its own async-proxy (bulk copy) reads.
-__device__ __forceinline__ void fence_proxy_async_global() {
-    asm volatile("fence.proxy.async.global;" ::: "memory");
-}
-
 // 16-byte asynchronous global -> shared copy through L2 only, with an L2 policy.
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint64_t policy) {
     asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "l"(policy)
                  : "memory");
 }
+
+// 16-byte asynchronous global -> shared copy through L2 only (generic proxy:
+// no proxy fence is needed against plain stores of other CTAs).
+__device__ __forceinline__ void cp_async16_plain(uint32_t dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_commit_wait_all() {
+    asm volatile("cp.async.commit_group;\n\tcp.async.wait_all;" ::: "memory");
+}
+
+// Release / acquire fence at GPU scope (message passing between CTAs).
+__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
 
 // Arrive on `bar` once every cp.async this thread has issued so far has landed
 // (the arrival counts against the barrier's expected count).
@@ -281,7 +278,7 @@ struct Smem {
     alignas(1024) uint8_t v[kStages][Cfg<D, G>::kMatBytes];
     alignas(16) uint16_t pt[kConsumerWarps][Cfg<D, G>::NPV * 2 * 8 * 8];   // P^T tiles, bf16 (MMA form)
     float p[kConsumerWarps][kBlockRows * G];   // softmax weights of the block (FMA form)
-    float acc[kConsumerWarps][G * D];          // per-warp states for the end-of-tile merge
+    alignas(16) float acc[kConsumerWarps][G * D];   // per-warp states for the end-of-tile merge
     float m[kConsumerWarps][G];
     float l[kConsumerWarps][G];
     float merge_m[G], merge_inv[G];
@@ -292,8 +289,6 @@ struct Smem {
     int abort;                  // a wait of this CTA ran out: stop waiting, drain, finish
     uint64_t full[kStages];
     uint64_t empty[kStages];
-    uint64_t merge_bar;         // completion of the fused merge's bulk copies
-    uint32_t merge_phase;       // phases of merge_bar used so far
     int tile_slot[2];
     int tile_fin, tile_splits;  // the finished tile's finalize flag and split count
 };
@@ -726,38 +721,39 @@ __device__ void merge_unit(const AttnParams& p, int b, int kvh, int ns, float* w
 }
 
 // The fused merge of the last-arriving CTA.  The ns partial outputs of
-// (b, kvh) are contiguous in the workspace, so they come into the CTA's idle
-// stage buffers with bulk asynchronous copies (a chunk of splits at a time)
-// while the threads read the LSEs and form the weights; the sum then runs out
-// of shared memory.  Same arithmetic as merge_unit; all CTA threads call it.
+// (b, kvh) are contiguous in the workspace: every thread copies its share of
+// them into the CTA's idle stage buffers with 16-byte cp.async (all in flight
+// at once, a chunk of splits at a time), while the LSEs come in with plain L2
+// loads; the weighted sum then runs out of shared memory, one float4 of the
+// output per thread with independent loads.  Same arithmetic as merge_unit;
+// all CTA threads call it.
 template <int D, int G>
-__device__ void merge_unit_bulk(Smem<D, G>& sm, const AttnParams& p, int b, int kvh, int ns) {
+__device__ void merge_unit_staged(Smem<D, G>& sm, const AttnParams& p, int b, int kvh, int ns) {
     constexpr int kScratch = Cfg<D, G>::kStages * Cfg<D, G>::kMatBytes * 2;   // K and V stages
     constexpr int kSplitBytes = G * D * 4;
-    const int tid = threadIdx.x, nthreads = blockDim.x;
+    constexpr int kOut = G * D / 4;                                            // float4 outputs of (b, kvh)
+    constexpr int kPer = (kOut + kThreads - 1) / kThreads;
+    const int tid = threadIdx.x;
     const size_t base = static_cast<size_t>(p.row_start[b]) + static_cast<size_t>(kvh) * ns;
     uint8_t* scratch = &sm.k[0][0];   // k and v stages are adjacent
     float* w = reinterpret_cast<float*>(scratch);                  // [ns][G] weights
     const int w_bytes = (ns * G * 4 + 1023) & ~1023;
     float* obuf = reinterpret_cast<float*>(scratch + w_bytes);     // [chunk][G][D] partials
     const int chunk = (kScratch - w_bytes) / kSplitBytes;
-    uint32_t* status = &p.ctr->status;
 
-    auto issue = [&](int s0) {   // thread 0: bulk-copy splits [s0, s0 + chunk) of (b, kvh)
-        const int n = min(chunk, ns - s0);
-        mbar_arrive_expect_tx(&sm.merge_bar, static_cast<uint32_t>(n * kSplitBytes));
-        bulk_load(obuf, p.ws_o + (base + s0) * G * D, static_cast<uint32_t>(n * kSplitBytes), &sm.merge_bar);
+    auto issue = [&](int s0) {   // every thread: its 16-byte pieces of splits [s0, s0 + chunk)
+        const int vecs = min(chunk, ns - s0) * (kSplitBytes / 16);
+        const uint8_t* src = reinterpret_cast<const uint8_t*>(p.ws_o + (base + s0) * G * D);
+        const uint32_t dst = smem_addr(obuf);
+        for (int i = tid; i < vecs; i += kThreads) cp_async16_plain(dst + i * 16, src + static_cast<size_t>(i) * 16);
     };
-    if (tid == 0) {
-        sm.merge_nan = 0;
-        fence_proxy_async_global();
-        issue(0);
-    }
-    for (int i = tid; i < ns * G; i += nthreads) w[i] = __ldcg(p.ws_lse + base * G + i);
+    issue(0);
+    if (tid == 0) sm.merge_nan = 0;
+    for (int i = tid; i < ns * G; i += kThreads) w[i] = __ldcg(p.ws_lse + base * G + i);
     __syncthreads();
     // per head: max and sum over the splits, one warp per head
     const int warp = tid / 32, lane = tid % 32;
-    for (int g = warp; g < G; g += nthreads / 32) {
+    for (int g = warp; g < G; g += kThreads / 32) {
         float M = -INFINITY;
         bool nan = false;
         for (int s = lane; s < ns; s += 32) {
@@ -781,24 +777,28 @@ __device__ void merge_unit_bulk(Smem<D, G>& sm, const AttnParams& p, int b, int 
         }
     }
     __syncthreads();
-    for (int i = tid; i < ns * G; i += nthreads) {
+    for (int i = tid; i < ns * G; i += kThreads) {
         const int g = i % G;
         w[i] = sm.merge_m[g] != -INFINITY ? exp2f(w[i] - sm.merge_m[g]) * sm.merge_inv[g] : 0.f;
     }
-    constexpr int kOut = G * D / 4;   // float4 outputs of (b, kvh)
-    float4 acc[2] = {make_float4(0.f, 0.f, 0.f, 0.f), make_float4(0.f, 0.f, 0.f, 0.f)};
+    float4 acc[kPer];
+#pragma unroll
+    for (int r = 0; r < kPer; ++r) acc[r] = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int s0 = 0; s0 < ns; s0 += chunk) {
         const int n = min(chunk, ns - s0);
-        mbar_wait(&sm.merge_bar, sm.merge_phase & 1u, status, nullptr);
-        __syncthreads();   // weights ready; every thread saw this chunk land
+        cp_async_commit_wait_all();
+        __syncthreads();   // this chunk (and the weights) visible to every thread
 #pragma unroll
-        for (int r = 0; r < 2; ++r) {
-            const int i = tid + r * nthreads;
+        for (int r = 0; r < kPer; ++r) {
+            const int i = tid + r * kThreads;
             if (i < kOut) {
                 const int g = i / (D / 4), d = (i % (D / 4)) * 4;
+                const float* wg = w + s0 * G + g;
+                const float* og = obuf + g * D + d;
+#pragma unroll 8
                 for (int s = 0; s < n; ++s) {
-                    const float ws = w[(s0 + s) * G + g];
-                    const float4 o = *reinterpret_cast<const float4*>(obuf + (s * G + g) * D + d);
+                    const float ws = wg[s * G];
+                    const float4 o = *reinterpret_cast<const float4*>(og + s * G * D);
                     acc[r].x = fmaf(ws, o.x, acc[r].x);
                     acc[r].y = fmaf(ws, o.y, acc[r].y);
                     acc[r].z = fmaf(ws, o.z, acc[r].z);
@@ -806,22 +806,22 @@ __device__ void merge_unit_bulk(Smem<D, G>& sm, const AttnParams& p, int b, int 
                 }
             }
         }
-        __syncthreads();   // chunk consumed
-        if (tid == 0) {
-            ++sm.merge_phase;
-            if (s0 + chunk < ns) issue(s0 + chunk);
+        if (s0 + chunk < ns) {
+            __syncthreads();   // chunk consumed before it is overwritten
+            issue(s0 + chunk);
         }
     }
     const bool nan = sm.merge_nan != 0;
 #pragma unroll
-    for (int r = 0; r < 2; ++r) {
-        const int i = tid + r * nthreads;
+    for (int r = 0; r < kPer; ++r) {
+        const int i = tid + r * kThreads;
         if (i < kOut) {
             const int g = i / (D / 4), d = (i % (D / 4)) * 4;
             *reinterpret_cast<float4*>(p.out + (static_cast<size_t>(b) * p.Hq + kvh * G + g) * D + d) =
                 nan ? make_float4(NAN, NAN, NAN, NAN) : acc[r];
         }
     }
+    fence_proxy_async_shared();   // a later TMA into these stages is ordered after the copies above
     __syncthreads();
 }
 
@@ -998,34 +998,51 @@ __device__ void run_tile(Smem<D, G>& sm, const AttnParams& p, TileWork tw, uint3
     if (lane == 0) sm.poisoned[warp] = poisoned;
     named_barrier_sync(1, kConsumerWarps * 32);
 
+    // Exact LSE combine of the four warp states: one float4 (head g, d .. d+3)
+    // per thread and pass, so every thread runs one short independent chain.
     const int tid = threadIdx.x;
     bool any_poison = false;
 #pragma unroll
     for (int w = 0; w < kConsumerWarps; ++w) any_poison |= sm.poisoned[w] != 0;
-    for (int idx = tid; idx < G * D; idx += kConsumerWarps * 32) {
-        const int g = idx / D, d = idx % D;
+    constexpr int kItems = G * D / 4;
+    for (int i = tid; i < kItems; i += kConsumerWarps * 32) {
+        const int g = i / (D / 4), d = (i % (D / 4)) * 4;
+        float mw[kConsumerWarps];
         float M = -INFINITY;
 #pragma unroll
-        for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, sm.m[w][g]);
-        float o = 0.f, lse2 = -INFINITY;
+        for (int w = 0; w < kConsumerWarps; ++w) {
+            mw[w] = sm.m[w][g];
+            M = fmaxf(M, mw[w]);
+        }
+        float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+        float lse2 = -INFINITY;
         if (M != -INFINITY) {
-            float lsum = 0.f, osum = 0.f;
+            float lsum = 0.f;
+            float4 os = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
             for (int w = 0; w < kConsumerWarps; ++w) {
-                const float sc = exp2f(sm.m[w][g] - M);   // idle warp: m = -inf -> 0
+                const float sc = exp2f(mw[w] - M);   // idle warp: m = -inf -> 0
                 lsum = fmaf(sm.l[w][g], sc, lsum);
-                osum = fmaf(sm.acc[w][g * D + d], sc, osum);
+                const float4 a = *reinterpret_cast<const float4*>(&sm.acc[w][g * D + d]);
+                os.x = fmaf(a.x, sc, os.x);
+                os.y = fmaf(a.y, sc, os.y);
+                os.z = fmaf(a.z, sc, os.z);
+                os.w = fmaf(a.w, sc, os.w);
             }
-            o = osum / lsum;
+            const float inv = 1.f / lsum;
+            o = make_float4(os.x * inv, os.y * inv, os.z * inv, os.w * inv);
             lse2 = M + log2f(lsum);
         }
-        if (any_poison) o = lse2 = NAN;
+        if (any_poison) {
+            o = make_float4(NAN, NAN, NAN, NAN);
+            lse2 = NAN;
+        }
         if (tw.finalize) {
             const int h = tw.kvh * G + g;
-            p.out[(static_cast<size_t>(tw.b) * p.Hq + h) * D + d] = o;
+            *reinterpret_cast<float4*>(p.out + (static_cast<size_t>(tw.b) * p.Hq + h) * D + d) = o;
             if (d == 0) p.lse[static_cast<size_t>(tw.b) * p.Hq + h] = lse2 * kLn2;
         } else {
-            p.ws_o[(static_cast<size_t>(tw.slot) * G + g) * D + d] = o;
+            *reinterpret_cast<float4*>(p.ws_o + (static_cast<size_t>(tw.slot) * G + g) * D + d) = o;
             if (d == 0) p.ws_lse[static_cast<size_t>(tw.slot) * G + g] = lse2;
         }
     }
@@ -1041,12 +1058,12 @@ __device__ void merge_if_last(Smem<D, G>& sm, const AttnParams& p, int b, int kv
     __syncthreads();
     if (threadIdx.x == 0) {
         const int u = b * p.Hkv + kvh;
-        __threadfence();
+        fence_acq_rel_gpu();
         const uint32_t prev = atomicAdd(&p.arrive[u], 1u);
         const int last = prev == static_cast<uint32_t>(ns - 1);
         if (last) {
             p.arrive[u] = 0;   // ready for the next launch
-            __threadfence();
+            fence_acq_rel_gpu();
         }
         sm.tile_slot[1] = last;
     }
@@ -1055,7 +1072,7 @@ __device__ void merge_if_last(Smem<D, G>& sm, const AttnParams& p, int b, int kv
         // the stage buffers are idle here and serve as the merge's scratch
         static_assert(2 * Cfg<D, G>::kStages * Cfg<D, G>::kMatBytes >= kMergeCapFloats * 4 + 2 * G * D * 4,
                       "merge scratch");
-        merge_unit_bulk<D, G>(sm, p, b, kvh, ns);
+        merge_unit_staged<D, G>(sm, p, b, kvh, ns);
     }
 }
 
@@ -1083,8 +1100,6 @@ __global__ void __launch_bounds__(kThreads, MMA ? 2 : 1) attention_kernel(const 
             sm.issued[s] = 0;
         }
         sm.abort = 0;
-        mbar_init(&sm.merge_bar, 1);
-        sm.merge_phase = 0;
         fence_mbar_init();
     }
     __syncthreads();
