@@ -4,15 +4,20 @@
 
 Default workload: batch-1 long context (1 x 32768 tokens, 32 query / 8 KV heads,
 D 128, 16-token pages scattered over a 4096-page pool, 32 splits).  One step is
-one pkv_decode: the split-partial kernel over the compact queue plus the LSE
-merge kernel.  Metric: KV-read GB/s (KV bytes of the step / device time of the
-step) and µs per step; roofline fraction against the measured HBM copy
-bandwidth.
+one pkv_decode: the split-partial kernel over the compact queue with the LSE
+merge fused into its last-arriving splits.  Metric: KV-read GB/s (KV bytes of
+the step / device time of the step) and µs per step; roofline fraction against
+the measured HBM copy bandwidth.
 
 Timing rules: parity against the fp64 oracle before any timing; W >= 3 warm-up
-steps; L2 flushed (a 2 x L2-size buffer written) before every timed step; each
-step timed with CUDA events on the launching stream; clocks sampled with
-nvidia-smi during the timed region.  Multi-GPU (torchrun, one rank per GPU)
+steps; clocks sampled with nvidia-smi during the timed region.  The K timed
+steps run back to back between one pair of CUDA events on the launching
+stream, on cold inputs: R copies of the page pool and q are used round robin,
+with R chosen so that at least 6 x L2 bytes are read between two reads of the
+same copy (a step that is itself over 6 x L2 needs no copy).  Steps too small
+for that (the tiny case) are timed one by one after an L2 flush (a 2 x L2-size
+buffer written).  Each step is also timed alone, after a flush, between its own
+events ("isolated_us_per_step"), which adds the launch latency to every step.  Multi-GPU (torchrun, one rank per GPU)
 runs independent replicas of the workload, partitioned by sequence: no
 collective on the data path, a barrier and max-over-ranks timing only.
 
@@ -219,7 +224,7 @@ def run_pkv(args):
     pkv.load()
 
     p, opts = build_workload(args.workload)
-    opts = dict(opts, math=args.math, separate_merge=args.separate_merge, copy=args.copy)
+    opts = dict(opts, math=args.math, separate_merge=args.separate_merge, copy=args.copy, merge=args.merge)
     if args.num_splits is not None:
         opts["num_splits"] = args.num_splits
     if args.mode is not None:
@@ -248,48 +253,95 @@ def run_pkv(args):
 
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
-    # With one launch per step the step's own events bracket exactly that kernel;
-    # extra per-kernel events (needed only for two launches) would add their own
-    # latency to every timed step.
-    per_kernel_events = info["launches_per_step"] > 1
-    plan.profile(per_kernel_events)
-    for _ in range(args.warmup):
-        flush.zero_()
-        pkv.decode(q, k, v, table, lens, plan, out, lse)
+    step_bytes = info["kv_bytes"] + p.B * p.Hq * p.D * 2
+    # Cold inputs without a flush: R copies of the page pool (and q), used round
+    # robin, so that at least 6 x L2 bytes are read between two reads of a copy
+    # (the L2 keeps a few percent of lines across 3 x L2 of streaming, measured
+    # with ncu; across 6 x L2 under 0.3 %).
+    rot = 1 if step_bytes >= 6 * l2 else 1 + -(-6 * l2 // step_bytes)
+    streamed = rot <= 16
+    copies = [(q, k, v)] + [(q.clone(), k.clone(), v.clone()) for _ in range(rot - 1 if streamed else 0)]
+    # The clones leave their last pages in L2 at normal priority, where the
+    # kernel's evict-first loads would never displace them: flush once.
+    flush.zero_()
+    n_launch = info["launches_per_step"]
+    per_kernel_events = n_launch > 1
+
+    def step(i):
+        qi, ki, vi = copies[i % len(copies)]
+        pkv.decode(qi, ki, vi, table, lens, plan, out, lse)
+
+    for i in range(args.warmup):
+        if not streamed:
+            flush.zero_()
+        step(i)
     torch.cuda.synchronize()
 
+    # (1) the timed region: K steps back to back on cold copies (or, when the
+    # step is too small for that, with an L2 flush before every step)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    kernel_ms = []
     with ClockSampler(smi_index(local)) as clk:
         time.sleep(0.3)
+        # a one-second soak of the same steps right before the timed region, so
+        # that the 200 ms clock samples see the GPU under this load
+        t_soak = time.perf_counter()
+        i = 0
+        while time.perf_counter() - t_soak < 1.0:
+            for _ in range(100):
+                step(i)
+                i += 1
+            torch.cuda.synchronize()
         if world > 1:
             dist.barrier()
         torch.cuda.synchronize()
         t_wall0 = time.perf_counter()
-        for i in range(args.steps):
-            flush.zero_()
-            starts[i].record(stream)
-            pkv.decode(q, k, v, table, lens, plan, out, lse)
-            ends[i].record(stream)
-            if per_kernel_events:
-                kernel_ms.append(plan.profile_read())   # waits for this step's kernels
+        if streamed:
+            ev0.record(stream)
+            for i in range(args.steps):
+                step(i)
+            ev1.record(stream)
+        else:
+            for i in range(args.steps):
+                flush.zero_()
+                starts[i].record(stream)
+                step(i)
+                ends[i].record(stream)
         torch.cuda.synchronize()
         if world > 1:
             dist.barrier()
         t_wall = time.perf_counter() - t_wall0
         time.sleep(0.3)
+    if streamed:
+        med_ms = ev0.elapsed_time(ev1) / args.steps
+    else:
+        med_ms = statistics.median(s.elapsed_time(e) for s, e in zip(starts, ends))
+
+    # (2) for reference: every step alone, after an L2 flush, between its own
+    # events (adds the launch latency to each step); per-kernel events when the
+    # step has two launches
+    plan.profile(per_kernel_events)
+    iso_ms, kernel_ms = [], []
+    for i in range(max(args.steps, 5)):
+        flush.zero_()
+        starts[i % args.steps].record(stream)
+        step(i)
+        ends[i % args.steps].record(stream)
+        ends[i % args.steps].synchronize()
+        iso_ms.append(starts[i % args.steps].elapsed_time(ends[i % args.steps]))
+        if per_kernel_events:
+            kernel_ms.append(plan.profile_read())
     plan.profile(False)
-    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    med_ms = statistics.median(step_ms)
+    iso_med = statistics.median(iso_ms)
     if per_kernel_events:
         attn_ms = statistics.mean(km[0] for km in kernel_ms)
         merge_ms = statistics.mean(km[1] for km in kernel_ms)
     else:
-        attn_ms = statistics.mean(step_ms)
+        attn_ms = med_ms
         merge_ms = 0.0
 
-    med_ms, attn_ms = reduce_max([med_ms, attn_ms], dist, dev)
+    med_ms, attn_ms, iso_med = reduce_max([med_ms, attn_ms, iso_med], dist, dev)
 
     kv = info["kv_bytes"]
     q_bytes = p.B * p.Hq * p.D * 2
@@ -339,12 +391,16 @@ def run_pkv(args):
                    else f"sum {int(p.seq_lens.sum())}", "q_heads": p.Hq, "kv_heads": p.Hkv,
                    "head_dim": p.D, "page_size": p.page_size, "num_pages": p.num_pages,
                    "mode": info["mode_name"], "math": args.math, "copy": args.copy,
+                   "merge": info["merge_name"],
                    "num_splits": info["max_splits"],
                    "chunk_pages": info["chunk_pages"], "tiles": info["num_work_items"],
                    "launches_per_step": info["launches_per_step"],
-                   "l2": "flushed before every timed step (2 x L2 bytes written)",
+                   "l2": (f"cold: {rot} copies of the page pool and q used round robin, >= 6 x L2 bytes "
+                          f"read between two reads of a copy; steps back to back, one event pair"
+                          if streamed else "flushed before every timed step (2 x L2 bytes written)"),
                    "parallelism": f"replicas x{world} (partition by sequence, no collective)"},
         "kv_bytes_per_step": kv,
+        "isolated_us_per_step": round(iso_med * 1e3, 2),
         "frac_of_nominal_7_9TBs": round(value / NOMINAL_HBM_GBS, 4),
         "kernel_ms": {"attention": round(attn_ms, 5), "merge": round(merge_ms, 5)},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
@@ -355,7 +411,7 @@ def run_pkv(args):
         "e2e": {"value": round(kv * world / e2e_med / 1e9, 2), "unit": "GB/s",
                 "us_per_step": round(e2e_med * 1e6, 2), "h2d_bytes_per_step": q_bytes + upload,
                 "d2h_bytes_per_step": o_bytes},
-        "gpu_launches": info["launches_per_step"] * args.steps,
+        "gpu_launches": n_launch * args.steps,
         "cpu_baseline": cpu,
         "clocks": {"sm_mhz": clocks["sm_mhz"], "sm_max_mhz": clocks["sm_max_mhz"],
                    "reasons": clocks["reasons"], "samples": clocks["samples"]},
@@ -580,6 +636,8 @@ def main():
     ap.add_argument("--math", default="auto", choices=["auto", "fma", "mma"],
                     help="block reduction: tensor cores (mma.sync) or CUDA-core FMA")
     ap.add_argument("--separate-merge", action="store_true", help="merge splits in a second launch")
+    ap.add_argument("--merge", default="auto", choices=["auto", "last", "all"],
+                    help="fused merge: the last arriving split, or every split sharing out the outputs")
     ap.add_argument("--mode", default=None, choices=["auto", "direct", "split_queue", "split_padded", "persistent"],
                     help="override the workload's route")
     ap.add_argument("--num-splits", type=int, default=None,

@@ -113,7 +113,20 @@ typedef struct {
     int32_t num_sms;             /* SM count to plan for (default: current device) */
     int32_t math;                /* pkv_math: block reduction on tensor cores or CUDA cores */
     int32_t copy;                /* pkv_copy: how K/V pages reach shared memory */
+    int32_t merge;               /* pkv_merge: how the fused merge is shared out */
 } pkv_plan_opts;
+
+/* How the split routes merge the partial states of a (row, KV head) inside the
+ * attention launch (with separate_merge = 0). */
+enum pkv_merge {
+    PKV_MERGE_AUTO = 0,   /* LAST */
+    PKV_MERGE_LAST = 1,   /* the last split to arrive merges all partials; the launch may
+                             overlap the previous kernel's tail (programmatic dependent launch) */
+    PKV_MERGE_ALL = 2     /* every split waits for the others, then merges a 1/S share of the
+                             outputs: a shorter merge, but a cooperative launch, which does not
+                             overlap the previous kernel; needs the queue or padded route with
+                             a grid that fits on the device at once, else PKV_EUNSUPPORTED */
+};
 
 /* How the producer warp moves K/V blocks into shared memory. */
 enum pkv_copy {
@@ -145,7 +158,7 @@ typedef struct {
     int32_t launches_per_step;  /* kernels pkv_decode launches */
     int32_t grid_ctas;          /* CTAs of the attention launch */
     int32_t num_sms;            /* SM count planned for */
-    int32_t reserved;
+    int32_t merge;              /* 0: no split is merged; pkv_merge LAST or ALL; 3: separate launch */
     int64_t kv_bytes;           /* sum_b N_b * Hkv * D * 2 (K and V) * 2 B */
     int64_t workspace_bytes;    /* split partial states written + read per step */
     int64_t table_bytes;        /* block-table entries read per step */

@@ -62,6 +62,7 @@ struct Options {
     int num_sms = 0;
     int math = PKV_MATH_AUTO;
     int copy = PKV_COPY_AUTO;
+    int merge = PKV_MERGE_AUTO;
 };
 
 int resolve_options(const pkv_plan_opts* o, Options* r) {
@@ -70,8 +71,9 @@ int resolve_options(const pkv_plan_opts* o, Options* r) {
     if (o->num_splits < 0 || o->direct_units_per_sm < 0 || o->target_ctas_per_sm < 0 ||
         o->min_chunk_pages < 0 || o->ctas_per_sm < 0 || o->num_sms < 0 || o->separate_merge < 0 ||
         o->separate_merge > 1 || o->math < PKV_MATH_AUTO || o->math > PKV_MATH_MMA || o->copy < PKV_COPY_AUTO ||
-        o->copy > PKV_COPY_TMA)
+        o->copy > PKV_COPY_TMA || o->merge < PKV_MERGE_AUTO || o->merge > PKV_MERGE_ALL)
         return PKV_EINVAL;
+    r->merge = o->merge;
     r->math = o->math;
     r->copy = o->copy;
     r->force_mode = o->force_mode;
@@ -121,6 +123,7 @@ struct Plan {
     int32_t grid = 0;
     int32_t empty_tiles = 0;
     bool need_merge = false;
+    int32_t merge = 0;   // pkv_plan_info.merge
     int32_t ws_slots = 0;
     int64_t kv_bytes = 0, ws_bytes = 0, table_bytes = 0;
     std::vector<pkv_work_item> items;   // queue (or padded grid / direct tiles, for inspection)
@@ -128,8 +131,10 @@ struct Plan {
     std::vector<int32_t> order;         // persistent route: queue indices, longest tile first
 };
 
+// `resident_ctas`: attention CTAs the device holds at once (a cooperative
+// launch of up to this many is possible).
 int compute_plan(const pkv_geom& g, int32_t ps, const int32_t* lens, const Options& o, int num_sms,
-                 int ctas_per_sm, Plan* r) {
+                 int ctas_per_sm, int64_t resident_ctas, Plan* r) {
     const int B = g.batch, Hkv = g.num_kv_heads, G = g.num_q_heads / g.num_kv_heads, D = g.head_dim;
     std::vector<int32_t> pages(B);
     int64_t p_max = 0, p_total = 0, tokens = 0;
@@ -240,6 +245,21 @@ int compute_plan(const pkv_geom& g, int32_t ps, const int32_t* lens, const Optio
             });
     }
     r->ws_bytes = merged_slots * G * (D + 1) * 4 * 2;   // written once, read once
+    // How the merge of the split partials is shared out
+    r->merge = 0;
+    if (merged_slots > 0) {
+        if (o.separate_merge) {
+            r->merge = 3;
+        } else {
+            const bool one_wave = (mode == PKV_MODE_SPLIT_QUEUE || mode == PKV_MODE_SPLIT_PADDED) &&
+                                  static_cast<int64_t>(r->grid) <= resident_ctas;
+            // AUTO takes LAST: its launch overlaps the previous kernel's tail
+            // (programmatic dependent launch), which a cooperative launch does
+            // not; back to back that is worth more than ALL's shorter merge.
+            if (o.merge == PKV_MERGE_ALL && !one_wave) return PKV_EUNSUPPORTED;
+            r->merge = o.merge == PKV_MERGE_ALL ? PKV_MERGE_ALL : PKV_MERGE_LAST;
+        }
+    }
     return PKV_OK;
 }
 
@@ -257,6 +277,7 @@ void fill_info(const Plan& p, const pkv_geom& g, int num_sms, pkv_plan_info* inf
     info->launches_per_step = g.batch > 0 ? launches_of(p) : 0;
     info->grid_ctas = p.grid;
     info->num_sms = num_sms;
+    info->merge = p.merge;
     info->kv_bytes = p.kv_bytes;
     info->workspace_bytes = p.ws_bytes;
     info->table_bytes = p.table_bytes;
@@ -315,6 +336,7 @@ struct pkv_plan_s {
     int device = 0;
     int num_sms = 0;
     int ctas_per_sm = 1;
+    int64_t resident_ctas = 0;   // attention CTAs the device holds at once
     Plan plan;
 
     // host staging (pinned) and device copy: [items][row_start B][row_splits B]
@@ -430,7 +452,8 @@ int pkv_plan_dry_run(const int32_t* seq_lens_h, const int32_t* block_table_h, in
     if ((rc = validate_rows(*geom, page_size, seq_lens_h, block_table_h))) return rc;
     if (o.num_sms <= 0) return PKV_EINVAL;   // no device is consulted here
     Plan pl;
-    if ((rc = compute_plan(*geom, page_size, seq_lens_h, o, o.num_sms, std::max(1, o.ctas_per_sm), &pl)))
+    if ((rc = compute_plan(*geom, page_size, seq_lens_h, o, o.num_sms, std::max(1, o.ctas_per_sm),
+                           static_cast<int64_t>(o.num_sms) * std::max(1, o.ctas_per_sm), &pl)))
         return rc;
     if (info) fill_info(pl, *geom, o.num_sms, info);
     const int32_t n = static_cast<int32_t>(pl.items.size());
@@ -461,24 +484,34 @@ int pkv_plan(const int32_t* seq_lens_h, const int32_t* block_table_h, int32_t pa
         delete p;
         return cuda_fail(e);
     }
-    if (o.num_sms > 0) p->num_sms = o.num_sms;
     const int G = geom->num_q_heads / geom->num_kv_heads;
+    {
+        int dev_sms = 0;
+        if (cudaDeviceGetAttribute(&dev_sms, cudaDevAttrMultiProcessorCount, p->device) != cudaSuccess) {
+            delete p;
+            return cuda_fail(cudaGetLastError());
+        }
+        const int occ = pkv::attention_ctas_per_sm(geom->head_dim, G, o.math != PKV_MATH_FMA);
+        p->resident_ctas = static_cast<int64_t>(dev_sms) * occ;
+    }
+    if (o.num_sms > 0) p->num_sms = o.num_sms;
     p->ctas_per_sm = o.ctas_per_sm > 0 ? o.ctas_per_sm
                                        : std::max(1, pkv::attention_ctas_per_sm(geom->head_dim, G,
                                                                                 o.math != PKV_MATH_FMA));
 
-    if ((rc = compute_plan(p->g, page_size, seq_lens_h, o, p->num_sms, p->ctas_per_sm, &p->plan))) {
+    if ((rc = compute_plan(p->g, page_size, seq_lens_h, o, p->num_sms, p->ctas_per_sm, p->resident_ctas,
+                           &p->plan))) {
         delete p;
         return rc;
     }
     if (cudaEventCreateWithFlags(&p->upload_done, cudaEventDisableTiming) != cudaSuccess ||
         cudaMalloc(&p->ctr, sizeof(pkv::DeviceCounters)) != cudaSuccess ||
-        cudaMalloc(&p->arrive, sizeof(uint32_t) * std::max(1, geom->batch * geom->num_kv_heads)) != cudaSuccess) {
+        cudaMalloc(&p->arrive, 2 * sizeof(uint32_t) * std::max(1, geom->batch * geom->num_kv_heads)) != cudaSuccess) {
         release(p);
         return PKV_ENOMEM;
     }
     if (cudaMemset(p->ctr, 0, sizeof(pkv::DeviceCounters)) != cudaSuccess ||
-        cudaMemset(p->arrive, 0, sizeof(uint32_t) * std::max(1, geom->batch * geom->num_kv_heads)) != cudaSuccess ||
+        cudaMemset(p->arrive, 0, 2 * sizeof(uint32_t) * std::max(1, geom->batch * geom->num_kv_heads)) != cudaSuccess ||
         cudaDeviceSynchronize() != cudaSuccess) {
         release(p);
         return cuda_fail(cudaGetLastError());
@@ -496,7 +529,9 @@ int pkv_plan_update(pkv_plan_t p, const int32_t* seq_lens_h, const int32_t* bloc
     int rc = validate_rows(p->g, p->page_size, seq_lens_h, block_table_h);
     if (rc) return rc;
     if (p->upload_recorded) PKV_CUDA(cudaEventSynchronize(p->upload_done));
-    if ((rc = compute_plan(p->g, p->page_size, seq_lens_h, p->opts, p->num_sms, p->ctas_per_sm, &p->plan))) return rc;
+    if ((rc = compute_plan(p->g, p->page_size, seq_lens_h, p->opts, p->num_sms, p->ctas_per_sm, p->resident_ctas,
+                           &p->plan)))
+        return rc;
     return stage(p);
 }
 
@@ -590,6 +625,7 @@ int enqueue_decode(pkv_plan_t p, const void* q, const void* k_pages, const void*
     a.max_splits = pl.s_max;
     a.num_tiles = static_cast<int32_t>(pl.items.size());
     a.fused_merge = p->opts.separate_merge ? 0 : 1;
+    a.all_merge = pl.merge == PKV_MERGE_ALL ? 1 : 0;
     a.use_mma = p->opts.math != PKV_MATH_FMA;
     a.copy_lsu = p->opts.copy != PKV_COPY_TMA;
     a.k_pages = static_cast<const uint16_t*>(k_pages);
@@ -613,6 +649,7 @@ int enqueue_decode(pkv_plan_t p, const void* q, const void* k_pages, const void*
         a.chunk_pages = dp->chunk;
         a.max_splits = dp->max_splits;
         a.fused_merge = 1;
+        a.all_merge = 0;
         grid = p->num_sms * std::max(1, p->ctas_per_sm);
         need_merge = false;
     }
@@ -624,7 +661,15 @@ int enqueue_decode(pkv_plan_t p, const void* q, const void* k_pages, const void*
     }
     int n = 0;
     if (grid > 0) {
-        PKV_CUDA(pkv::launch_attention(a, p->kmap, p->vmap, grid, s));
+        cudaError_t e = pkv::launch_attention(a, p->kmap, p->vmap, grid, s, a.all_merge != 0);
+        if (e == cudaErrorCooperativeLaunchTooLarge && a.all_merge) {
+            // the device holds fewer CTAs right now than planned for: the last
+            // arriving split merges instead (the counters are untouched)
+            (void)cudaGetLastError();
+            a.all_merge = 0;
+            e = pkv::launch_attention(a, p->kmap, p->vmap, grid, s, false);
+        }
+        PKV_CUDA(e);
         ++n;
         if (p->profile) PKV_CUDA(cudaEventRecord(p->ev[n], s));
     }

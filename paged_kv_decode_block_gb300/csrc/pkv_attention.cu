@@ -131,6 +131,25 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32
     return mbar_wait_slow(bar, parity, status, abort);
 }
 
+// Bounded wait (one thread) until the counter at `ctr` reaches `target`, read
+// with acquire semantics at GPU scope.  On expiry: flag the status word, raise
+// the CTA's abort flag and return false.
+__device__ __noinline__ bool wait_count(const uint32_t* ctr, uint32_t target, uint32_t* status, volatile int* abort) {
+    if (abort && *abort) return false;
+    const uint64_t start = globaltimer_ns();
+    while (true) {
+        uint32_t v;
+        asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(ctr) : "memory");
+        if (v >= target) return true;
+        if (globaltimer_ns() - start > kWaitLimitNs) {
+            atomicOr(status, static_cast<uint32_t>(PKV_DEV_TIMEOUT));
+            if (abort) *abort = 1;
+            return false;
+        }
+        __nanosleep(32);
+    }
+}
+
 __device__ __forceinline__ uint64_t l2_evict_first_policy() {
     uint64_t policy;
     asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(policy));
@@ -162,6 +181,12 @@ __device__ __forceinline__ void cp_async16_plain(uint32_t dst, const void* src) 
 __device__ __forceinline__ void cp_async_commit_wait_all() {
     asm volatile("cp.async.commit_group;\n\tcp.async.wait_all;" ::: "memory");
 }
+
+// Programmatic dependent launch: wait until the grids this launch depends on
+// have completed and their memory is visible (a no-op for an ordinary launch),
+// and let the next grid in the stream start launching its CTAs.
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
 // Release / acquire fence at GPU scope (message passing between CTAs).
 __device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
@@ -829,8 +854,7 @@ __device__ void merge_unit_staged(Smem<D, G>& sm, const AttnParams& p, int b, in
 
 // Tile of a queue entry: only the entry itself, so the producers can start
 // streaming its planned pages at once (all of them are in the row's table).
-__device__ __forceinline__ TileWork tile_from_item(const AttnParams& p, int t) {
-    const pkv_work_item it = p.queue[t];
+__device__ __forceinline__ TileWork tile_from_item(const AttnParams& p, const pkv_work_item& it) {
     TileWork tw;
     tw.b = it.b;
     tw.kvh = it.kvh;
@@ -1076,6 +1100,116 @@ __device__ void merge_if_last(Smem<D, G>& sm, const AttnParams& p, int b, int kv
     }
 }
 
+// The merge shared by all ns splits of (b, kvh), for a launch whose CTAs are
+// all resident at once (cooperative launch of one wave).  Each split publishes
+// its partial, waits until all ns have arrived, then merges its own 1/ns share
+// of the G*D/4 float4 outputs, lanes over the splits, so each CTA reads only
+// its share's columns of every partial (plus the LSEs) instead of one CTA
+// reading all of them.  Every split departs once after the
+// wait; the last to depart rewinds both counters for the next launch.  Same
+// exact LSE rule as merge_unit (all CTA threads call this).
+template <int D, int G>
+__device__ void merge_all_splits(Smem<D, G>& sm, const AttnParams& p, int b, int kvh, int split, int ns) {
+    __syncthreads();
+    const int u = b * p.Hkv + kvh;
+    uint32_t* arrive = p.arrive + u;
+    uint32_t* depart = p.arrive + static_cast<size_t>(p.B) * p.Hkv + u;
+    uint32_t departed = 0;   // thread 0: departures before this one (read after the merge)
+    if (threadIdx.x == 0) {
+        fence_acq_rel_gpu();   // release: the partial written above, before the arrival
+        atomicAdd(arrive, 1u);
+        const bool ok = wait_count(arrive, static_cast<uint32_t>(ns), &p.ctr->status, &sm.abort);
+        departed = atomicAdd(depart, 1u);
+        sm.tile_slot[1] = ok;
+    }
+    __syncthreads();
+    const bool ok = sm.tile_slot[1] != 0;
+    // This split's share: float4 outputs [i0, i1).  L lanes (a power of two, at
+    // most 32, at least ns when ns <= 32) merge one output over the splits, so
+    // a warp covers 32 / L outputs per pass and the whole share usually takes
+    // one pass: every load of the share is in flight at once.
+    constexpr int kItems = G * D / 4;
+    const int per = (kItems + ns - 1) / ns;
+    const int i0 = split * per, i1 = min(kItems, i0 + per);
+    int L = 1;
+    while (L < ns && L < 32) L <<= 1;
+    const int groups = 32 / L;
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int sub = lane % L, grp = lane / L;
+    const size_t base = static_cast<size_t>(p.row_start[b]) + static_cast<size_t>(kvh) * ns;
+    for (int pass = i0; pass < i1; pass += (kThreads / 32) * groups) {   // uniform over the CTA
+        const int i = pass + warp * groups + grp;
+        const bool live = i < i1;
+        const int g = live ? i / (D / 4) : 0, d = live ? (i % (D / 4)) * 4 : 0;
+        float m = -INFINITY, l = 0.f;
+        float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+        int nan = 0;
+        if (live) {
+            for (int s = sub; s < ns; s += L) {   // the lane's splits, merged online
+                const float ls = __ldcg(p.ws_lse + (base + s) * G + g);
+                const float4 o = __ldcg(reinterpret_cast<const float4*>(p.ws_o + ((base + s) * G + g) * D + d));
+                nan |= isnan(ls) ? 1 : 0;
+                if (ls > m) {
+                    const float c = exp2f(m - ls);   // m = -inf: 0
+                    l *= c;
+                    a.x *= c;
+                    a.y *= c;
+                    a.z *= c;
+                    a.w *= c;
+                    m = ls;
+                }
+                if (ls != -INFINITY) {
+                    const float e = exp2f(ls - m);
+                    l += e;
+                    a.x = fmaf(e, o.x, a.x);
+                    a.y = fmaf(e, o.y, a.y);
+                    a.z = fmaf(e, o.z, a.z);
+                    a.w = fmaf(e, o.w, a.w);
+                }
+            }
+        }
+        // combine the L lanes of the group (xor partners stay inside it)
+        float M = m;
+        for (int x = L / 2; x > 0; x >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, x));
+        const float sc = m != -INFINITY ? exp2f(m - M) : 0.f;
+        l *= sc;
+        a.x *= sc;
+        a.y *= sc;
+        a.z *= sc;
+        a.w *= sc;
+        for (int x = L / 2; x > 0; x >>= 1) {
+            l += __shfl_xor_sync(kFull, l, x);
+            a.x += __shfl_xor_sync(kFull, a.x, x);
+            a.y += __shfl_xor_sync(kFull, a.y, x);
+            a.z += __shfl_xor_sync(kFull, a.z, x);
+            a.w += __shfl_xor_sync(kFull, a.w, x);
+            nan |= __shfl_xor_sync(kFull, nan, x);
+        }
+        if (live && sub == 0) {
+            float4 o;
+            float lse2;
+            if (nan || !ok) {
+                o = make_float4(NAN, NAN, NAN, NAN);
+                lse2 = NAN;
+            } else if (M == -INFINITY) {
+                o = make_float4(0.f, 0.f, 0.f, 0.f);
+                lse2 = -INFINITY;
+            } else {
+                const float inv = 1.f / l;
+                o = make_float4(a.x * inv, a.y * inv, a.z * inv, a.w * inv);
+                lse2 = M + log2f(l);
+            }
+            const int h = kvh * G + g;
+            *reinterpret_cast<float4*>(p.out + (static_cast<size_t>(b) * p.Hq + h) * D + d) = o;
+            if (d == 0) p.lse[static_cast<size_t>(b) * p.Hq + h] = lse2 * kLn2;
+        }
+    }
+    if (threadIdx.x == 0 && departed == static_cast<uint32_t>(ns - 1)) {
+        *arrive = 0;   // every split has seen the full count: ready for the next launch
+        *depart = 0;
+    }
+}
+
 // After an abort, wait (bounded again) for every TMA copy this CTA issued, so
 // that none lands in shared memory after the CTA has moved on or exited.
 // Called by one thread once the producer has stopped issuing.
@@ -1102,13 +1236,16 @@ __global__ void __launch_bounds__(kThreads, MMA ? 2 : 1) attention_kernel(const 
         sm.abort = 0;
         fence_mbar_init();
     }
+    // Everything below reads what earlier kernels in the stream may have
+    // written (q, pages, lengths, table, plan): wait for them first.
+    grid_dependency_wait();
     __syncthreads();
-
-    if (p.route == kRoutePersistent || p.route == kRouteQueue) {
-        // rows with no tokens get no tiles: write their neutral state here
+    // rows with no tokens get no tiles: their neutral state is written after
+    // the CTA's own tile, off the tile's critical path
+    auto neutral_rows = [&]() {
         for (int b = blockIdx.x; b < p.B; b += gridDim.x)
             if (p.row_splits[b] == 0) write_neutral_row(p, b, threadIdx.x, blockDim.x);
-    }
+    };
 
     if (p.route == kRoutePersistent) {
         const int num_tiles = p.tiles_d ? *p.tiles_d : p.num_tiles;   // a device-planned step sets it
@@ -1118,13 +1255,15 @@ __global__ void __launch_bounds__(kThreads, MMA ? 2 : 1) attention_kernel(const 
             __syncthreads();
             const int t = sm.tile_slot[0];
             if (t >= num_tiles) break;
-            const TileWork tw = tile_from_item(p, p.order ? p.order[t] : t);
+            const TileWork tw = tile_from_item(p, p.queue[p.order ? p.order[t] : t]);
             run_tile<D, G, MMA>(sm, p, tw, pipe, &kmap, &vmap);
             pipe += stream_blocks(tw);
             __syncthreads();
             if (!sm.tile_fin && p.fused_merge) merge_if_last<D, G>(sm, p, tw.b, tw.kvh, sm.tile_splits);
             __syncthreads();
         }
+        launch_dependents();
+        neutral_rows();
         if (threadIdx.x == 0) {
             if (sm.abort) drain_after_abort<D, G>(sm, &p.ctr->status);
             // the last CTA out rewinds the queue for the next launch
@@ -1155,13 +1294,18 @@ __global__ void __launch_bounds__(kThreads, MMA ? 2 : 1) attention_kernel(const 
         }
         tw.t_stream = tw.t1;
     } else if (p.route == kRouteQueue) {
-        if (static_cast<int>(blockIdx.x) >= p.num_tiles) return;   // launched only for the neutral rows
-        tw = tile_from_item(p, blockIdx.x);
+        if (static_cast<int>(blockIdx.x) >= p.num_tiles) {   // launched only for the neutral rows
+            launch_dependents();
+            neutral_rows();
+            return;
+        }
+        tw = tile_from_item(p, p.queue[blockIdx.x]);
     } else {   // padded grid: (b, kvh, s) from the block index, ranges from the device lengths
         const int per_row = p.Hkv * p.max_splits;
         tw.b = blockIdx.x / per_row;
         tw.kvh = (blockIdx.x % per_row) / p.max_splits;
         const int s = blockIdx.x % p.max_splits;
+        tw.split = s;
         const int n = p.seq_lens[tw.b];
         const int pages = (n + p.page_size - 1) / p.page_size;
         tw.poisoned = n < 0 || pages > p.max_splits * p.chunk_pages || n > p.max_pages * p.page_size;
@@ -1177,7 +1321,14 @@ __global__ void __launch_bounds__(kThreads, MMA ? 2 : 1) attention_kernel(const 
     }
     run_tile<D, G, MMA>(sm, p, tw, 0, &kmap, &vmap);
     __syncthreads();
-    if (!sm.tile_fin && p.fused_merge) merge_if_last<D, G>(sm, p, tw.b, tw.kvh, sm.tile_splits);
+    launch_dependents();   // the next grid may start its CTAs in the slots this tail frees
+    if (!sm.tile_fin && p.fused_merge) {
+        if (p.all_merge)
+            merge_all_splits<D, G>(sm, p, tw.b, tw.kvh, tw.split, sm.tile_splits);
+        else
+            merge_if_last<D, G>(sm, p, tw.b, tw.kvh, sm.tile_splits);
+    }
+    if (p.route == kRouteQueue) neutral_rows();
     if (threadIdx.x == 0 && sm.abort) drain_after_abort<D, G>(sm, &p.ctr->status);
 }
 
@@ -1203,7 +1354,7 @@ __global__ void __launch_bounds__(128) merge_kernel(const AttnParams p) {
 
 template <int D, int G, bool MMA>
 cudaError_t launch_attention_t(const AttnParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap, int grid,
-                               cudaStream_t stream) {
+                               cudaStream_t stream, bool cooperative) {
     constexpr size_t smem = smem_bytes<D, G>();
     static bool configured = false;
     if (!configured) {
@@ -1212,8 +1363,27 @@ cudaError_t launch_attention_t(const AttnParams& p, const CUtensorMap& kmap, con
         if (e != cudaSuccess) return e;
         configured = true;
     }
-    attention_kernel<D, G, MMA><<<grid, kThreads, smem, stream>>>(p, kmap, vmap);
-    return cudaGetLastError();
+    // The launch may overlap the tail of the previous kernel in the stream
+    // (programmatic dependent launch; the kernel waits for it before reading
+    // anything); cooperative: every CTA resident at once, or the launch fails.
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    int n = 0;
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+    if (cooperative) {
+        attr[n].id = cudaLaunchAttributeCooperative;
+        attr[n].val.cooperative = 1;
+        ++n;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = n;
+    return cudaLaunchKernelEx(&cfg, attention_kernel<D, G, MMA>, p, kmap, vmap);
 }
 
 template <int D, int G, bool MMA>
@@ -1283,11 +1453,11 @@ int attention_ctas_per_sm(int D, int G, bool mma) {
 }
 
 cudaError_t launch_attention(const AttnParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap, int grid,
-                             cudaStream_t stream) {
+                             cudaStream_t stream, bool cooperative) {
     const int G = p.Hq / p.Hkv;
     PKV_DISPATCH(p.D, G,
-                 return p.use_mma ? launch_attention_t<kD, kG, true>(p, kmap, vmap, grid, stream)
-                                  : launch_attention_t<kD, kG, false>(p, kmap, vmap, grid, stream));
+                 return p.use_mma ? launch_attention_t<kD, kG, true>(p, kmap, vmap, grid, stream, cooperative)
+                                  : launch_attention_t<kD, kG, false>(p, kmap, vmap, grid, stream, cooperative));
     return cudaErrorInvalidValue;
 }
 

@@ -50,12 +50,14 @@ struct AttnParams {
     float* lse;                   // [B][Hq]
     float* ws_o;                  // [slots][G][D] normalised partial outputs
     float* ws_lse;                // [slots][G] partial LSE, log2 units
-    uint32_t* arrive;             // [B*Hkv] fused-merge arrival counters
+    uint32_t* arrive;             // [2][B*Hkv] fused-merge arrival, then departure counters
     DeviceCounters* ctr;
     int32_t B, Hq, Hkv, D, page_size, max_pages, num_pages;
     int32_t chunk_pages, max_splits, num_tiles;
     int32_t route;
-    int32_t fused_merge;          // split tiles: the last arriving split of (b, kvh) merges
+    int32_t fused_merge;          // split tiles merge inside the attention launch
+    int32_t all_merge;            // ... every split merges its share once all have arrived
+                                  //     (cooperative one-wave launch); else the last arriver
     int32_t use_mma;              // block reduction on tensor cores (mma.sync) instead of FMA
     int32_t copy_lsu;             // stage K/V with cp.async from the producer warp instead of TMA
     float scale_log2;             // log2(e) / sqrt(D)
@@ -86,7 +88,7 @@ cudaError_t launch_plan_step(const DevPlanParams& p, cudaStream_t stream);
 // of the K and V pools viewed as [page_size * num_pages][Hkv][D] (innermost D),
 // box {64, 1, kBlockRows}, 128-byte swizzle.
 cudaError_t launch_attention(const AttnParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap,
-                             int grid, cudaStream_t stream);
+                             int grid, cudaStream_t stream, bool cooperative = false);
 cudaError_t launch_merge(const AttnParams& p, cudaStream_t stream);
 cudaError_t launch_append(const uint16_t* k_new, const uint16_t* v_new, uint16_t* k_pages,
                           uint16_t* v_pages, const int32_t* block_table, int32_t* seq_lens,

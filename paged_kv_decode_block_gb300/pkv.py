@@ -21,6 +21,8 @@ MODE_NAMES = {MODE_AUTO: "auto", MODE_DIRECT: "direct", MODE_SPLIT_QUEUE: "split
 MODES = {v: k for k, v in MODE_NAMES.items()}
 MATH = {"auto": 0, "fma": 1, "mma": 2}
 COPY = {"auto": 0, "lsu": 1, "tma": 2}
+MERGE = {"auto": 0, "last": 1, "all": 2}
+MERGE_NAMES = {0: "none", 1: "last", 2: "all", 3: "separate"}
 
 OK, EINVAL, ENOMEM, ECUDA, EUNSUPPORTED, EDEVICE, ENOSPACE = range(7)
 DEV_PAGE_OOB, DEV_PLAN_MISMATCH, DEV_TIMEOUT, DEV_ROW_FULL = 1, 2, 4, 8
@@ -37,7 +39,7 @@ class PlanOpts(ctypes.Structure):
                 ("direct_units_per_sm", ctypes.c_int32), ("target_ctas_per_sm", ctypes.c_int32),
                 ("min_chunk_pages", ctypes.c_int32), ("ctas_per_sm", ctypes.c_int32),
                 ("separate_merge", ctypes.c_int32), ("num_sms", ctypes.c_int32),
-                ("math", ctypes.c_int32), ("copy", ctypes.c_int32)]
+                ("math", ctypes.c_int32), ("copy", ctypes.c_int32), ("merge", ctypes.c_int32)]
 
 
 class WorkItem(ctypes.Structure):
@@ -50,13 +52,14 @@ class PlanInfo(ctypes.Structure):
                 ("max_splits", ctypes.c_int32), ("num_tiles", ctypes.c_int32),
                 ("num_work_items", ctypes.c_int32), ("empty_tiles", ctypes.c_int32),
                 ("launches_per_step", ctypes.c_int32), ("grid_ctas", ctypes.c_int32),
-                ("num_sms", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("num_sms", ctypes.c_int32), ("merge", ctypes.c_int32),
                 ("kv_bytes", ctypes.c_int64), ("workspace_bytes", ctypes.c_int64),
                 ("table_bytes", ctypes.c_int64)]
 
     def as_dict(self) -> dict:
-        d = {name: getattr(self, name) for name, _ in self._fields_ if name != "reserved"}
+        d = {name: getattr(self, name) for name, _ in self._fields_}
         d["mode_name"] = MODE_NAMES.get(self.mode, "?")
+        d["merge_name"] = MERGE_NAMES.get(self.merge, "?")
         return d
 
 
@@ -139,16 +142,18 @@ def _ptr_i32(a):
 
 def _opts(force_mode=MODE_AUTO, num_splits=0, direct_units_per_sm=0, target_ctas_per_sm=0,
           min_chunk_pages=0, ctas_per_sm=0, separate_merge=False, num_sms=0, math="auto",
-          copy="auto") -> PlanOpts:
+          copy="auto", merge="auto") -> PlanOpts:
     if isinstance(force_mode, str):
         force_mode = MODES[force_mode]
     if isinstance(math, str):
         math = MATH[math]
     if isinstance(copy, str):
         copy = COPY[copy]
+    if isinstance(merge, str):
+        merge = MERGE[merge]
     return PlanOpts(int(force_mode), int(num_splits), int(direct_units_per_sm),
                     int(target_ctas_per_sm), int(min_chunk_pages), int(ctas_per_sm),
-                    int(bool(separate_merge)), int(num_sms), int(math), int(copy))
+                    int(bool(separate_merge)), int(num_sms), int(math), int(copy), int(merge))
 
 
 def _geom(B, Hq, Hkv, D, max_pages, num_pages) -> Geom:

@@ -116,6 +116,54 @@ def test_larger_pages(page_size, copy):
         assert_close(out, lse, *ref, what=f"ps={page_size} {route} {copy}")
 
 
+MERGES = ["last", "all"]
+
+
+@pytest.mark.parametrize("merge", MERGES)
+@pytest.mark.parametrize("route", ["split_queue", "split_padded"])
+@pytest.mark.parametrize("splits", [2, 3, 16])
+def test_fused_merge_kinds(route, splits, merge):
+    """Both fused merges (last arriver; every split sharing out the outputs) match
+    the oracle, and their counters rewind: repeated launches give the same bits."""
+    p = wl.make_problem("merges", EDGE_LENS, Hq=8, Hkv=2, D=128, page_size=16, num_pages=48, seed=27)
+    ref = oracle_result(p)
+    out, lse, plan, dev = run(p, force_mode=route, num_splits=splits, merge=merge)
+    assert plan.info()["merge_name"] == merge
+    assert_close(out, lse, *ref, what=f"{merge} merge {route} S={splits}")
+    for _ in range(2):
+        out2, lse2, _, _ = run(p, dev=dev, plan=plan)
+        assert np.array_equal(out2, out) and np.array_equal(lse2, lse)
+    assert plan.status() == 0
+
+
+@pytest.mark.parametrize("merge", MERGES)
+@pytest.mark.parametrize("Hq,D", [(8, 128), (2, 64)])
+def test_fused_merge_more_splits_than_lanes(merge, Hq, D):
+    """64 splits of one (row, KV head): more than a warp's lanes; with G = 1 and
+    D = 64 also more splits than float4 outputs, so some splits merge nothing."""
+    p = wl.make_problem("manysplits", [4096, 1000, 17, 0], Hq=Hq, Hkv=2, D=D, page_size=16,
+                        num_pages=360, seed=28)
+    ref = oracle_result(p)
+    out, lse, plan, _ = run(p, force_mode="split_queue", num_splits=64, merge=merge)
+    info = plan.info()
+    assert info["merge_name"] == merge and info["max_splits"] == 64
+    assert_close(out, lse, *ref, what=f"{merge} merge, 64 splits")
+    assert plan.status() == 0
+
+
+@pytest.mark.parametrize("merge", MERGES)
+def test_bad_page_poisons_through_either_merge(merge):
+    p = wl.tiny()
+    bad = p.block_table.copy()
+    bad[1, 2] = p.num_pages + 5
+    p_bad = wl.Problem("bad", p.q, p.k_pages, p.v_pages, bad, p.seq_lens, p.page_size)
+    for route in ["split_queue", "split_padded"]:
+        out, lse, plan, _ = run(p_bad, host_table=False, force_mode=route, num_splits=4, merge=merge)
+        assert plan.status() & pkv.DEV_PAGE_OOB, route
+        assert np.all(np.isnan(out[1])) and np.all(np.isnan(lse[1])), route
+        assert np.all(np.isfinite(out[0])), route
+
+
 def test_all_rows_empty():
     p = wl.make_problem("empty", [0, 0, 0], Hq=4, Hkv=1, D=64, page_size=16, num_pages=4, seed=24)
     for route in ROUTES:
@@ -195,12 +243,13 @@ def mixed_ref():
     return p, oracle_result(p, nthreads=16)
 
 
-@pytest.mark.parametrize("math,copy", [("fma", "lsu"), ("mma", "lsu"), ("mma", "tma")])
+@pytest.mark.parametrize("math,copy,merge", [("fma", "lsu", "auto"), ("mma", "lsu", "auto"), ("mma", "tma", "auto"),
+                                             ("mma", "lsu", "last")])
 @pytest.mark.parametrize("route", ["split_queue", "persistent"])
-def test_batch1_long_32k(route, math, copy, batch1_long_ref):
+def test_batch1_long_32k(route, math, copy, merge, batch1_long_ref):
     p, ref = batch1_long_ref
-    out, lse, plan, _ = run(p, force_mode=route, num_splits=32, math=math, copy=copy)
-    assert_close(out, lse, *ref, what=f"batch1_long {route} {math} {copy}")
+    out, lse, plan, _ = run(p, force_mode=route, num_splits=32, math=math, copy=copy, merge=merge)
+    assert_close(out, lse, *ref, what=f"batch1_long {route} {math} {copy} {merge}")
     info = plan.info()
     assert info["chunk_pages"] == 64 and info["num_work_items"] == 256
     assert np.array_equal(plan.queue(), expected_queue(p, info))

@@ -239,3 +239,30 @@ def test_policy_on_trace_families_never_picks_direct_below_one_wave():
             if max(lens) > 16 * 8:
                 assert info["mode_name"] == "split_queue", (kind, B)
                 assert info["num_work_items"] <= 2 * NUM_SMS
+
+
+def test_merge_choice_follows_route_and_wave():
+    """Fused merge: the last arriving split merges (LAST) unless every split is asked
+    to share it out (ALL), which needs a split launch of one wave of resident CTAs.
+    The dry run takes num_sms * ctas_per_sm as the resident capacity."""
+    lens = [4096, 1000, 17, 0]
+    kw = dict(B=4, Hq=8, Hkv=2, D=128, max_pages=256, num_pages=600)
+
+    def info(**o):
+        return pkv.dry_run(lens, None, 16, num_sms=NUM_SMS, ctas_per_sm=2, **kw, **o)[0]
+
+    assert info(force_mode="split_queue", num_splits=8)["merge_name"] == "last"
+    assert info(force_mode="split_queue", num_splits=8, merge="all")["merge_name"] == "all"
+    assert info(force_mode="split_padded", num_splits=8, merge="all")["merge_name"] == "all"
+    assert info(force_mode="split_queue", num_splits=8, merge="last")["merge_name"] == "last"
+    assert info(force_mode="split_queue", num_splits=8, separate_merge=True)["merge_name"] == "separate"
+    assert info(force_mode="persistent", num_splits=8)["merge_name"] == "last"
+    assert info(force_mode="direct")["merge_name"] == "none"
+    assert info(force_mode="split_queue", num_splits=1)["merge_name"] == "none"
+    # more tiles than resident CTAs: ALL is refused
+    small = dict(num_sms=4, ctas_per_sm=2)
+    i = pkv.dry_run(lens, None, 16, **small, **kw, force_mode="split_queue", num_splits=8)[0]
+    assert i["num_tiles"] > 8 and i["merge_name"] == "last"
+    with pytest.raises(pkv.PkvError) as e:
+        pkv.dry_run(lens, None, 16, **small, **kw, force_mode="split_queue", num_splits=8, merge="all")
+    assert e.value.code == pkv.EUNSUPPORTED
