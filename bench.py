@@ -259,6 +259,8 @@ def run_pkv(args):
     # (the L2 keeps a few percent of lines across 3 x L2 of streaming, measured
     # with ncu; across 6 x L2 under 0.3 %).
     rot = 1 if step_bytes >= 6 * l2 else 1 + -(-6 * l2 // step_bytes)
+    if args.copies:
+        rot = args.copies   # e.g. 1 under a profiler, which flushes caches itself
     streamed = rot <= 16
     copies = [(q, k, v)] + [(q.clone(), k.clone(), v.clone()) for _ in range(rot - 1 if streamed else 0)]
     # The clones leave their last pages in L2 at normal priority, where the
@@ -648,6 +650,8 @@ def main():
                     help="continuous: plan each step on the device (pkv_session_device_plan)")
     ap.add_argument("--graph", action="store_true",
                     help="continuous: device-planned step captured once in a CUDA graph and replayed")
+    ap.add_argument("--copies", type=int, default=0,
+                    help="copies of the inputs used round robin (default: enough for >= 6 x L2 between reuses)")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time for the CPU baseline")
     ap.add_argument("--skip-cpu", action="store_true")
     args = ap.parse_args()
