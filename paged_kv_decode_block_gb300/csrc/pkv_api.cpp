@@ -628,6 +628,7 @@ int enqueue_decode(pkv_plan_t p, const void* q, const void* k_pages, const void*
     a.all_merge = pl.merge == PKV_MERGE_ALL ? 1 : 0;
     a.use_mma = p->opts.math != PKV_MATH_FMA;
     a.copy_lsu = p->opts.copy != PKV_COPY_TMA;
+    a.queue_host_staged = dp ? 0 : 1;
     a.k_pages = static_cast<const uint16_t*>(k_pages);
     a.v_pages = static_cast<const uint16_t*>(v_pages);
     a.scale_log2 = static_cast<float>(1.4426950408889634 / sqrt(static_cast<double>(p->g.head_dim)));

@@ -188,6 +188,16 @@ __device__ __forceinline__ void cp_async_commit_wait_all() {
 __device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
+// Hint: bring the 128-byte line holding `p` into L2 (no data returns; a stale
+// or unused prefetch changes nothing but the cache).
+__device__ __forceinline__ void prefetch_l2(const void* p) { asm volatile("prefetch.global.L2 [%0];" ::"l"(p)); }
+
+__device__ __forceinline__ int32_t ld_volatile_i32(const int32_t* p) {
+    int32_t v;
+    asm volatile("ld.volatile.global.s32 %0, [%1];" : "=r"(v) : "l"(p));
+    return v;
+}
+
 // Release / acquire fence at GPU scope (message passing between CTAs).
 __device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
 
@@ -1226,6 +1236,35 @@ __global__ void __launch_bounds__(kThreads, MMA ? 2 : 1) attention_kernel(const 
     extern __shared__ uint8_t smem_raw[];
     Smem<D, G>& sm =
         *reinterpret_cast<Smem<D, G>*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    // Before the grid dependency wait, only data no kernel writes may be used:
+    // the host-staged queue entry.  The producers also warm L2 with the first
+    // ring's worth of the tile's K/V rows, reading the block table
+    // speculatively: prefetches change no value, and every value used below is
+    // read again after the wait.
+    const bool staged_item = p.route == kRouteQueue && p.queue_host_staged && static_cast<int>(blockIdx.x) < p.num_tiles;
+    pkv_work_item item{};
+    if (staged_item) {
+        item = p.queue[blockIdx.x];
+        const int pw = static_cast<int>(threadIdx.x) / 32 - kConsumerWarps;
+        if (pw >= 0 && item.b >= 0 && item.b < p.B && item.kvh >= 0 && item.kvh < p.Hkv && item.page_begin >= 0 &&
+            item.page_end <= p.max_pages) {
+            const int lane = threadIdx.x % 32;
+            const int ps = p.page_size;
+            const int t0 = item.page_begin * ps;
+            const int t_end = min(item.page_end * ps, t0 + Cfg<D, G>::kStages * kBlockRows);
+            const int32_t* bt_row = p.block_table + static_cast<size_t>(item.b) * p.max_pages;
+            for (int tok = t0 + pw * 32 + lane; tok < t_end; tok += kProducerWarps * 32) {
+                const int page = ld_volatile_i32(bt_row + tok / ps);
+                if (page < 0 || page >= p.num_pages) continue;
+                const size_t row = (static_cast<size_t>(page) * ps + tok % ps) * p.Hkv + item.kvh;
+#pragma unroll
+                for (int c = 0; c < D * 2; c += 128) {
+                    prefetch_l2(reinterpret_cast<const uint8_t*>(p.k_pages + row * D) + c);
+                    prefetch_l2(reinterpret_cast<const uint8_t*>(p.v_pages + row * D) + c);
+                }
+            }
+        }
+    }
     if (threadIdx.x == 0) {
         for (int s = 0; s < Cfg<D, G>::kStages; ++s) {
             // LSU copies: 32 producer lanes' cp.async arrivals + lane 0's flag arrival
@@ -1299,7 +1338,7 @@ __global__ void __launch_bounds__(kThreads, MMA ? 2 : 1) attention_kernel(const 
             neutral_rows();
             return;
         }
-        tw = tile_from_item(p, p.queue[blockIdx.x]);
+        tw = tile_from_item(p, staged_item ? item : p.queue[blockIdx.x]);
     } else {   // padded grid: (b, kvh, s) from the block index, ranges from the device lengths
         const int per_row = p.Hkv * p.max_splits;
         tw.b = blockIdx.x / per_row;

@@ -60,6 +60,9 @@ struct AttnParams {
                                   //     (cooperative one-wave launch); else the last arriver
     int32_t use_mma;              // block reduction on tensor cores (mma.sync) instead of FMA
     int32_t copy_lsu;             // stage K/V with cp.async from the producer warp instead of TMA
+    int32_t queue_host_staged;    // queue / row_start / row_splits come from a host upload (never
+                                  // written by a kernel), so they may be read before the grid
+                                  // dependency wait
     float scale_log2;             // log2(e) / sqrt(D)
 };
 
