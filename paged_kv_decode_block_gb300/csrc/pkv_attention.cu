@@ -59,6 +59,7 @@ namespace {
 constexpr int kConsumerWarps = 4;
 constexpr int kProducerWarps = 2;   // block j is staged by producer warp j % kProducerWarps
 constexpr int kThreads = (kConsumerWarps + kProducerWarps) * 32;
+constexpr int kPrefetchBlocks = 8;   // blocks of a tile warmed in L2 before the grid dependency wait
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 constexpr unsigned kFull = 0xffffffffu;
 constexpr float kLn2 = 0.69314718055994530942f;
@@ -1089,6 +1090,7 @@ __device__ void merge_if_last(Smem<D, G>& sm, const AttnParams& p, int b, int kv
     // The CTA's partial is written; after the barrier, thread 0's fence makes those
     // writes visible device-wide before its arrival is counted (release), and after
     // the arrival its fence orders the other splits' writes before our reads (acquire).
+    // (The caller has just passed a barrier too; dropping this one measured slower.)
     __syncthreads();
     if (threadIdx.x == 0) {
         const int u = b * p.Hkv + kvh;
@@ -1251,7 +1253,7 @@ __global__ void __launch_bounds__(kThreads, MMA ? 2 : 1) attention_kernel(const 
             const int lane = threadIdx.x % 32;
             const int ps = p.page_size;
             const int t0 = item.page_begin * ps;
-            const int t_end = min(item.page_end * ps, t0 + Cfg<D, G>::kStages * kBlockRows);
+            const int t_end = min(item.page_end * ps, t0 + kPrefetchBlocks * kBlockRows);
             const int32_t* bt_row = p.block_table + static_cast<size_t>(item.b) * p.max_pages;
             for (int tok = t0 + pw * 32 + lane; tok < t_end; tok += kProducerWarps * 32) {
                 const int page = ld_volatile_i32(bt_row + tok / ps);
