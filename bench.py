@@ -595,6 +595,123 @@ def run_continuous(args):
         print(json.dumps(line), flush=True)
 
 
+def run_resident(args):
+    """The continuous-session workload on one resident kernel (pkv_resident_*):
+    launched once, it runs every step the host publishes (device plan, append,
+    persistent decode, grid barriers between them).  Each step's new tokens and
+    q go host -> device from pinned memory, and out / lse come back, inside the
+    step call.  Device time per step comes from the kernel's own globaltimer
+    stamps (step seen -> outputs published); the decode phase's stamps give the
+    attention time for the roofline."""
+    import torch
+    import oracle
+    from paged_kv_decode_block_gb300 import pkv
+    from paged_kv_decode_block_gb300 import workloads as wl
+    from paged_kv_decode_block_gb300.session import ContinuousSessions
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    pkv.load()
+    steps = args.steps
+    total = args.warmup + steps
+    p = wl.continuous(steps=total + 1)
+    splits = 1 if args.num_splits is None else args.num_splits
+    sess = ContinuousSessions(p, force_mode="persistent", num_splits=splits, math=args.math, copy=args.copy)
+    sess.session.device_plan()
+    rng = np.random.default_rng(wl.HELD_OUT_SEED + 1)
+    toks = [wl.new_tokens(rng, p.B, p.Hkv, p.D) for _ in range(total)]
+    kh = torch.from_numpy(np.stack([t[0] for t in toks]).view(np.int16)).pin_memory()
+    vh = torch.from_numpy(np.stack([t[1] for t in toks]).view(np.int16)).pin_memory()
+    qh = torch.from_numpy(p.q.view(np.int16)).pin_memory()
+    oh = torch.empty(sess.out.shape, dtype=torch.float32).pin_memory()
+    lh = torch.empty(sess.lse.shape, dtype=torch.float32).pin_memory()
+    kbuf = torch.empty((p.B, p.Hkv, p.D), dtype=torch.int16, device="cuda")
+    vbuf = torch.empty_like(kbuf)
+    lens0 = int(p.seq_lens.astype(np.int64).sum())
+    torch.cuda.synchronize()
+    res = pkv.Resident(sess.session, sess.k, sess.v, sess.q, kbuf, vbuf, sess.out, sess.lse,
+                       idle_limit_ns=20_000_000_000, times_cap=total)
+    wall_us = []
+    try:
+        # correctness gate on the first step (the kernel waits while the host checks)
+        res.step(q_h=qh, k_new_h=kh[0], v_new_h=vh[0], out_h=oh, lse_h=lh)
+        table0 = p.block_table.copy()
+        free = list(p.free_pages)
+        for b in range(p.B):
+            if p.seq_lens[b] % p.page_size == 0 and table0[b, p.seq_lens[b] // p.page_size] < 0:
+                table0[b, p.seq_lens[b] // p.page_size] = free.pop(0)
+        k0, v0, l0 = oracle.append(toks[0][0], toks[0][1], p.k_pages, p.v_pages, table0, p.seq_lens)
+        ref_out, ref_lse = oracle.decode(p.q, k0, v0, table0, l0, nthreads=host_cores())
+        del k0, v0
+        err_out = float(np.max(np.abs(oh.numpy() - ref_out)))
+        err_lse = float(np.max(np.abs(lh.numpy() - ref_lse)))
+        log(f"parity vs oracle (step 0): max|out|={err_out:.3g} max|lse|={err_lse:.3g}")
+        if err_out > 2e-3 or err_lse > 1e-4:
+            raise SystemExit("parity gate failed; not timing")
+        for i in range(1, args.warmup):
+            res.step(q_h=qh, k_new_h=kh[i], v_new_h=vh[i], out_h=oh, lse_h=lh)
+        with ClockSampler(smi_index(local)) as clk:
+            time.sleep(0.3)
+            t_region = time.perf_counter()
+            for i in range(args.warmup, total):
+                t0 = time.perf_counter()
+                res.step(q_h=qh, k_new_h=kh[i], v_new_h=vh[i], out_h=oh, lse_h=lh)
+                wall_us.append((time.perf_counter() - t0) * 1e6)
+            t_region = time.perf_counter() - t_region
+            time.sleep(0.3)
+    finally:
+        res.stop()
+    stamps = res.times().astype(np.int64)[args.warmup:total]
+    res.close()
+    if sess.plan.status() != 0:
+        raise SystemExit("device status word set")
+    dev_us = (stamps[:, 3] - stamps[:, 0]) / 1e3
+    dec_us = (stamps[:, 3] - stamps[:, 2]) / 1e3
+    kv = [(lens0 + (i + 1) * p.B) * p.Hkv * p.D * 4 for i in range(args.warmup, total)]
+    value = float(np.sum(kv)) / (float(np.sum(dev_us)) * 1e-6) / 1e9
+    peak, peak_src = hbm_peak()
+    q_bytes = p.B * p.Hq * p.D * 2
+    achieved = float(np.mean([(k + q_bytes) / (t * 1e-6) / 1e9 for k, t in zip(kv, dec_us)]))
+    clocks = clk.summary()
+    info = sess.plan.info()
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": steps,
+        "warmup": args.warmup, "ms_per_step": round(float(np.median(dev_us)) / 1e3, 5),
+        "us_per_step": {"device_p50": round(float(np.percentile(dev_us, 50)), 2),
+                        "device_p99": round(float(np.percentile(dev_us, 99)), 2),
+                        "decode_phase_p50": round(float(np.percentile(dec_us, 50)), 2),
+                        "wall_p50": round(float(np.percentile(wall_us, 50)), 2),
+                        "wall_p99": round(float(np.percentile(wall_us, 99)), 2)},
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16 in, fp32 accumulate", "data": "synthetic (seeded, bf16 ~N(0,1))",
+        "config": {"workload": p.name, "sessions": p.B, "seq_lens": "U[1024, 8192] + appended",
+                   "q_heads": p.Hq, "kv_heads": p.Hkv, "head_dim": p.D, "page_size": p.page_size,
+                   "num_pages": p.num_pages, "mode": "resident (one cooperative launch for all steps)",
+                   "math": args.math, "copy": args.copy, "num_splits": splits,
+                   "l2": "not flushed: each step reads ~1 GB of KV, far above L2",
+                   "step": "device plan + append + persistent decode inside one resident kernel, grid barriers "
+                           "between them; the host publishes each step through mapped pinned memory"},
+        "kv_bytes_per_step": int(np.mean(kv)),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "peak_source": peak_src,
+                     "kernel": "resident_kernel, decode phase (append done -> outputs published)",
+                     "algorithmic_bytes_per_launch": int(np.mean(kv)) + q_bytes, "traffic": None},
+        "e2e": {"value": round(float(np.mean(kv)) / (float(np.median(wall_us)) * 1e-6) / 1e9, 2), "unit": "GB/s",
+                "us_per_step": round(float(np.median(wall_us)), 2),
+                "h2d_bytes_per_step": 2 * p.B * p.Hkv * p.D * 2 + q_bytes,
+                "d2h_bytes_per_step": p.B * p.Hq * (p.D + 1) * 4},
+        "gpu_launches": 1,
+        "cpu_baseline": None,
+        "clocks": {"sm_mhz": clocks["sm_mhz"], "sm_max_mhz": clocks["sm_max_mhz"],
+                   "reasons": clocks["reasons"], "samples": clocks["samples"]},
+        "timed_region_wall_s": round(t_region, 4),
+        "parity": {"max_abs_out": err_out, "max_abs_lse": err_lse, "checked_step": 0},
+        "tiles": info["num_work_items"],
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
 # ----------------------------------------------------------------------------- reference arm
 
 def run_reference(args):
@@ -650,6 +767,8 @@ def main():
                     help="continuous: plan each step on the device (pkv_session_device_plan)")
     ap.add_argument("--graph", action="store_true",
                     help="continuous: device-planned step captured once in a CUDA graph and replayed")
+    ap.add_argument("--resident", action="store_true",
+                    help="continuous workload: one resident kernel runs every step (pkv_resident_*)")
     ap.add_argument("--copies", type=int, default=0,
                     help="copies of the inputs used round robin (default: enough for >= 6 x L2 between reuses)")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time for the CPU baseline")
@@ -659,6 +778,8 @@ def main():
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":
         run_reference(args)
+    elif args.workload == "continuous" and args.resident:
+        run_resident(args)
     elif args.workload == "continuous":
         run_continuous(args)
     else:

@@ -361,6 +361,52 @@ int pkv_session_device_plan(pkv_session_t session, pkv_stream_t stream);
 int pkv_session_device_queue(pkv_session_t session, pkv_work_item *items, int32_t *order, int32_t capacity,
                              int32_t *count);
 
+/*
+ * Resident steps (a continuous session kept on the GPU by one launch).
+ * pkv_resident_start launches one cooperative kernel over every SM on a stream
+ * of its own; the kernel stays resident and runs one step each time the host
+ * publishes one through a control block in mapped pinned host memory.  A step
+ * is what a device-planned pkv_session_step enqueues -- page allocation and
+ * plan (the device planner), the append of k_new / v_new, the persistent
+ * decode of q into out / lse -- separated by grid-wide barriers instead of
+ * launches, in the spirit of the persistent worker of "GPUOS" (arXiv
+ * 2604.17861, section 4.1) and the resident beat of "WPK persistent kernel"
+ * (dotwave.ai).
+ *   pkv_resident_start   session in device-plan mode; k_pages / v_pages the
+ *                        pools; q_d, k_new_d, v_new_d, out_d, lse_d device
+ *                        buffers of the step's inputs and outputs (caller
+ *                        owned, bound for the kernel's life); idle_limit_ns
+ *                        (0, 60 s]: the longest the kernel waits for the next
+ *                        step before leaving with PKV_DEV_TIMEOUT; times_cap:
+ *                        steps whose device start / end times are kept.
+ *                        Synchronises the device first.  PKV_EUNSUPPORTED if
+ *                        the kernel cannot be resident on this device
+ *   pkv_resident_step    copies the host inputs given (pinned host pointers, or
+ *                        NULL to keep the device buffer) to the bound buffers,
+ *                        publishes the step, waits (at most wait_limit_ns) for
+ *                        the kernel to finish it, then copies out / lse to the
+ *                        host pointers given.  PKV_EDEVICE if the kernel left
+ *                        its loop or the wait ran out (then pkv_resident_stop)
+ *   pkv_resident_stop    asks the kernel to leave and waits for it; PKV_EDEVICE
+ *                        if it had left on an error (see pkv_status)
+ *   pkv_resident_times   after stop: [count][4] globaltimer ns of each kept
+ *                        step: the kernel saw it, plan done, append done,
+ *                        outputs published (the last times_cap steps, by
+ *                        step index modulo times_cap)
+ * While a resident kernel runs, the session refuses pkv_session_step and its
+ * read-back calls (PKV_EINVAL), and no other kernel should be queued behind it
+ * on the device: it holds every SM until it is stopped.
+ */
+typedef struct pkv_resident_s *pkv_resident_t;
+int pkv_resident_start(pkv_session_t session, void *k_pages, void *v_pages, void *q_d, void *k_new_d,
+                       void *v_new_d, float *out_d, float *lse_d, int64_t idle_limit_ns, int32_t times_cap,
+                       pkv_resident_t *resident);
+int pkv_resident_step(pkv_resident_t resident, const void *q_h, const void *k_new_h, const void *v_new_h,
+                      float *out_h, float *lse_h, int64_t wait_limit_ns);
+int pkv_resident_stop(pkv_resident_t resident);
+int pkv_resident_times(pkv_resident_t resident, uint64_t *stamps_ns, int32_t capacity, int32_t *count);
+void pkv_resident_destroy(pkv_resident_t resident);
+
 const char *pkv_strerror(int code);
 /* The CUDA error code behind the last PKV_ECUDA on this thread (0 if none). */
 int pkv_last_cuda_error(void);

@@ -26,6 +26,7 @@
 #include <string.h>
 
 #include <algorithm>
+#include <chrono>
 #include <deque>
 #include <mutex>
 #include <new>
@@ -568,10 +569,12 @@ struct DevicePlan {
     int32_t max_splits;
 };
 
-int enqueue_decode(pkv_plan_t p, const void* q, const void* k_pages, const void* v_pages,
+// Everything a decode launch needs, checked: the pending plan upload is
+// enqueued on `s`, the TMA maps follow the pools, and `a` / `grid` /
+// `need_merge` describe the launch (over the device-built plan `dp` if given).
+int prepare_decode(pkv_plan_t p, const void* q, const void* k_pages, const void* v_pages,
                    const int32_t* block_table_d, const int32_t* seq_lens_d, float* out, float* lse, cudaStream_t s,
-                   const DevicePlan* dp) {
-    if (p->g.batch == 0) return PKV_OK;
+                   const DevicePlan* dp, pkv::AttnParams* a_out, int* grid_out, bool* need_merge_out) {
     if (!q || !k_pages || !v_pages || !block_table_d || !seq_lens_d || !out || !lse) return PKV_EINVAL;
     if (!aligned16(q) || !aligned16(k_pages) || !aligned16(v_pages) || !aligned16(out) ||
         (reinterpret_cast<uintptr_t>(lse) & 3u) || (reinterpret_cast<uintptr_t>(block_table_d) & 3u) ||
@@ -654,6 +657,21 @@ int enqueue_decode(pkv_plan_t p, const void* q, const void* k_pages, const void*
         grid = p->num_sms * std::max(1, p->ctas_per_sm);
         need_merge = false;
     }
+    *a_out = a;
+    *grid_out = grid;
+    *need_merge_out = need_merge;
+    return PKV_OK;
+}
+
+int enqueue_decode(pkv_plan_t p, const void* q, const void* k_pages, const void* v_pages,
+                   const int32_t* block_table_d, const int32_t* seq_lens_d, float* out, float* lse, cudaStream_t s,
+                   const DevicePlan* dp) {
+    if (p->g.batch == 0) return PKV_OK;
+    pkv::AttnParams a{};
+    int grid = 0;
+    bool need_merge = false;
+    int rc = prepare_decode(p, q, k_pages, v_pages, block_table_d, seq_lens_d, out, lse, s, dp, &a, &grid, &need_merge);
+    if (rc) return rc;
 
     if (p->profile) {
         for (auto& ev : p->ev)
@@ -864,6 +882,26 @@ struct pkv_session_s {
     int32_t queue_cap = 0;
     int32_t chunk = 0;
     int32_t max_splits = 0;
+    pkv_resident_s* resident = nullptr;   // a resident kernel owns the session's device state
+};
+
+struct pkv_resident_s {
+    pkv_session_t session = nullptr;
+    cudaStream_t kstream = nullptr;   // the resident kernel (non-blocking)
+    cudaStream_t cstream = nullptr;   // the per-step copies (non-blocking)
+    pkv::ResidentCtl* ctl_h = nullptr;   // mapped pinned control block
+    pkv::ResidentCtl* ctl_d = nullptr;
+    uint32_t* grid_sync = nullptr;
+    uint64_t* times_d = nullptr;
+    int32_t times_cap = 0;
+    void* q_d = nullptr;
+    void* k_new_d = nullptr;
+    void* v_new_d = nullptr;
+    float* out_d = nullptr;
+    float* lse_d = nullptr;
+    size_t q_bytes = 0, new_bytes = 0, out_bytes = 0, lse_bytes = 0;
+    uint32_t step = 0;
+    bool running = false;
 };
 
 namespace {
@@ -962,8 +1000,8 @@ int pkv_session_device_plan(pkv_session_t s, pkv_stream_t stream) {
 }
 
 namespace {
-int session_step_device(pkv_session_t s, const void* k_new, const void* v_new, void* k_pages, void* v_pages,
-                        const void* q, float* out, float* lse, cudaStream_t st) {
+// The device planner's parameters and the decode's view of the device plan.
+void device_plan_views(pkv_session_t s, pkv::DevPlanParams* dp_out, DevicePlan* plan_out) {
     pkv_plan_s* p = s->plan;
     const pkv_geom& g = p->g;
     const int B = g.batch;
@@ -990,18 +1028,27 @@ int session_step_device(pkv_session_t s, const void* k_new, const void* v_new, v
     dp.page_size = p->page_size;
     dp.max_pages = g.max_pages_per_seq;
     dp.chunk = s->chunk;
+    *dp_out = dp;
+    *plan_out = DevicePlan{reinterpret_cast<const pkv_work_item*>(q_items), row_start, row_splits, order, tiles,
+                           s->chunk, s->max_splits};
+}
+
+int session_step_device(pkv_session_t s, const void* k_new, const void* v_new, void* k_pages, void* v_pages,
+                        const void* q, float* out, float* lse, cudaStream_t st) {
+    pkv_plan_s* p = s->plan;
+    pkv::DevPlanParams dp{};
+    DevicePlan plan{};
+    device_plan_views(s, &dp, &plan);
     PKV_CUDA(pkv::launch_plan_step(dp, st));
     int rc = pkv_append(k_new, v_new, k_pages, v_pages, s->table_d, s->lens_d, p, reinterpret_cast<pkv_stream_t>(st));
     if (rc) return rc;
-    const DevicePlan plan{reinterpret_cast<const pkv_work_item*>(q_items), row_start, row_splits, order, tiles,
-                          s->chunk, s->max_splits};
     return enqueue_decode(p, q, k_pages, v_pages, s->table_d, s->lens_d, out, lse, st, &plan);
 }
 }  // namespace
 
 int pkv_session_step(pkv_session_t s, const void* k_new, const void* v_new, void* k_pages, void* v_pages,
                      const void* q, float* out, float* lse, pkv_stream_t stream) {
-    if (!s) return PKV_EINVAL;
+    if (!s || s->resident) return PKV_EINVAL;
     const pkv_geom& g = s->plan->g;
     const int B = g.batch, ps = s->plan->page_size, mp = g.max_pages_per_seq;
     if (B == 0) return PKV_OK;
@@ -1029,7 +1076,7 @@ int pkv_session_step(pkv_session_t s, const void* k_new, const void* v_new, void
 }
 
 int pkv_session_lengths(pkv_session_t s, int32_t* seq_lens_h) {
-    if (!s || !seq_lens_h) return PKV_EINVAL;
+    if (!s || !seq_lens_h || s->resident) return PKV_EINVAL;
     const size_t bytes = sizeof(int32_t) * s->plan->g.batch;
     if (s->device_mode) {   // the device holds the truth; synchronises the device
         PKV_CUDA(cudaDeviceSynchronize());
@@ -1041,7 +1088,7 @@ int pkv_session_lengths(pkv_session_t s, int32_t* seq_lens_h) {
 }
 
 int pkv_session_table(pkv_session_t s, int32_t* block_table_h) {
-    if (!s || !block_table_h) return PKV_EINVAL;
+    if (!s || !block_table_h || s->resident) return PKV_EINVAL;
     const size_t bytes = sizeof(int32_t) * static_cast<size_t>(s->plan->g.batch) * s->plan->g.max_pages_per_seq;
     if (s->device_mode) {
         PKV_CUDA(cudaDeviceSynchronize());
@@ -1054,7 +1101,7 @@ int pkv_session_table(pkv_session_t s, int32_t* block_table_h) {
 
 int pkv_session_device_queue(pkv_session_t s, pkv_work_item* items, int32_t* order, int32_t capacity,
                              int32_t* count) {
-    if (!s || !count) return PKV_EINVAL;
+    if (!s || !count || s->resident) return PKV_EINVAL;
     if (!s->device_mode) return PKV_EINVAL;
     PKV_CUDA(cudaDeviceSynchronize());
     const int32_t* tiles = s->dev_plan + static_cast<size_t>(s->queue_cap) * 6 + 2 * s->plan->g.batch;
@@ -1070,6 +1117,166 @@ int pkv_session_device_queue(pkv_session_t s, pkv_work_item* items, int32_t* ord
     return PKV_OK;
 }
 
-void pkv_session_destroy(pkv_session_t s) { session_free(s); }
+// ------------------------------------------------------------------ resident steps
+
+namespace {
+void resident_free(pkv_resident_s* r) {
+    if (!r) return;
+    cudaFreeHost(r->ctl_h);
+    cudaFree(r->grid_sync);
+    cudaFree(r->times_d);
+    if (r->kstream) cudaStreamDestroy(r->kstream);
+    if (r->cstream) cudaStreamDestroy(r->cstream);
+    delete r;
+}
+
+uint32_t host_load(const uint32_t* p) { return __atomic_load_n(p, __ATOMIC_ACQUIRE); }
+void host_store(uint32_t* p, uint32_t v) { __atomic_store_n(p, v, __ATOMIC_SEQ_CST); }
+}  // namespace
+
+int pkv_resident_start(pkv_session_t s, void* k_pages, void* v_pages, void* q_d, void* k_new_d, void* v_new_d,
+                       float* out_d, float* lse_d, int64_t idle_limit_ns, int32_t times_cap, pkv_resident_t* out) {
+    if (!out) return PKV_EINVAL;
+    *out = nullptr;
+    if (!s || !s->device_mode || s->resident || !k_pages || !v_pages || !q_d || !k_new_d || !v_new_d || !out_d ||
+        !lse_d || idle_limit_ns <= 0 || idle_limit_ns > 60000000000ll || times_cap < 0)
+        return PKV_EINVAL;
+    if (!aligned16(k_new_d) || !aligned16(v_new_d)) return PKV_EINVAL;
+    pkv_plan_s* p = s->plan;
+    const pkv_geom& g = p->g;
+    if (g.batch == 0) return PKV_EINVAL;
+    const int G = g.num_q_heads / g.num_kv_heads;
+    int dev_sms = 0;
+    PKV_CUDA(cudaDeviceGetAttribute(&dev_sms, cudaDevAttrMultiProcessorCount, p->device));
+    const int per_sm = pkv::resident_ctas_per_sm(g.head_dim, G, p->opts.math != PKV_MATH_FMA);
+    if (per_sm <= 0) return PKV_EUNSUPPORTED;
+
+    pkv_resident_s* r = new (std::nothrow) pkv_resident_s;
+    if (!r) return PKV_ENOMEM;
+    r->session = s;
+    r->q_d = q_d;
+    r->k_new_d = k_new_d;
+    r->v_new_d = v_new_d;
+    r->out_d = out_d;
+    r->lse_d = lse_d;
+    r->q_bytes = static_cast<size_t>(g.batch) * g.num_q_heads * g.head_dim * 2;
+    r->new_bytes = static_cast<size_t>(g.batch) * g.num_kv_heads * g.head_dim * 2;
+    r->out_bytes = static_cast<size_t>(g.batch) * g.num_q_heads * g.head_dim * 4;
+    r->lse_bytes = static_cast<size_t>(g.batch) * g.num_q_heads * 4;
+    r->times_cap = times_cap;
+    const size_t times_bytes = sizeof(uint64_t) * 4 * std::max(times_cap, 1);
+    if (cudaStreamCreateWithFlags(&r->kstream, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaStreamCreateWithFlags(&r->cstream, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaHostAlloc(&r->ctl_h, sizeof(pkv::ResidentCtl), cudaHostAllocMapped) != cudaSuccess ||
+        cudaMalloc(&r->grid_sync, sizeof(uint32_t) * pkv::kSyncWords) != cudaSuccess ||
+        cudaMalloc(&r->times_d, times_bytes) != cudaSuccess) {
+        resident_free(r);
+        return PKV_ENOMEM;
+    }
+    memset(r->ctl_h, 0, sizeof(pkv::ResidentCtl));
+    cudaError_t e = cudaHostGetDevicePointer(reinterpret_cast<void**>(&r->ctl_d), r->ctl_h, 0);
+    if (e == cudaSuccess) e = cudaMemset(r->grid_sync, 0, sizeof(uint32_t) * pkv::kSyncWords);
+    if (e == cudaSuccess) e = cudaMemset(r->times_d, 0, times_bytes);
+    // the kernel takes over the session's device state: earlier work on any stream must be done
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) {
+        resident_free(r);
+        return cuda_fail(e);
+    }
+
+    pkv::DevPlanParams dp{};
+    DevicePlan plan{};
+    device_plan_views(s, &dp, &plan);
+    pkv::AttnParams a{};
+    int grid = 0;
+    bool need_merge = false;
+    int rc = prepare_decode(p, q_d, k_pages, v_pages, s->table_d, s->lens_d, out_d, lse_d, r->kstream, &plan, &a, &grid,
+                            &need_merge);
+    if (rc) {
+        resident_free(r);
+        return rc;
+    }
+    pkv::ResidentParams rp{};
+    rp.attn = a;
+    rp.plan = dp;
+    rp.k_new = static_cast<const uint16_t*>(k_new_d);
+    rp.v_new = static_cast<const uint16_t*>(v_new_d);
+    rp.k_pages_w = static_cast<uint16_t*>(k_pages);
+    rp.v_pages_w = static_cast<uint16_t*>(v_pages);
+    rp.lens_w = s->lens_d;
+    rp.ctl = r->ctl_d;
+    rp.grid_sync = r->grid_sync;
+    rp.times = times_cap > 0 ? r->times_d : nullptr;
+    rp.times_cap = std::max(times_cap, 1);
+    rp.idle_limit_ns = static_cast<uint64_t>(idle_limit_ns);
+    e = pkv::launch_resident(rp, p->kmap, p->vmap, dev_sms * per_sm, r->kstream);
+    if (e != cudaSuccess) {
+        resident_free(r);
+        return cuda_fail(e);
+    }
+    r->running = true;
+    s->resident = r;
+    *out = r;
+    return PKV_OK;
+}
+
+int pkv_resident_step(pkv_resident_t r, const void* q_h, const void* k_new_h, const void* v_new_h, float* out_h,
+                      float* lse_h, int64_t wait_limit_ns) {
+    if (!r || !r->running || wait_limit_ns <= 0) return PKV_EINVAL;
+    if (q_h) PKV_CUDA(cudaMemcpyAsync(r->q_d, q_h, r->q_bytes, cudaMemcpyHostToDevice, r->cstream));
+    if (k_new_h) PKV_CUDA(cudaMemcpyAsync(r->k_new_d, k_new_h, r->new_bytes, cudaMemcpyHostToDevice, r->cstream));
+    if (v_new_h) PKV_CUDA(cudaMemcpyAsync(r->v_new_d, v_new_h, r->new_bytes, cudaMemcpyHostToDevice, r->cstream));
+    PKV_CUDA(cudaStreamSynchronize(r->cstream));
+    const uint32_t step = ++r->step;
+    host_store(&r->ctl_h->step, step);
+    const auto t0 = std::chrono::steady_clock::now();
+    while (host_load(&r->ctl_h->done) < step) {
+        if (host_load(&r->ctl_h->exited)) return PKV_EDEVICE;   // the kernel left its loop (see pkv_status)
+        if (std::chrono::steady_clock::now() - t0 > std::chrono::nanoseconds(wait_limit_ns)) return PKV_EDEVICE;
+    }
+    if (out_h) PKV_CUDA(cudaMemcpyAsync(out_h, r->out_d, r->out_bytes, cudaMemcpyDeviceToHost, r->cstream));
+    if (lse_h) PKV_CUDA(cudaMemcpyAsync(lse_h, r->lse_d, r->lse_bytes, cudaMemcpyDeviceToHost, r->cstream));
+    if (out_h || lse_h) PKV_CUDA(cudaStreamSynchronize(r->cstream));
+    return PKV_OK;
+}
+
+int pkv_resident_stop(pkv_resident_t r) {
+    if (!r) return PKV_EINVAL;
+    if (!r->running) return PKV_OK;
+    host_store(&r->ctl_h->stop, 1u);
+    cudaError_t e = cudaStreamSynchronize(r->kstream);
+    r->running = false;
+    r->session->resident = nullptr;
+    // the persistent route expects its queue counters rewound
+    if (e == cudaSuccess) e = cudaMemset(r->session->plan->ctr, 0, 2 * sizeof(uint32_t));
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return cuda_fail(e);
+    return host_load(&r->ctl_h->exited) == 2u ? PKV_EDEVICE : PKV_OK;
+}
+
+int pkv_resident_times(pkv_resident_t r, uint64_t* stamps_ns, int32_t capacity, int32_t* count) {
+    if (!r || !count || r->running) return PKV_EINVAL;
+    const int32_t n = static_cast<int32_t>(std::min<uint32_t>(r->step, static_cast<uint32_t>(r->times_cap)));
+    *count = n;
+    if (stamps_ns && capacity > 0 && n > 0)
+        PKV_CUDA(cudaMemcpy(stamps_ns, r->times_d, sizeof(uint64_t) * 4 * std::min(n, capacity),
+                            cudaMemcpyDeviceToHost));
+    return PKV_OK;
+}
+
+void pkv_resident_destroy(pkv_resident_t r) {
+    if (!r) return;
+    if (r->running) pkv_resident_stop(r);
+    resident_free(r);
+}
+
+void pkv_session_destroy(pkv_session_t s) {
+    if (s && s->resident) {   // stop the kernel; the resident handle stays the caller's to destroy
+        pkv_resident_s* r = s->resident;
+        pkv_resident_stop(r);
+        r->session = nullptr;
+    }
+    session_free(s);
+}
 
 }  // extern "C"

@@ -51,6 +51,7 @@
 #include <math.h>
 #include <stdint.h>
 
+#include "pkv_devplan.cuh"
 #include "pkv_internal.h"
 
 namespace pkv {
@@ -199,6 +200,28 @@ __device__ __forceinline__ int32_t ld_volatile_i32(const int32_t* p) {
     return v;
 }
 
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ uint32_t ld_acquire_sys(const uint32_t* p) {
+    uint32_t v;
+    asm volatile("ld.acquire.sys.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_release_gpu(uint32_t* p, uint32_t v) {
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ void st_release_sys(uint32_t* p, uint32_t v) {
+    asm volatile("st.release.sys.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ void fence_sc_sys() { asm volatile("fence.sc.sys;" ::: "memory"); }
+
 // Release / acquire fence at GPU scope (message passing between CTAs).
 __device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
 
@@ -327,6 +350,8 @@ struct Smem {
     uint64_t empty[kStages];
     int tile_slot[2];
     int tile_fin, tile_splits;  // the finished tile's finalize flag and split count
+    int sync_ok;                // resident kernel: the last grid barrier / host wait succeeded
+    int append_page, append_pos;
 };
 
 template <int D, int G>
@@ -1373,6 +1398,231 @@ __global__ void __launch_bounds__(kThreads, MMA ? 2 : 1) attention_kernel(const 
     if (threadIdx.x == 0 && sm.abort) drain_after_abort<D, G>(sm, &p.ctr->status);
 }
 
+// ------------------------------------------------------------------ resident steps
+//
+// One cooperative launch that stays resident across continuous-decoding steps,
+// as the persistent worker of "GPUOS" (arXiv 2604.17861, section 4.1) and the
+// resident beat of "WPK persistent kernel" (dotwave.ai) do.  Per step:
+//   CTA 0 waits (bounded) for the host to publish the step in the mapped
+//   control block, then allocates pages and builds the plan (the device
+//   planner of pkv_devplan.cuh) -- grid barrier -- every CTA appends the new
+//   tokens of its rows -- grid barrier -- the CTAs drain the step's queue as
+//   the persistent route does (fused last-arriver merge) -- grid barrier --
+//   CTA 0 publishes the step's outputs to the host (system-scope release).
+// Every wait is bounded: the host wait by idle_limit_ns, a grid barrier by
+// kWaitLimitNs; on expiry the status word gets PKV_DEV_TIMEOUT, the abort word
+// is raised and every CTA leaves the loop at its next barrier.
+
+enum ResidentCmd : uint32_t { kCmdGo = 1, kCmdStop = 2, kCmdFail = 3 };
+
+// Grid barrier of a cooperative launch (all CTAs resident).  Returns false if
+// the barrier was aborted or ran out of time.
+template <int D, int G>
+__device__ bool grid_barrier(Smem<D, G>& sm, uint32_t* gs, uint32_t* status, uint64_t limit_ns = kWaitLimitNs) {
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        int ok = 1;
+        if (*reinterpret_cast<volatile uint32_t*>(gs + kSyncAbort)) {
+            ok = 0;
+        } else {
+            const uint32_t gen = ld_acquire_gpu(gs + kSyncGen);
+            fence_acq_rel_gpu();   // this CTA's writes before its arrival
+            if (atomicAdd(gs + kSyncCount, 1u) == gridDim.x - 1) {
+                gs[kSyncCount] = 0;
+                st_release_gpu(gs + kSyncGen, gen + 1);
+            } else {
+                const uint64_t t0 = globaltimer_ns();
+                while (ld_acquire_gpu(gs + kSyncGen) == gen) {
+                    if (*reinterpret_cast<volatile uint32_t*>(gs + kSyncAbort)) {
+                        ok = 0;
+                        break;
+                    }
+                    if (globaltimer_ns() - t0 > limit_ns) {
+                        atomicOr(status, static_cast<uint32_t>(PKV_DEV_TIMEOUT));
+                        atomicExch(gs + kSyncAbort, 1u);
+                        ok = 0;
+                        break;
+                    }
+                    __nanosleep(64);
+                }
+            }
+        }
+        sm.sync_ok = ok;
+    }
+    __syncthreads();
+    return sm.sync_ok != 0;
+}
+
+// CTA 0, thread 0: wait for the host to publish `step` (or to stop).
+__device__ uint32_t wait_host_step(const ResidentCtl* ctl, uint32_t step, uint64_t limit_ns, uint32_t* status) {
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+        if (ld_acquire_sys(&ctl->step) >= step) return kCmdGo;
+        if (ld_acquire_sys(&ctl->stop)) return kCmdStop;
+        if (globaltimer_ns() - t0 > limit_ns) {
+            atomicOr(status, static_cast<uint32_t>(PKV_DEV_TIMEOUT));
+            return kCmdFail;
+        }
+        __nanosleep(200);
+    }
+}
+
+template <int D, int G, bool MMA>
+__global__ void __launch_bounds__(kThreads, MMA ? 2 : 1) resident_kernel(const ResidentParams rp,
+                                                                         const __grid_constant__ CUtensorMap kmap,
+                                                                         const __grid_constant__ CUtensorMap vmap) {
+    extern __shared__ uint8_t smem_raw[];
+    Smem<D, G>& sm =
+        *reinterpret_cast<Smem<D, G>*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const AttnParams& p = rp.attn;
+    uint32_t* status = &p.ctr->status;
+    uint32_t* gs = rp.grid_sync;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < Cfg<D, G>::kStages; ++s) {
+            mbar_init(&sm.full[s], p.copy_lsu ? 33 : 1);
+            mbar_init(&sm.empty[s], 1);
+            sm.issued[s] = 0;
+        }
+        sm.abort = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    uint32_t pipe = 0;
+    bool failed = false;
+    for (uint32_t step = 1;; ++step) {
+        // ---- 1. CTA 0: the host's step, then allocation and plan
+        if (blockIdx.x == 0) {
+            if (threadIdx.x == 0) {
+                const uint32_t cmd = wait_host_step(rp.ctl, step, rp.idle_limit_ns, status);
+                if (cmd == kCmdGo) {
+                    p.ctr->next_tile = 0;
+                    if (rp.times) rp.times[4 * ((step - 1) % rp.times_cap)] = globaltimer_ns();
+                }
+                if (cmd == kCmdFail) atomicExch(gs + kSyncAbort, 1u);
+                gs[kSyncCmd] = cmd;
+                sm.tile_slot[0] = static_cast<int>(cmd);
+            }
+            __syncthreads();
+            if (sm.tile_slot[0] == kCmdGo) {
+                int* scratch = reinterpret_cast<int*>(&sm.k[0][0]);   // the idle ring
+                devplan::plan_step<kThreads>(rp.plan, scratch, scratch + kDevPlanMaxRows,
+                                             scratch + 2 * kDevPlanMaxRows);
+                fence_proxy_async_shared();   // generic writes to the ring before later TMA writes
+            }
+        }
+        // (CTA 0 may wait up to idle_limit_ns for the host before it arrives)
+        if (!grid_barrier<D, G>(sm, gs, status, rp.idle_limit_ns + kWaitLimitNs)) {
+            failed = true;
+            break;
+        }
+        if (*reinterpret_cast<volatile uint32_t*>(gs + kSyncCmd) != kCmdGo) break;
+        if (blockIdx.x == 0 && threadIdx.x == 0 && rp.times) rp.times[4 * ((step - 1) % rp.times_cap) + 1] = globaltimer_ns();
+
+        // ---- 2. append: every CTA takes rows blockIdx.x, blockIdx.x + gridDim.x, ...
+        for (int b = blockIdx.x; b < p.B; b += gridDim.x) {
+            if (threadIdx.x == 0) {
+                const int pos = rp.lens_w[b];
+                int page = -1;
+                if (pos < 0 || pos / p.page_size >= p.max_pages) {
+                    atomicOr(status, static_cast<uint32_t>(PKV_DEV_ROW_FULL));
+                } else {
+                    page = p.block_table[static_cast<size_t>(b) * p.max_pages + pos / p.page_size];
+                    if (page < 0 || page >= p.num_pages) {
+                        atomicOr(status, static_cast<uint32_t>(PKV_DEV_PAGE_OOB));
+                        page = -1;
+                    }
+                }
+                sm.append_page = page;
+                sm.append_pos = pos;
+            }
+            __syncthreads();
+            if (sm.append_page >= 0) {
+                const int row = p.Hkv * D;
+                const size_t dst = (static_cast<size_t>(sm.append_page) * p.page_size + sm.append_pos % p.page_size) * row;
+                const size_t src = static_cast<size_t>(b) * row;
+                for (int c = threadIdx.x * 8; c < row; c += kThreads * 8) {
+                    *reinterpret_cast<uint4*>(rp.k_pages_w + dst + c) = *reinterpret_cast<const uint4*>(rp.k_new + src + c);
+                    *reinterpret_cast<uint4*>(rp.v_pages_w + dst + c) = *reinterpret_cast<const uint4*>(rp.v_new + src + c);
+                }
+                if (threadIdx.x == 0) rp.lens_w[b] = sm.append_pos + 1;
+            }
+            __syncthreads();
+        }
+        if (!grid_barrier<D, G>(sm, gs, status)) {
+            failed = true;
+            break;
+        }
+
+        // ---- 3. decode: drain the step's queue (the persistent route)
+        if (blockIdx.x == 0 && threadIdx.x == 0 && rp.times) rp.times[4 * ((step - 1) % rp.times_cap) + 2] = globaltimer_ns();
+        const int num_tiles = *p.tiles_d;
+        while (true) {
+            if (threadIdx.x == 0) sm.tile_slot[0] = static_cast<int>(atomicAdd(&p.ctr->next_tile, 1u));
+            __syncthreads();
+            const int t = sm.tile_slot[0];
+            if (t >= num_tiles) break;
+            const TileWork tw = tile_from_item(p, p.queue[p.order[t]]);
+            run_tile<D, G, MMA>(sm, p, tw, pipe, &kmap, &vmap);
+            pipe += stream_blocks(tw);
+            __syncthreads();
+            if (!sm.tile_fin && p.fused_merge) merge_if_last<D, G>(sm, p, tw.b, tw.kvh, sm.tile_splits);
+            __syncthreads();
+        }
+        for (int b = blockIdx.x; b < p.B; b += gridDim.x)
+            if (p.row_splits[b] == 0) write_neutral_row(p, b, threadIdx.x, blockDim.x);
+        if (sm.abort) atomicExch(gs + kSyncAbort, 1u);   // a bounded wait of this CTA ran out
+        if (!grid_barrier<D, G>(sm, gs, status)) {
+            failed = true;
+            break;
+        }
+
+        // ---- 4. CTA 0: the step's outputs are written; tell the host
+        if (blockIdx.x == 0 && threadIdx.x == 0) {
+            if (rp.times) rp.times[4 * ((step - 1) % rp.times_cap) + 3] = globaltimer_ns();
+            fence_sc_sys();
+            st_release_sys(&rp.ctl->done, step);
+        }
+    }
+    if (threadIdx.x == 0 && sm.abort) drain_after_abort<D, G>(sm, status);
+    if (blockIdx.x == 0 && threadIdx.x == 0) {
+        fence_sc_sys();
+        st_release_sys(&rp.ctl->exited, failed ? 2u : 1u);
+    }
+}
+
+template <int D, int G, bool MMA>
+cudaError_t launch_resident_t(const ResidentParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap, int grid,
+                              cudaStream_t stream) {
+    constexpr size_t smem = smem_bytes<D, G>();
+    static_assert(Cfg<D, G>::kStages * Cfg<D, G>::kMatBytes >= (2 * kDevPlanMaxRows + 32) * 4, "planner scratch");
+    cudaError_t e = cudaFuncSetAttribute(resident_kernel<D, G, MMA>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;   // the grid barriers need every CTA resident
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, resident_kernel<D, G, MMA>, p, kmap, vmap);
+}
+
+template <int D, int G, bool MMA>
+int resident_ctas_per_sm_t() {
+    constexpr size_t smem = smem_bytes<D, G>();
+    if (cudaFuncSetAttribute(resident_kernel<D, G, MMA>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem)) != cudaSuccess)
+        return 0;
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, resident_kernel<D, G, MMA>, kThreads, smem) != cudaSuccess)
+        return 0;
+    return n;
+}
+
 template <int D, int G>
 __global__ void __launch_bounds__(128) merge_kernel(const AttnParams p) {
     __shared__ float wsm[kMergeCapFloats];
@@ -1500,6 +1750,20 @@ cudaError_t launch_attention(const AttnParams& p, const CUtensorMap& kmap, const
                  return p.use_mma ? launch_attention_t<kD, kG, true>(p, kmap, vmap, grid, stream, cooperative)
                                   : launch_attention_t<kD, kG, false>(p, kmap, vmap, grid, stream, cooperative));
     return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_resident(const ResidentParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap, int grid,
+                            cudaStream_t stream) {
+    const int G = p.attn.Hq / p.attn.Hkv;
+    PKV_DISPATCH(p.attn.D, G,
+                 return p.attn.use_mma ? launch_resident_t<kD, kG, true>(p, kmap, vmap, grid, stream)
+                                       : launch_resident_t<kD, kG, false>(p, kmap, vmap, grid, stream));
+    return cudaErrorInvalidValue;
+}
+
+int resident_ctas_per_sm(int D, int G, bool mma) {
+    PKV_DISPATCH(D, G, return mma ? resident_ctas_per_sm_t<kD, kG, true>() : resident_ctas_per_sm_t<kD, kG, false>());
+    return 0;
 }
 
 cudaError_t launch_merge(const AttnParams& p, cudaStream_t stream) {

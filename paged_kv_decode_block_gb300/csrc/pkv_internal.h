@@ -100,6 +100,35 @@ cudaError_t launch_append(const uint16_t* k_new, const uint16_t* v_new, uint16_t
 // Bounded-wait self-test (see pkv_selftest_wait): result[3] = {wait returned true,
 // abort flag raised, second wait returned true}.
 cudaError_t launch_wait_selftest(uint32_t* status, uint64_t limit_ns, int* result, cudaStream_t stream);
+
+// Resident continuous decoding (pkv_resident_*): one cooperative launch that
+// stays on the GPU and runs a step (plan, append, decode) each time the host
+// publishes one.  The control block lives in mapped pinned host memory.
+struct ResidentCtl {
+    uint32_t step;     // host: the last step it has published (1, 2, ...)
+    uint32_t stop;     // host: 1 = leave the loop instead of waiting for another step
+    uint32_t done;     // kernel: the last step whose outputs are written
+    uint32_t exited;   // kernel: 1 once it has left the loop; 2 if it left on an error
+};
+// grid_sync words (device memory, zero before the launch)
+enum ResidentSync { kSyncCount = 0, kSyncGen = 1, kSyncCmd = 2, kSyncAbort = 3, kSyncWords = 4 };
+struct ResidentParams {
+    AttnParams attn;            // persistent route over the device plan below
+    DevPlanParams plan;         // allocation + plan of each step (lengths before its append)
+    const uint16_t* k_new;      // device bf16 [B][Hkv][D]: the step's new token per row
+    const uint16_t* v_new;
+    uint16_t* k_pages_w;        // the pools and lengths, writable (the append)
+    uint16_t* v_pages_w;
+    int32_t* lens_w;
+    ResidentCtl* ctl;           // device view of the mapped control block
+    uint32_t* grid_sync;        // [kSyncWords]
+    uint64_t* times;            // [times_cap][4] globaltimer of a step: seen, planned, appended, published
+    int32_t times_cap;
+    uint64_t idle_limit_ns;     // longest wait for the host's next step
+};
+cudaError_t launch_resident(const ResidentParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap, int grid,
+                            cudaStream_t stream);
+int resident_ctas_per_sm(int D, int G, bool mma);
 // Resident CTAs per SM of the attention kernel for this (D, G); 0 if unsupported.
 int attention_ctas_per_sm(int D, int G, bool mma);
 bool shape_supported(int D, int G);

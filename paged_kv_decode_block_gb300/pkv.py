@@ -95,6 +95,11 @@ SIGNATURES = {
     "pkv_session_device_plan": (ctypes.c_int, [_P, _P]),
     "pkv_session_device_queue": (ctypes.c_int, [_P, ctypes.POINTER(WorkItem), _I32P, _I32, _I32P]),
     "pkv_selftest_wait": (ctypes.c_int, [_I64, _U32P, _I32P]),
+    "pkv_resident_start": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, _P, _I64, _I32, ctypes.POINTER(ctypes.c_void_p)]),
+    "pkv_resident_step": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _I64]),
+    "pkv_resident_stop": (ctypes.c_int, [_P]),
+    "pkv_resident_times": (ctypes.c_int, [_P, ctypes.POINTER(ctypes.c_uint64), _I32, _I32P]),
+    "pkv_resident_destroy": (None, [_P]),
     "pkv_strerror": (ctypes.c_char_p, [ctypes.c_int]),
     "pkv_last_cuda_error": (ctypes.c_int, []),
 }
@@ -418,6 +423,70 @@ class Session:
     def close(self):
         if getattr(self, "_h", None) is not None and _lib is not None:
             _lib.pkv_session_destroy(self._h)
+        self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def _host_ptr(t, what):
+    """Address of a contiguous host buffer (torch CPU tensor or numpy array), or None."""
+    if t is None:
+        return None
+    if isinstance(t, np.ndarray):
+        if not t.flags["C_CONTIGUOUS"]:
+            raise ValueError(f"{what}: host array must be contiguous")
+        return ctypes.c_void_p(t.ctypes.data)
+    if t.is_cuda or not t.is_contiguous():
+        raise ValueError(f"{what}: must be a contiguous host tensor")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+class Resident:
+    """Resident steps (pkv_resident_*): one cooperative kernel stays on the GPU and
+    runs a continuous-decoding step (plan, append, decode) each time step() is
+    called.  The session must be in device-plan mode; the device tensors are bound
+    for the kernel's life."""
+
+    def __init__(self, session: "Session", k_pages, v_pages, q, k_new, v_new, out, lse,
+                 idle_limit_ns: int = 2_000_000_000, times_cap: int = 4096):
+        import torch
+        bf = _bf16_types()
+        self._keep = (session, k_pages, v_pages, q, k_new, v_new, out, lse)
+        h = ctypes.c_void_p()
+        _check(load().pkv_resident_start(session._h, _dev_ptr(k_pages, "k_pages", bf), _dev_ptr(v_pages, "v_pages", bf),
+                                         _dev_ptr(q, "q", bf), _dev_ptr(k_new, "k_new", bf),
+                                         _dev_ptr(v_new, "v_new", bf), _dev_ptr(out, "out", (torch.float32,)),
+                                         _dev_ptr(lse, "lse", (torch.float32,)), int(idle_limit_ns), int(times_cap),
+                                         ctypes.byref(h)), "pkv_resident_start")
+        self._h = h
+
+    def step(self, q_h=None, k_new_h=None, v_new_h=None, out_h=None, lse_h=None,
+             wait_limit_ns: int = 5_000_000_000):
+        """One step: host inputs (None keeps the bound device buffer) in, outputs to the
+        host buffers given."""
+        _check(load().pkv_resident_step(self._h, _host_ptr(q_h, "q_h"), _host_ptr(k_new_h, "k_new_h"),
+                                        _host_ptr(v_new_h, "v_new_h"), _host_ptr(out_h, "out_h"),
+                                        _host_ptr(lse_h, "lse_h"), int(wait_limit_ns)), "pkv_resident_step")
+
+    def stop(self):
+        _check(load().pkv_resident_stop(self._h), "pkv_resident_stop")
+
+    def times(self) -> np.ndarray:
+        """[steps][4] globaltimer ns of each step (after stop): seen, planned, appended,
+        published."""
+        n = ctypes.c_int32(0)
+        _check(load().pkv_resident_times(self._h, None, 0, ctypes.byref(n)), "pkv_resident_times")
+        buf = (ctypes.c_uint64 * max(4 * n.value, 1))()
+        _check(load().pkv_resident_times(self._h, buf, n.value, ctypes.byref(n)), "pkv_resident_times")
+        return np.ctypeslib.as_array(buf)[: 4 * n.value].reshape(-1, 4).copy()
+
+    def close(self):
+        if getattr(self, "_h", None) is not None and _lib is not None:
+            _lib.pkv_resident_destroy(self._h)
         self._h = None
 
     def __del__(self):
