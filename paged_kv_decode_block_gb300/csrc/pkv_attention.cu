@@ -21,12 +21,19 @@
 //   * the producers resolve the block table (32 entries per coalesced load,
 //     prefetched one batch ahead) and stream 16-token blocks of K and V into
 //     a ring of 10-16 shared-memory stages (about 80-96 KB per CTA, two CTAs
-//     per SM) with TMA (cp.async.bulk.tensor, 128-byte swizzle, L2
-//     evict-first), completion tracked by mbarriers;
+//     per SM), in a 128-byte-swizzled layout with L2 evict-first: 16-byte
+//     cp.async from all producer lanes (default) or TMA boxes
+//     (cp.async.bulk.tensor); completion tracked by mbarriers;
+//   * the launch may overlap the previous kernel's tail (programmatic
+//     dependent launch): nothing is read before the grid dependency wait
+//     except the host-staged queue entry, and the tile's first blocks are
+//     warmed in L2 there;
 //   * each consumer warp owns every 4th block and keeps a private
 //     online-softmax state (running max, sum, fp32 accumulator), so the loop has
 //     no CTA-wide barrier; the four states are merged with the exact LSE rule at
-//     the end of the tile;
+//     the end of the tile, and a split tile's partial goes to the workspace
+//     where the last-arriving split of its (row, KV head) merges them all (or,
+//     in a cooperative launch, every split merges a share);
 //   * two interchangeable block reductions (template MMA):
 //       - FMA: CUDA cores; D/8 lanes cover a K row in 16-byte slices and the G
 //         dot products are summed by a transposing butterfly;
