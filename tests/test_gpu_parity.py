@@ -197,6 +197,33 @@ def test_deterministic_across_runs():
         assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1]), route
 
 
+def test_back_to_back_launches_of_different_plans():
+    """Decodes of different plans queued back to back on one stream, with no host
+    synchronisation between them: each launch may start while the previous one
+    finishes (programmatic dependent launch), reads its own host-staged queue
+    entry early, and everything else only after the dependency wait; the clones
+    between the decodes read what the previous decode wrote."""
+    pa = wl.make_problem("b2b_a", [700, 33, 1500], Hq=16, Hkv=4, D=128, page_size=16, num_pages=200, seed=31)
+    pb = wl.mixed()
+    da, db = to_device(pa), to_device(pb)
+    plans = [make_plan(pa, force_mode="split_queue", num_splits=8), make_plan(pb),
+             make_plan(pa, force_mode="persistent", num_splits=3)]
+    stream = torch.cuda.Stream()
+    with torch.cuda.stream(stream):
+        pkv.decode(da["q"], da["k"], da["v"], da["table"], da["lens"], plans[0], da["out"], da["lse"], stream=stream)
+        out0 = da["out"].clone()
+        pkv.decode(db["q"], db["k"], db["v"], db["table"], db["lens"], plans[1], db["out"], db["lse"], stream=stream)
+        out1, lse1 = db["out"].clone(), db["lse"].clone()
+        pkv.decode(da["q"], da["k"], da["v"], da["table"], da["lens"], plans[2], da["out"], da["lse"], stream=stream)
+    stream.synchronize()
+    ref_a, ref_b = oracle_result(pa), oracle_result(pb)
+    assert np.max(np.abs(out0.cpu().numpy() - ref_a[0])) <= 2e-3
+    assert_close(out1.cpu().numpy(), lse1.cpu().numpy(), *ref_b, what="second of three")
+    assert_close(da["out"].cpu().numpy(), da["lse"].cpu().numpy(), *ref_a, what="third of three")
+    for plan in plans:
+        assert plan.status() == 0
+
+
 def test_bad_page_id_flags_status_and_poisons():
     """A table entry outside the pool (the planner is not shown the table) is caught in
     the kernel: status bit set, output NaN, no access through the bad id."""

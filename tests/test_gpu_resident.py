@@ -53,8 +53,9 @@ def _case(case, steps):
     return _ragged_problem(steps), 4
 
 
-@pytest.mark.parametrize("case", ["continuous_one_split", "ragged_four_splits"])
-def test_resident_steps_match_oracle_and_launched_steps(case):
+@pytest.mark.parametrize("case,math", [("continuous_one_split", "mma"), ("ragged_four_splits", "mma"),
+                                       ("ragged_four_splits", "fma")])
+def test_resident_steps_match_oracle_and_launched_steps(case, math):
     steps = 40
     check = (0, 17, steps - 1)
     p, splits = _case(case, steps)
@@ -62,7 +63,7 @@ def test_resident_steps_match_oracle_and_launched_steps(case):
     toks = [wl.new_tokens(rng, p.B, p.Hkv, p.D) for _ in range(steps)]
 
     # the same steps as separate launches
-    eager = ContinuousSessions(p, force_mode="persistent", num_splits=splits)
+    eager = ContinuousSessions(p, force_mode="persistent", num_splits=splits, math=math)
     eager.session.device_plan()
     eager_out = {}
     for step, (kn, vn) in enumerate(toks):
@@ -72,7 +73,7 @@ def test_resident_steps_match_oracle_and_launched_steps(case):
     del eager
     torch.cuda.empty_cache()
 
-    sess = ContinuousSessions(p, force_mode="persistent", num_splits=splits)
+    sess = ContinuousSessions(p, force_mode="persistent", num_splits=splits, math=math)
     sess.session.device_plan()
     kbuf = torch.empty((p.B, p.Hkv, p.D), dtype=torch.int16, device="cuda")
     vbuf = torch.empty_like(kbuf)
