@@ -353,8 +353,9 @@ def run_pkv(args):
     peak, peak_src = hbm_peak()
     achieved = alg_bytes_attn / (attn_ms * 1e-3) / 1e9
 
-    # end to end through the public API with host buffers: q H2D (pinned), host re-plan
-    # and queue upload, decode, out + lse D2H; wall time per step
+    # end to end through the C ABI with host buffers: host re-plan and queue upload,
+    # q host -> device, decode, out + lse device -> host (pkv_decode_host, which
+    # synchronises); wall time per step, each step cold (L2 flushed before it)
     q_host = torch.from_numpy(p.q.view(np.int16)).pin_memory()
     out_host = torch.empty(out.shape, dtype=torch.float32).pin_memory()
     lse_host = torch.empty(lse.shape, dtype=torch.float32).pin_memory()
@@ -363,15 +364,13 @@ def run_pkv(args):
         flush.zero_()
         torch.cuda.synchronize()
         t0 = time.perf_counter()
-        q.copy_(q_host, non_blocking=True)
         plan.update(p.seq_lens)
-        pkv.decode(q, k, v, table, lens, plan, out, lse)
-        out_host.copy_(out, non_blocking=True)
-        lse_host.copy_(lse, non_blocking=True)
-        torch.cuda.synchronize()
+        pkv.decode_host(q_host, k, v, table, lens, plan, out_host, lse_host)
         if i >= args.warmup:
             e2e_s.append(time.perf_counter() - t0)
     e2e_med = statistics.median(e2e_s)
+    if not (np.array_equal(out_host.numpy(), out.cpu().numpy()) and np.array_equal(lse_host.numpy(), lse.cpu().numpy())):
+        raise SystemExit("the host-buffer path disagrees with the device path")
     upload = 4 * (5 * info["num_work_items"] + 2 * p.B) if info["mode"] != pkv.MODE_DIRECT else 0
     e2e_med = reduce_max([e2e_med], dist, dev)[0]
 

@@ -223,6 +223,15 @@ int pkv_decode(const void *q, const void *k_pages, const void *v_pages,
                float *out, float *lse, pkv_stream_t stream);
 
 /*
+ * pkv_decode with host buffers: copies q_h (bf16 [B][Hq][D]) to device
+ * staging owned by the plan, decodes, copies out / lse back to out_h / lse_h
+ * (fp32) and synchronises `stream`.  Pinned host buffers keep the copies
+ * asynchronous.  The other arguments and errors are those of pkv_decode.
+ */
+int pkv_decode_host(const void *q_h, const void *k_pages, const void *v_pages, const int32_t *block_table_d,
+                    const int32_t *seq_lens_d, pkv_plan_t plan, float *out_h, float *lse_h, pkv_stream_t stream);
+
+/*
  * Append one new token per row: for every row b and KV head, write
  * k_new[b][kvh][:] / v_new[b][kvh][:] (device bf16 [B][Hkv][D]) at position
  * seq_lens_d[b] -- page block_table_d[b][pos / page_size], slot

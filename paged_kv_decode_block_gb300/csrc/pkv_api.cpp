@@ -362,6 +362,11 @@ struct pkv_plan_s {
     bool profile = false;
     cudaEvent_t ev[3] = {nullptr, nullptr, nullptr};
     int ev_launches = 0;
+
+    // pkv_decode_host: device staging of q / out / lse (allocated on first use)
+    void* q_stage = nullptr;
+    float* out_stage = nullptr;
+    float* lse_stage = nullptr;
 };
 
 namespace {
@@ -375,6 +380,9 @@ void release(pkv_plan_s* p) {
     cudaFree(p->ws_lse);
     cudaFree(p->arrive);
     cudaFree(p->ctr);
+    cudaFree(p->q_stage);
+    cudaFree(p->out_stage);
+    cudaFree(p->lse_stage);
     if (p->upload_done) cudaEventDestroy(p->upload_done);
     for (auto& e : p->ev)
         if (e) cudaEventDestroy(e);
@@ -710,6 +718,36 @@ int pkv_decode(const void* q, const void* k_pages, const void* v_pages, const in
     if (!p) return PKV_EINVAL;
     return enqueue_decode(p, q, k_pages, v_pages, block_table_d, seq_lens_d, out, lse,
                           reinterpret_cast<cudaStream_t>(stream), nullptr);
+}
+
+int pkv_decode_host(const void* q_h, const void* k_pages, const void* v_pages, const int32_t* block_table_d,
+                    const int32_t* seq_lens_d, pkv_plan_t p, float* out_h, float* lse_h, pkv_stream_t stream) {
+    if (!p) return PKV_EINVAL;
+    if (p->g.batch == 0) return PKV_OK;
+    if (!q_h || !out_h || !lse_h) return PKV_EINVAL;
+    const size_t rows = static_cast<size_t>(p->g.batch) * p->g.num_q_heads;
+    const size_t q_bytes = rows * p->g.head_dim * 2, out_bytes = rows * p->g.head_dim * 4, lse_bytes = rows * 4;
+    if (!p->q_stage) {
+        if (cudaMalloc(&p->q_stage, q_bytes) != cudaSuccess || cudaMalloc(&p->out_stage, out_bytes) != cudaSuccess ||
+            cudaMalloc(&p->lse_stage, lse_bytes) != cudaSuccess) {
+            cudaFree(p->q_stage);
+            cudaFree(p->out_stage);
+            cudaFree(p->lse_stage);
+            p->q_stage = nullptr;
+            p->out_stage = nullptr;
+            p->lse_stage = nullptr;
+            return PKV_ENOMEM;
+        }
+    }
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    PKV_CUDA(cudaMemcpyAsync(p->q_stage, q_h, q_bytes, cudaMemcpyHostToDevice, s));
+    int rc = enqueue_decode(p, p->q_stage, k_pages, v_pages, block_table_d, seq_lens_d, p->out_stage, p->lse_stage, s,
+                            nullptr);
+    if (rc) return rc;
+    PKV_CUDA(cudaMemcpyAsync(out_h, p->out_stage, out_bytes, cudaMemcpyDeviceToHost, s));
+    PKV_CUDA(cudaMemcpyAsync(lse_h, p->lse_stage, lse_bytes, cudaMemcpyDeviceToHost, s));
+    PKV_CUDA(cudaStreamSynchronize(s));
+    return PKV_OK;
 }
 
 int pkv_append(const void* k_new, const void* v_new, void* k_pages, void* v_pages, const int32_t* block_table_d,

@@ -76,6 +76,7 @@ SIGNATURES = {
     "pkv_plan_get_info": (ctypes.c_int, [_P, ctypes.POINTER(PlanInfo)]),
     "pkv_plan_queue": (ctypes.c_int, [_P, ctypes.POINTER(WorkItem), _I32, _I32P]),
     "pkv_decode": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, _P, _P]),
+    "pkv_decode_host": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, _P, _P]),
     "pkv_append": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, _P]),
     "pkv_status": (ctypes.c_int, [_P, _P, _U32P]),
     "pkv_read_workspace": (ctypes.c_int, [_P, _P, _P, _P, _I32, _I32P]),
@@ -297,6 +298,17 @@ def decode(q, k_pages, v_pages, block_table, seq_lens, plan: Plan, out, lse, str
                            _dev_ptr(out, "out", (torch.float32,)), _dev_ptr(lse, "lse", (torch.float32,)),
                            _stream_handle(stream))
     _check(rc, "pkv_decode")
+
+
+def decode_host(q_h, k_pages, v_pages, block_table, seq_lens, plan: Plan, out_h, lse_h, stream=None):
+    """pkv_decode_host: q from host memory, out / lse back to host memory (synchronises)."""
+    import torch
+    bf = _bf16_types()
+    rc = load().pkv_decode_host(_host_ptr(q_h, "q_h"), _dev_ptr(k_pages, "k_pages", bf),
+                                _dev_ptr(v_pages, "v_pages", bf), _dev_ptr(block_table, "block_table", (torch.int32,)),
+                                _dev_ptr(seq_lens, "seq_lens", (torch.int32,)), plan.handle,
+                                _host_ptr(out_h, "out_h"), _host_ptr(lse_h, "lse_h"), _stream_handle(stream))
+    _check(rc, "pkv_decode_host")
 
 
 STATIC_SCRATCH_BYTES = 8 * 1024 * 1024

@@ -224,6 +224,22 @@ def test_back_to_back_launches_of_different_plans():
         assert plan.status() == 0
 
 
+@pytest.mark.parametrize("route", ["split_queue", "direct", "persistent"])
+def test_decode_with_host_buffers(route):
+    """pkv_decode_host: q from host memory, out / lse back to host memory."""
+    p = wl.make_problem("host_bufs", [700, 33, 1500, 0], Hq=16, Hkv=4, D=128, page_size=16, num_pages=200, seed=33)
+    dev = to_device(p)
+    plan = make_plan(p, force_mode=route, num_splits=5)
+    q_h = torch.from_numpy(p.q.view(np.int16)).pin_memory()
+    out_h = torch.empty((p.B, p.Hq, p.D), dtype=torch.float32).pin_memory()
+    lse_h = torch.empty((p.B, p.Hq), dtype=torch.float32).pin_memory()
+    pkv.decode_host(q_h, dev["k"], dev["v"], dev["table"], dev["lens"], plan, out_h, lse_h)
+    assert_close(out_h.numpy(), lse_h.numpy(), *oracle_result(p), what=f"host buffers {route}")
+    out, lse, _, _ = run(p, dev=dev, plan=plan)
+    assert np.array_equal(out, out_h.numpy()) and np.array_equal(lse, lse_h.numpy())
+    assert plan.status() == 0
+
+
 def test_bad_page_id_flags_status_and_poisons():
     """A table entry outside the pool (the planner is not shown the table) is caught in
     the kernel: status bit set, output NaN, no access through the bad id."""
