@@ -816,11 +816,36 @@ __device__ void merge_unit_staged(Smem<D, G>& sm, const AttnParams& p, int b, in
         for (int i = tid; i < vecs; i += kThreads) cp_async16_plain(dst + i * 16, src + static_cast<size_t>(i) * 16);
     };
     issue(0);
+    const int warp = tid / 32, lane = tid % 32;
+    if (ns <= 32) {
+        // One warp per head, one split per lane: the LSEs go straight from L2 to
+        // registers, the max and sum are shuffles, and the normalised weights land
+        // in shared memory while the partials are still arriving.
+        if (tid == 0) sm.merge_nan = 0;
+        __syncthreads();
+        for (int g = warp; g < G; g += kThreads / 32) {
+            const float ls = lane < ns ? __ldcg(p.ws_lse + (base + lane) * G + g) : -INFINITY;
+            const bool nan = __any_sync(kFull, isnan(ls));
+            float M = ls;
+#pragma unroll
+            for (int x = 16; x > 0; x >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, x));
+            const float e = M != -INFINITY && lane < ns ? exp2f(ls - M) : 0.f;
+            float wsum = e;
+#pragma unroll
+            for (int x = 16; x > 0; x >>= 1) wsum += __shfl_xor_sync(kFull, wsum, x);
+            const float inv = M != -INFINITY ? 1.f / wsum : 0.f;
+            if (lane < ns) w[lane * G + g] = e * inv;
+            if (lane == 0) {
+                if (nan) sm.merge_nan = 1;
+                const float lse2 = M != -INFINITY ? M + log2f(wsum) : -INFINITY;
+                p.lse[static_cast<size_t>(b) * p.Hq + kvh * G + g] = nan ? NAN : lse2 * kLn2;
+            }
+        }
+    } else {
     if (tid == 0) sm.merge_nan = 0;
     for (int i = tid; i < ns * G; i += kThreads) w[i] = __ldcg(p.ws_lse + base * G + i);
     __syncthreads();
     // per head: max and sum over the splits, one warp per head
-    const int warp = tid / 32, lane = tid % 32;
     for (int g = warp; g < G; g += kThreads / 32) {
         float M = -INFINITY;
         bool nan = false;
@@ -848,6 +873,7 @@ __device__ void merge_unit_staged(Smem<D, G>& sm, const AttnParams& p, int b, in
     for (int i = tid; i < ns * G; i += kThreads) {
         const int g = i % G;
         w[i] = sm.merge_m[g] != -INFINITY ? exp2f(w[i] - sm.merge_m[g]) * sm.merge_inv[g] : 0.f;
+    }
     }
     float4 acc[kPer];
 #pragma unroll
