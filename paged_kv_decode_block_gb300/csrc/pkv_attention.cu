@@ -348,7 +348,7 @@ struct Smem {
     float m[kConsumerWarps][G];
     float l[kConsumerWarps][G];
     float merge_m[G], merge_inv[G];
-    int merge_nan;
+    int merge_nan_h[G];         // per head: a split's LSE was NaN (written once per merge, no reset)
     int poisoned[kConsumerWarps];
     int bad[kStages];
     uint32_t issued[kStages];   // 1 + use index of the last TMA issued into each stage
@@ -821,8 +821,6 @@ __device__ void merge_unit_staged(Smem<D, G>& sm, const AttnParams& p, int b, in
         // One warp per head, one split per lane: the LSEs go straight from L2 to
         // registers, the max and sum are shuffles, and the normalised weights land
         // in shared memory while the partials are still arriving.
-        if (tid == 0) sm.merge_nan = 0;
-        __syncthreads();
         for (int g = warp; g < G; g += kThreads / 32) {
             const float ls = lane < ns ? __ldcg(p.ws_lse + (base + lane) * G + g) : -INFINITY;
             const bool nan = __any_sync(kFull, isnan(ls));
@@ -836,13 +834,12 @@ __device__ void merge_unit_staged(Smem<D, G>& sm, const AttnParams& p, int b, in
             const float inv = M != -INFINITY ? 1.f / wsum : 0.f;
             if (lane < ns) w[lane * G + g] = e * inv;
             if (lane == 0) {
-                if (nan) sm.merge_nan = 1;
+                sm.merge_nan_h[g] = nan ? 1 : 0;
                 const float lse2 = M != -INFINITY ? M + log2f(wsum) : -INFINITY;
                 p.lse[static_cast<size_t>(b) * p.Hq + kvh * G + g] = nan ? NAN : lse2 * kLn2;
             }
         }
     } else {
-    if (tid == 0) sm.merge_nan = 0;
     for (int i = tid; i < ns * G; i += kThreads) w[i] = __ldcg(p.ws_lse + base * G + i);
     __syncthreads();
     // per head: max and sum over the splits, one warp per head
@@ -864,7 +861,7 @@ __device__ void merge_unit_staged(Smem<D, G>& sm, const AttnParams& p, int b, in
         if (lane == 0) {
             sm.merge_m[g] = M;
             sm.merge_inv[g] = M != -INFINITY ? 1.f / wsum : 0.f;
-            if (nan) sm.merge_nan = 1;
+            sm.merge_nan_h[g] = nan ? 1 : 0;
             const float lse2 = M != -INFINITY ? M + log2f(wsum) : -INFINITY;
             p.lse[static_cast<size_t>(b) * p.Hq + kvh * G + g] = nan ? NAN : lse2 * kLn2;
         }
@@ -905,18 +902,18 @@ __device__ void merge_unit_staged(Smem<D, G>& sm, const AttnParams& p, int b, in
             issue(s0 + chunk);
         }
     }
-    const bool nan = sm.merge_nan != 0;
 #pragma unroll
     for (int r = 0; r < kPer; ++r) {
         const int i = tid + r * kThreads;
         if (i < kOut) {
             const int g = i / (D / 4), d = (i % (D / 4)) * 4;
             *reinterpret_cast<float4*>(p.out + (static_cast<size_t>(b) * p.Hq + kvh * G + g) * D + d) =
-                nan ? make_float4(NAN, NAN, NAN, NAN) : acc[r];
+                sm.merge_nan_h[g] ? make_float4(NAN, NAN, NAN, NAN) : acc[r];
         }
     }
-    fence_proxy_async_shared();   // a later TMA into these stages is ordered after the copies above
-    __syncthreads();
+    // A later TMA into these stages is ordered after the copies above; every
+    // caller that reuses the stages passes a CTA barrier before it does.
+    fence_proxy_async_shared();
 }
 
 // ------------------------------------------------------------------ tile
