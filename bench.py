@@ -353,9 +353,10 @@ def run_pkv(args):
     peak, peak_src = hbm_peak()
     achieved = alg_bytes_attn / (attn_ms * 1e-3) / 1e9
 
-    # end to end through the C ABI with host buffers: host re-plan and queue upload,
-    # q host -> device, decode, out + lse device -> host (pkv_decode_host, which
-    # synchronises); wall time per step, each step cold (L2 flushed before it)
+    # end to end through the C ABI with host buffers: host re-plan, then
+    # pkv_decode_host, which synchronises: the kernel reads the new plan and q in
+    # pinned host memory and writes out + lse there (over NVLink-C2C, no copy
+    # engine); wall time per step, each step cold (L2 flushed before it)
     q_host = torch.from_numpy(p.q.view(np.int16)).pin_memory()
     out_host = torch.empty(out.shape, dtype=torch.float32).pin_memory()
     lse_host = torch.empty(lse.shape, dtype=torch.float32).pin_memory()
@@ -411,7 +412,9 @@ def run_pkv(args):
                      "traffic": profiled_traffic(args.workload)},
         "e2e": {"value": round(kv * world / e2e_med / 1e9, 2), "unit": "GB/s",
                 "us_per_step": round(e2e_med * 1e6, 2), "h2d_bytes_per_step": q_bytes + upload,
-                "d2h_bytes_per_step": o_bytes},
+                "d2h_bytes_per_step": o_bytes,
+                "path": "host re-plan + pkv_decode_host: the kernel reads the plan and q from pinned host "
+                        "memory and writes out/lse to pinned host memory (NVLink-C2C), then a synchronise"},
         "gpu_launches": n_launch * args.steps,
         "cpu_baseline": cpu,
         "clocks": {"sm_mhz": clocks["sm_mhz"], "sm_max_mhz": clocks["sm_max_mhz"],

@@ -223,10 +223,16 @@ int pkv_decode(const void *q, const void *k_pages, const void *v_pages,
                float *out, float *lse, pkv_stream_t stream);
 
 /*
- * pkv_decode with host buffers: copies q_h (bf16 [B][Hq][D]) to device
- * staging owned by the plan, decodes, copies out / lse back to out_h / lse_h
- * (fp32) and synchronises `stream`.  Pinned host buffers keep the copies
- * asynchronous.  The other arguments and errors are those of pkv_decode.
+ * pkv_decode with host buffers: q_h (bf16 [B][Hq][D]) in, out_h / lse_h (fp32)
+ * out; synchronises `stream`.  No copy engine is used: pinned host memory
+ * (cudaMallocHost, cudaHostAlloc, cudaHostRegister) is mapped into the GPU's
+ * address space, and on GB300 the kernel reads q and writes out / lse there
+ * directly, over NVLink-C2C.  A buffer that is pageable (or whose mapped
+ * address is not 16-byte aligned; 4 for lse_h) goes through pinned staging
+ * owned by the plan, with a host memcpy before (q) or after (out, lse) the
+ * decode.  A plan re-planned since its last upload is likewise read in place
+ * from its pinned host copy.  The other arguments and errors are those of
+ * pkv_decode; ENOMEM if the staging cannot be allocated.
  */
 int pkv_decode_host(const void *q_h, const void *k_pages, const void *v_pages, const int32_t *block_table_d,
                     const int32_t *seq_lens_d, pkv_plan_t plan, float *out_h, float *lse_h, pkv_stream_t stream);

@@ -326,6 +326,23 @@ int encode_pool_map(CUtensorMap* map, const void* pool, const pkv_geom& g, int32
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// The address through which the current device reaches host memory `h`, if
+// `h` lies in pinned (page-locked, cudaMallocHost / cudaHostAlloc /
+// cudaHostRegister) memory mapped for this device and that address has the
+// given alignment; nullptr for pageable or unmapped memory.
+const void* mapped_host_address(const void* h, uintptr_t align) {
+    cudaPointerAttributes attr{};
+    if (cudaPointerGetAttributes(&attr, h) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return nullptr;
+    }
+    if (attr.type != cudaMemoryTypeHost || !attr.devicePointer) return nullptr;
+    if (reinterpret_cast<uintptr_t>(attr.devicePointer) & (align - 1)) return nullptr;
+    return attr.devicePointer;
+}
+
 }  // namespace
 
 // ------------------------------------------------------------------ plan object
@@ -363,10 +380,14 @@ struct pkv_plan_s {
     cudaEvent_t ev[3] = {nullptr, nullptr, nullptr};
     int ev_launches = 0;
 
-    // pkv_decode_host: device staging of q / out / lse (allocated on first use)
-    void* q_stage = nullptr;
-    float* out_stage = nullptr;
-    float* lse_stage = nullptr;
+    // Device address of host_buf (pinned memory is mapped into the GPU's
+    // address space), so pkv_decode_host can read a fresh plan in place.
+    const int32_t* host_buf_dev = nullptr;
+
+    // pkv_decode_host: pinned, device-mapped staging [q][out][lse] for host
+    // buffers the GPU cannot address itself (allocated on first need)
+    uint8_t* host_stage = nullptr;
+    uint8_t* host_stage_dev = nullptr;
 };
 
 namespace {
@@ -380,9 +401,7 @@ void release(pkv_plan_s* p) {
     cudaFree(p->ws_lse);
     cudaFree(p->arrive);
     cudaFree(p->ctr);
-    cudaFree(p->q_stage);
-    cudaFree(p->out_stage);
-    cudaFree(p->lse_stage);
+    cudaFreeHost(p->host_stage);
     if (p->upload_done) cudaEventDestroy(p->upload_done);
     for (auto& e : p->ev)
         if (e) cudaEventDestroy(e);
@@ -400,10 +419,16 @@ int stage(pkv_plan_s* p) {
         cudaFreeHost(p->host_buf);
         cudaFree(p->dev_buf);
         p->host_buf = nullptr;
+        p->host_buf_dev = nullptr;
         p->dev_buf = nullptr;
         const size_t bytes = (cap * 6 + 2 * static_cast<size_t>(B)) * sizeof(int32_t);
         if (cudaMallocHost(&p->host_buf, bytes) != cudaSuccess) return PKV_ENOMEM;
         if (cudaMalloc(&p->dev_buf, bytes) != cudaSuccess) return PKV_ENOMEM;
+        void* mapped = nullptr;
+        if (cudaHostGetDevicePointer(&mapped, p->host_buf, 0) == cudaSuccess)
+            p->host_buf_dev = static_cast<const int32_t*>(mapped);
+        else
+            (void)cudaGetLastError();   // not mapped: pkv_decode_host uploads the plan instead
         p->buf_cap_items = cap;
     }
     const size_t slots = static_cast<size_t>(std::max(pl.ws_slots, 1));
@@ -580,9 +605,14 @@ struct DevicePlan {
 // Everything a decode launch needs, checked: the pending plan upload is
 // enqueued on `s`, the TMA maps follow the pools, and `a` / `grid` /
 // `need_merge` describe the launch (over the device-built plan `dp` if given).
+// With `plan_in_place`, a plan not yet uploaded is read by the kernel from its
+// pinned, device-mapped host staging instead (no copy; the upload stays
+// pending for later launches), so the caller must not let the plan change
+// before the launch has finished.
 int prepare_decode(pkv_plan_t p, const void* q, const void* k_pages, const void* v_pages,
                    const int32_t* block_table_d, const int32_t* seq_lens_d, float* out, float* lse, cudaStream_t s,
-                   const DevicePlan* dp, pkv::AttnParams* a_out, int* grid_out, bool* need_merge_out) {
+                   const DevicePlan* dp, pkv::AttnParams* a_out, int* grid_out, bool* need_merge_out,
+                   bool plan_in_place = false) {
     if (!q || !k_pages || !v_pages || !block_table_d || !seq_lens_d || !out || !lse) return PKV_EINVAL;
     if (!aligned16(q) || !aligned16(k_pages) || !aligned16(v_pages) || !aligned16(out) ||
         (reinterpret_cast<uintptr_t>(lse) & 3u) || (reinterpret_cast<uintptr_t>(block_table_d) & 3u) ||
@@ -592,7 +622,10 @@ int prepare_decode(pkv_plan_t p, const void* q, const void* k_pages, const void*
     PKV_CUDA(cudaGetDevice(&dev));
     if (dev != p->device) return PKV_EINVAL;
 
-    if (p->dirty && !dp) {
+    const int32_t* plan_buf = p->dev_buf;
+    if (p->dirty && !dp && plan_in_place && p->host_buf_dev) {
+        plan_buf = p->host_buf_dev;
+    } else if (p->dirty && !dp) {
         PKV_CUDA(cudaMemcpyAsync(p->dev_buf, p->host_buf, p->upload_bytes, cudaMemcpyHostToDevice, s));
         PKV_CUDA(cudaEventRecord(p->upload_done, s));
         p->upload_recorded = true;
@@ -614,8 +647,8 @@ int prepare_decode(pkv_plan_t p, const void* q, const void* k_pages, const void*
     a.q = static_cast<const uint16_t*>(q);
     a.block_table = block_table_d;
     a.seq_lens = seq_lens_d;
-    a.queue = reinterpret_cast<const pkv_work_item*>(p->dev_buf);
-    a.row_start = p->dev_buf + p->buf_cap_items * 5;
+    a.queue = reinterpret_cast<const pkv_work_item*>(plan_buf);
+    a.row_start = plan_buf + p->buf_cap_items * 5;
     a.row_splits = a.row_start + p->g.batch;
     a.order = pl.mode == PKV_MODE_PERSISTENT ? a.row_splits + p->g.batch : nullptr;
     a.tiles_d = nullptr;
@@ -673,12 +706,13 @@ int prepare_decode(pkv_plan_t p, const void* q, const void* k_pages, const void*
 
 int enqueue_decode(pkv_plan_t p, const void* q, const void* k_pages, const void* v_pages,
                    const int32_t* block_table_d, const int32_t* seq_lens_d, float* out, float* lse, cudaStream_t s,
-                   const DevicePlan* dp) {
+                   const DevicePlan* dp, bool plan_in_place = false) {
     if (p->g.batch == 0) return PKV_OK;
     pkv::AttnParams a{};
     int grid = 0;
     bool need_merge = false;
-    int rc = prepare_decode(p, q, k_pages, v_pages, block_table_d, seq_lens_d, out, lse, s, dp, &a, &grid, &need_merge);
+    int rc = prepare_decode(p, q, k_pages, v_pages, block_table_d, seq_lens_d, out, lse, s, dp, &a, &grid, &need_merge,
+                            plan_in_place);
     if (rc) return rc;
 
     if (p->profile) {
@@ -727,26 +761,41 @@ int pkv_decode_host(const void* q_h, const void* k_pages, const void* v_pages, c
     if (!q_h || !out_h || !lse_h) return PKV_EINVAL;
     const size_t rows = static_cast<size_t>(p->g.batch) * p->g.num_q_heads;
     const size_t q_bytes = rows * p->g.head_dim * 2, out_bytes = rows * p->g.head_dim * 4, lse_bytes = rows * 4;
-    if (!p->q_stage) {
-        if (cudaMalloc(&p->q_stage, q_bytes) != cudaSuccess || cudaMalloc(&p->out_stage, out_bytes) != cudaSuccess ||
-            cudaMalloc(&p->lse_stage, lse_bytes) != cudaSuccess) {
-            cudaFree(p->q_stage);
-            cudaFree(p->out_stage);
-            cudaFree(p->lse_stage);
-            p->q_stage = nullptr;
-            p->out_stage = nullptr;
-            p->lse_stage = nullptr;
-            return PKV_ENOMEM;
+    // Pinned host buffers are in the GPU's address space (read and written
+    // over NVLink-C2C on GB300): the kernel uses them in place.  Pageable ones
+    // go through the plan's pinned, mapped staging with a host memcpy.
+    const void* q_d = mapped_host_address(q_h, 16);
+    float* out_d = static_cast<float*>(const_cast<void*>(mapped_host_address(out_h, 16)));
+    float* lse_d = static_cast<float*>(const_cast<void*>(mapped_host_address(lse_h, 4)));
+    const size_t off_out = round_up(q_bytes, 256), off_lse = off_out + round_up(out_bytes, 256);
+    if ((!q_d || !out_d || !lse_d) && !p->host_stage) {
+        void* h = nullptr;
+        void* d = nullptr;
+        if (cudaMallocHost(&h, off_lse + lse_bytes) != cudaSuccess) return PKV_ENOMEM;
+        if (cudaHostGetDevicePointer(&d, h, 0) != cudaSuccess) {
+            cudaFreeHost(h);
+            return cuda_fail(cudaErrorInvalidValue);
         }
+        p->host_stage = static_cast<uint8_t*>(h);
+        p->host_stage_dev = static_cast<uint8_t*>(d);
     }
+    if (!q_d) {
+        memcpy(p->host_stage, q_h, q_bytes);
+        q_d = p->host_stage_dev;
+    }
+    const bool stage_out = !out_d, stage_lse = !lse_d;
+    if (stage_out) out_d = reinterpret_cast<float*>(p->host_stage_dev + off_out);
+    if (stage_lse) lse_d = reinterpret_cast<float*>(p->host_stage_dev + off_lse);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    PKV_CUDA(cudaMemcpyAsync(p->q_stage, q_h, q_bytes, cudaMemcpyHostToDevice, s));
-    int rc = enqueue_decode(p, p->q_stage, k_pages, v_pages, block_table_d, seq_lens_d, p->out_stage, p->lse_stage, s,
-                            nullptr);
+    const int rc = enqueue_decode(p, q_d, k_pages, v_pages, block_table_d, seq_lens_d, out_d, lse_d, s, nullptr,
+                                  /*plan_in_place=*/true);
+    // synchronise even after an error: a launched kernel may still read the
+    // staging and the plan in host memory
+    const cudaError_t e = cudaStreamSynchronize(s);
     if (rc) return rc;
-    PKV_CUDA(cudaMemcpyAsync(out_h, p->out_stage, out_bytes, cudaMemcpyDeviceToHost, s));
-    PKV_CUDA(cudaMemcpyAsync(lse_h, p->lse_stage, lse_bytes, cudaMemcpyDeviceToHost, s));
-    PKV_CUDA(cudaStreamSynchronize(s));
+    PKV_CUDA(e);
+    if (stage_out) memcpy(out_h, p->host_stage + off_out, out_bytes);
+    if (stage_lse) memcpy(lse_h, p->host_stage + off_lse, lse_bytes);
     return PKV_OK;
 }
 

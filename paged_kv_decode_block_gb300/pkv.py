@@ -301,9 +301,17 @@ def decode(q, k_pages, v_pages, block_table, seq_lens, plan: Plan, out, lse, str
 
 
 def decode_host(q_h, k_pages, v_pages, block_table, seq_lens, plan: Plan, out_h, lse_h, stream=None):
-    """pkv_decode_host: q from host memory, out / lse back to host memory (synchronises)."""
+    """pkv_decode_host: q from host memory, out / lse back to host memory (synchronises).
+    Pinned buffers (torch ``pin_memory()``) are used in place by the kernel; pageable
+    ones are staged through the plan's pinned buffer."""
     import torch
     bf = _bf16_types()
+    rows = plan.geom.batch * plan.geom.num_q_heads
+    for buf, what, nbytes in ((q_h, "q_h", rows * plan.D * 2), (out_h, "out_h", rows * plan.D * 4),
+                              (lse_h, "lse_h", rows * 4)):
+        size = buf.nbytes if isinstance(buf, np.ndarray) else buf.numel() * buf.element_size()
+        if size != nbytes:
+            raise ValueError(f"{what}: {size} bytes, expected {nbytes}")
     rc = load().pkv_decode_host(_host_ptr(q_h, "q_h"), _dev_ptr(k_pages, "k_pages", bf),
                                 _dev_ptr(v_pages, "v_pages", bf), _dev_ptr(block_table, "block_table", (torch.int32,)),
                                 _dev_ptr(seq_lens, "seq_lens", (torch.int32,)), plan.handle,

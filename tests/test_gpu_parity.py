@@ -224,19 +224,69 @@ def test_back_to_back_launches_of_different_plans():
         assert plan.status() == 0
 
 
+def _host_buffers(p, kind):
+    """q / out / lse host buffers: pinned (the kernel uses them in place), pageable
+    numpy arrays (staged through the plan's pinned buffer), or pinned tensors whose
+    address is 4 bytes past a 16-byte boundary (staged too: the kernel's vector
+    accesses need 16-byte alignment)."""
+    q = p.q.view(np.int16)
+    if kind == "pageable":
+        return q.copy(), np.empty((p.B, p.Hq, p.D), np.float32), np.empty((p.B, p.Hq), np.float32)
+    if kind == "pinned":
+        return (torch.from_numpy(q).pin_memory(), torch.empty((p.B, p.Hq, p.D), dtype=torch.float32).pin_memory(),
+                torch.empty((p.B, p.Hq), dtype=torch.float32).pin_memory())
+    qb = torch.empty(q.size + 2, dtype=torch.int16).pin_memory()
+    q_h = qb[2:].view(p.B, p.Hq, p.D)
+    q_h.copy_(torch.from_numpy(q))
+    out_h = torch.empty(p.B * p.Hq * p.D + 1, dtype=torch.float32).pin_memory()[1:].view(p.B, p.Hq, p.D)
+    lse_h = torch.empty(p.B * p.Hq + 1, dtype=torch.float32).pin_memory()[1:].view(p.B, p.Hq)
+    assert q_h.data_ptr() % 16 == 4 and out_h.data_ptr() % 16 == 4
+    return q_h, out_h, lse_h
+
+
+def _np(a):
+    return a.numpy() if isinstance(a, torch.Tensor) else a
+
+
+@pytest.mark.parametrize("kind", ["pinned", "pageable", "misaligned"])
 @pytest.mark.parametrize("route", ["split_queue", "direct", "persistent"])
-def test_decode_with_host_buffers(route):
+def test_decode_with_host_buffers(route, kind):
     """pkv_decode_host: q from host memory, out / lse back to host memory."""
     p = wl.make_problem("host_bufs", [700, 33, 1500, 0], Hq=16, Hkv=4, D=128, page_size=16, num_pages=200, seed=33)
     dev = to_device(p)
     plan = make_plan(p, force_mode=route, num_splits=5)
-    q_h = torch.from_numpy(p.q.view(np.int16)).pin_memory()
-    out_h = torch.empty((p.B, p.Hq, p.D), dtype=torch.float32).pin_memory()
-    lse_h = torch.empty((p.B, p.Hq), dtype=torch.float32).pin_memory()
+    q_h, out_h, lse_h = _host_buffers(p, kind)
     pkv.decode_host(q_h, dev["k"], dev["v"], dev["table"], dev["lens"], plan, out_h, lse_h)
-    assert_close(out_h.numpy(), lse_h.numpy(), *oracle_result(p), what=f"host buffers {route}")
+    assert_close(_np(out_h), _np(lse_h), *oracle_result(p), what=f"host buffers {route} {kind}")
     out, lse, _, _ = run(p, dev=dev, plan=plan)
-    assert np.array_equal(out, out_h.numpy()) and np.array_equal(lse, lse_h.numpy())
+    assert np.array_equal(out, _np(out_h)) and np.array_equal(lse, _np(lse_h))
+    assert plan.status() == 0
+
+
+@pytest.mark.parametrize("route", ["split_queue", "persistent"])
+def test_host_buffers_after_replanning(route):
+    """A re-planned queue is read in place from the plan's pinned host copy by
+    pkv_decode_host and uploaded by the next pkv_decode; both agree with the oracle
+    for the new lengths, and a second host-buffer decode (plan now uploaded) too."""
+    p = wl.make_problem("replan", [700, 33, 1500, 0], Hq=16, Hkv=4, D=128, page_size=16, num_pages=200, seed=34)
+    dev = to_device(p)
+    plan = make_plan(p, force_mode=route, num_splits=5)
+    q_h, out_h, lse_h = _host_buffers(p, "pinned")
+    pkv.decode_host(q_h, dev["k"], dev["v"], dev["table"], dev["lens"], plan, out_h, lse_h)
+    assert_close(out_h.numpy(), lse_h.numpy(), *oracle_result(p), what="before re-plan")
+    lens2 = np.array([650, 40, 1401, 0], np.int32)
+    p2 = wl.Problem("replan2", p.q, p.k_pages, p.v_pages, p.block_table, lens2, p.page_size)
+    ref2 = oracle_result(p2)
+    dev["lens"].copy_(torch.from_numpy(lens2))
+    plan.update(lens2, p.block_table)
+    pkv.decode_host(q_h, dev["k"], dev["v"], dev["table"], dev["lens"], plan, out_h, lse_h)   # plan read in place
+    assert_close(out_h.numpy(), lse_h.numpy(), *ref2, what="host buffers after re-plan")
+    first = (out_h.numpy().copy(), lse_h.numpy().copy())
+    out, lse, _, _ = run(p2, dev=dev, plan=plan)   # uploads the new plan
+    assert np.array_equal(out, first[0]) and np.array_equal(lse, first[1])
+    out_h.fill_(float("nan"))
+    pkv.decode_host(q_h, dev["k"], dev["v"], dev["table"], dev["lens"], plan, out_h, lse_h)   # uploaded plan
+    assert np.array_equal(out_h.numpy(), first[0]) and np.array_equal(lse_h.numpy(), first[1])
     assert plan.status() == 0
 
 
