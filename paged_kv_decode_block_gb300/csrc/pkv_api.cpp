@@ -124,6 +124,7 @@ struct Plan {
     int32_t grid = 0;
     int32_t empty_tiles = 0;
     bool need_merge = false;
+    bool any_empty_row = false;   // some row has no tokens
     int32_t merge = 0;   // pkv_plan_info.merge
     int32_t ws_slots = 0;
     int64_t kv_bytes = 0, ws_bytes = 0, table_bytes = 0;
@@ -188,6 +189,7 @@ int compute_plan(const pkv_geom& g, int32_t ps, const int32_t* lens, const Optio
     r->row_splits.assign(B, 0);
     r->empty_tiles = 0;
     r->need_merge = false;
+    r->any_empty_row = std::any_of(pages.begin(), pages.end(), [](int32_t n) { return n == 0; });
     int64_t merged_slots = 0;
 
     if (mode == PKV_MODE_DIRECT) {
@@ -673,6 +675,7 @@ int prepare_decode(pkv_plan_t p, const void* q, const void* k_pages, const void*
     a.use_mma = p->opts.math != PKV_MATH_FMA;
     a.copy_lsu = p->opts.copy != PKV_COPY_TMA;
     a.queue_host_staged = dp ? 0 : 1;
+    a.no_empty_rows = !dp && !pl.any_empty_row ? 1 : 0;
     a.k_pages = static_cast<const uint16_t*>(k_pages);
     a.v_pages = static_cast<const uint16_t*>(v_pages);
     a.scale_log2 = static_cast<float>(1.4426950408889634 / sqrt(static_cast<double>(p->g.head_dim)));

@@ -357,6 +357,7 @@ struct Smem {
     uint64_t empty[kStages];
     int tile_slot[2];
     int tile_fin, tile_splits;  // the finished tile's finalize flag and split count
+    int tile_base;              // workspace slot of split 0 of the finished tile's (row, KV head)
     int sync_ok;                // resident kernel: the last grid barrier / host wait succeeded
     int append_page, append_pos;
 };
@@ -796,13 +797,13 @@ __device__ void merge_unit(const AttnParams& p, int b, int kvh, int ns, float* w
 // output per thread with independent loads.  Same arithmetic as merge_unit;
 // all CTA threads call it.
 template <int D, int G>
-__device__ void merge_unit_staged(Smem<D, G>& sm, const AttnParams& p, int b, int kvh, int ns) {
+__device__ void merge_unit_staged(Smem<D, G>& sm, const AttnParams& p, int b, int kvh, int ns, int base_slot) {
     constexpr int kScratch = Cfg<D, G>::kStages * Cfg<D, G>::kMatBytes * 2;   // K and V stages
     constexpr int kSplitBytes = G * D * 4;
     constexpr int kOut = G * D / 4;                                            // float4 outputs of (b, kvh)
     constexpr int kPer = (kOut + kThreads - 1) / kThreads;
     const int tid = threadIdx.x;
-    const size_t base = static_cast<size_t>(p.row_start[b]) + static_cast<size_t>(kvh) * ns;
+    const size_t base = static_cast<size_t>(base_slot);
     uint8_t* scratch = &sm.k[0][0];   // k and v stages are adjacent
     float* w = reinterpret_cast<float*>(scratch);                  // [ns][G] weights
     const int w_bytes = (ns * G * 4 + 1023) & ~1023;
@@ -1048,6 +1049,7 @@ __device__ void run_tile(Smem<D, G>& sm, const AttnParams& p, TileWork tw, uint3
     if (threadIdx.x == 0) {
         sm.tile_fin = tw.finalize;
         sm.tile_splits = tw.splits;
+        sm.tile_base = tw.slot - tw.split;   // the merge needs no second read of the row table
     }
     const int ntok = tw.t1 > tw.t0 ? tw.t1 - tw.t0 : 0;
     int poisoned = tw.poisoned;
@@ -1163,7 +1165,7 @@ __device__ void merge_if_last(Smem<D, G>& sm, const AttnParams& p, int b, int kv
         // the stage buffers are idle here and serve as the merge's scratch
         static_assert(2 * Cfg<D, G>::kStages * Cfg<D, G>::kMatBytes >= kMergeCapFloats * 4 + 2 * G * D * 4,
                       "merge scratch");
-        merge_unit_staged<D, G>(sm, p, b, kvh, ns);
+        merge_unit_staged<D, G>(sm, p, b, kvh, ns, sm.tile_base);
     }
 }
 
@@ -1203,7 +1205,7 @@ __device__ void merge_all_splits(Smem<D, G>& sm, const AttnParams& p, int b, int
     const int groups = 32 / L;
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int sub = lane % L, grp = lane / L;
-    const size_t base = static_cast<size_t>(p.row_start[b]) + static_cast<size_t>(kvh) * ns;
+    const size_t base = static_cast<size_t>(sm.tile_base);
     for (int pass = i0; pass < i1; pass += (kThreads / 32) * groups) {   // uniform over the CTA
         const int i = pass + warp * groups + grp;
         const bool live = i < i1;
@@ -1339,6 +1341,7 @@ __global__ void __launch_bounds__(kThreads, MMA ? 2 : 1) attention_kernel(const 
     // rows with no tokens get no tiles: their neutral state is written after
     // the CTA's own tile, off the tile's critical path
     auto neutral_rows = [&]() {
+        if (p.no_empty_rows) return;   // the plan has no empty row
         for (int b = blockIdx.x; b < p.B; b += gridDim.x)
             if (p.row_splits[b] == 0) write_neutral_row(p, b, threadIdx.x, blockDim.x);
     };

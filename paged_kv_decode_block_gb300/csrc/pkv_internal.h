@@ -63,6 +63,8 @@ struct AttnParams {
     int32_t queue_host_staged;    // queue / row_start / row_splits come from a host upload (never
                                   // written by a kernel), so they may be read before the grid
                                   // dependency wait
+    int32_t no_empty_rows;        // queue / persistent routes: every row has tokens, so there is no
+                                  // neutral state to write (0: look for empty rows after the tiles)
     float scale_log2;             // log2(e) / sqrt(D)
 };
 

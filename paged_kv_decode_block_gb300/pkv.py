@@ -71,7 +71,7 @@ SIGNATURES = {
                                 ctypes.POINTER(ctypes.c_void_p)]),
     "pkv_plan_dry_run": (ctypes.c_int, [_I32P, _I32P, _I32, ctypes.POINTER(Geom), ctypes.POINTER(PlanOpts),
                                         ctypes.POINTER(PlanInfo), ctypes.POINTER(WorkItem), _I32, _I32P]),
-    "pkv_plan_update": (ctypes.c_int, [_P, _I32P, _I32P]),
+    "pkv_plan_update": (ctypes.c_int, [_P, _P, _P]),
     "pkv_plan_destroy": (None, [_P]),
     "pkv_plan_get_info": (ctypes.c_int, [_P, ctypes.POINTER(PlanInfo)]),
     "pkv_plan_queue": (ctypes.c_int, [_P, ctypes.POINTER(WorkItem), _I32, _I32P]),
@@ -185,10 +185,15 @@ def dry_run(seq_lens, block_table, page_size, *, B, Hq, Hkv, D, max_pages, num_p
 
 
 def _stream_handle(stream):
+    """cudaStream_t of `stream` (a torch.cuda.Stream or a raw handle); None means
+    torch's current stream on the current device."""
     import torch
     if stream is None:
+        raw = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+        if raw is not None:   # the handle alone, without building a Stream object
+            return raw(torch._C._cuda_getDevice())
         stream = torch.cuda.current_stream()
-    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
 
 
 class Plan:
@@ -217,7 +222,10 @@ class Plan:
     def update(self, seq_lens, block_table=None):
         lens = _i32(seq_lens)
         table = _i32(block_table) if block_table is not None else None
-        _check(load().pkv_plan_update(self.handle, _ptr_i32(lens), _ptr_i32(table)), "pkv_plan_update")
+        rc = (_lib or load()).pkv_plan_update(self.handle, lens.ctypes.data,
+                                              table.ctypes.data if table is not None else None)
+        if rc:
+            _check(rc, "pkv_plan_update")
 
     def info(self) -> dict:
         info = PlanInfo()
@@ -273,38 +281,48 @@ def plan(seq_lens, block_table, page_size, **kw) -> Plan:
 
 
 def _dev_ptr(t, name, dtypes=None):
-    import torch
-    if not isinstance(t, torch.Tensor) or not t.is_cuda:
-        raise TypeError(f"{name} must be a CUDA tensor")
-    if not t.is_contiguous():
-        raise ValueError(f"{name} must be contiguous")
+    """Device address of a contiguous CUDA tensor (checked), as an int."""
+    try:
+        ok = t.is_cuda and t.is_contiguous()
+    except AttributeError:
+        ok = False
+    if not ok:
+        raise TypeError(f"{name} must be a contiguous CUDA tensor")
     if dtypes is not None and t.dtype not in dtypes:
         raise TypeError(f"{name}: dtype {t.dtype} not in {dtypes}")
-    return ctypes.c_void_p(t.data_ptr())
+    return t.data_ptr()
+
+
+_BF16 = None
+_I32T = None
+_F32T = None
 
 
 def _bf16_types():
-    import torch
-    return (torch.bfloat16, torch.int16, getattr(torch, "uint16", torch.int16))
+    global _BF16, _I32T, _F32T
+    if _BF16 is None:
+        import torch
+        _BF16 = (torch.bfloat16, torch.int16, getattr(torch, "uint16", torch.int16))
+        _I32T = (torch.int32,)
+        _F32T = (torch.float32,)
+    return _BF16
 
 
 def decode(q, k_pages, v_pages, block_table, seq_lens, plan: Plan, out, lse, stream=None):
     """pkv_decode: out[b][h] / lse[b][h] for every row and query head."""
-    import torch
     bf = _bf16_types()
-    rc = load().pkv_decode(_dev_ptr(q, "q", bf), _dev_ptr(k_pages, "k_pages", bf),
-                           _dev_ptr(v_pages, "v_pages", bf), _dev_ptr(block_table, "block_table", (torch.int32,)),
-                           _dev_ptr(seq_lens, "seq_lens", (torch.int32,)), plan.handle,
-                           _dev_ptr(out, "out", (torch.float32,)), _dev_ptr(lse, "lse", (torch.float32,)),
-                           _stream_handle(stream))
-    _check(rc, "pkv_decode")
+    rc = (_lib or load()).pkv_decode(_dev_ptr(q, "q", bf), _dev_ptr(k_pages, "k_pages", bf),
+                                     _dev_ptr(v_pages, "v_pages", bf), _dev_ptr(block_table, "block_table", _I32T),
+                                     _dev_ptr(seq_lens, "seq_lens", _I32T), plan.handle,
+                                     _dev_ptr(out, "out", _F32T), _dev_ptr(lse, "lse", _F32T), _stream_handle(stream))
+    if rc:
+        _check(rc, "pkv_decode")
 
 
 def decode_host(q_h, k_pages, v_pages, block_table, seq_lens, plan: Plan, out_h, lse_h, stream=None):
     """pkv_decode_host: q from host memory, out / lse back to host memory (synchronises).
     Pinned buffers (torch ``pin_memory()``) are used in place by the kernel; pageable
     ones are staged through the plan's pinned buffer."""
-    import torch
     bf = _bf16_types()
     rows = plan.geom.batch * plan.geom.num_q_heads
     for buf, what, nbytes in ((q_h, "q_h", rows * plan.D * 2), (out_h, "out_h", rows * plan.D * 4),
@@ -312,11 +330,13 @@ def decode_host(q_h, k_pages, v_pages, block_table, seq_lens, plan: Plan, out_h,
         size = buf.nbytes if isinstance(buf, np.ndarray) else buf.numel() * buf.element_size()
         if size != nbytes:
             raise ValueError(f"{what}: {size} bytes, expected {nbytes}")
-    rc = load().pkv_decode_host(_host_ptr(q_h, "q_h"), _dev_ptr(k_pages, "k_pages", bf),
-                                _dev_ptr(v_pages, "v_pages", bf), _dev_ptr(block_table, "block_table", (torch.int32,)),
-                                _dev_ptr(seq_lens, "seq_lens", (torch.int32,)), plan.handle,
-                                _host_ptr(out_h, "out_h"), _host_ptr(lse_h, "lse_h"), _stream_handle(stream))
-    _check(rc, "pkv_decode_host")
+    rc = (_lib or load()).pkv_decode_host(_host_ptr(q_h, "q_h"), _dev_ptr(k_pages, "k_pages", bf),
+                                          _dev_ptr(v_pages, "v_pages", bf),
+                                          _dev_ptr(block_table, "block_table", _I32T),
+                                          _dev_ptr(seq_lens, "seq_lens", _I32T), plan.handle,
+                                          _host_ptr(out_h, "out_h"), _host_ptr(lse_h, "lse_h"), _stream_handle(stream))
+    if rc:
+        _check(rc, "pkv_decode_host")
 
 
 STATIC_SCRATCH_BYTES = 8 * 1024 * 1024
@@ -453,16 +473,16 @@ class Session:
 
 
 def _host_ptr(t, what):
-    """Address of a contiguous host buffer (torch CPU tensor or numpy array), or None."""
+    """Address (int) of a contiguous host buffer (torch CPU tensor or numpy array), or None."""
     if t is None:
         return None
     if isinstance(t, np.ndarray):
         if not t.flags["C_CONTIGUOUS"]:
             raise ValueError(f"{what}: host array must be contiguous")
-        return ctypes.c_void_p(t.ctypes.data)
+        return t.ctypes.data
     if t.is_cuda or not t.is_contiguous():
         raise ValueError(f"{what}: must be a contiguous host tensor")
-    return ctypes.c_void_p(t.data_ptr())
+    return t.data_ptr()
 
 
 class Resident:
