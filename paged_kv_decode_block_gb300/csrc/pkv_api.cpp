@@ -607,14 +607,20 @@ struct DevicePlan {
 // Everything a decode launch needs, checked: the pending plan upload is
 // enqueued on `s`, the TMA maps follow the pools, and `a` / `grid` /
 // `need_merge` describe the launch (over the device-built plan `dp` if given).
-// With `plan_in_place`, a plan not yet uploaded is read by the kernel from its
-// pinned, device-mapped host staging instead (no copy; the upload stays
-// pending for later launches), so the caller must not let the plan change
-// before the launch has finished.
+// How the host plan reaches the kernel (when it is not device-built).
+enum class PlanSource {
+    kUpload,        // copied to the device buffer on the stream if it changed (default)
+    kInPlace,       // a plan not yet uploaded is read by the kernel from its pinned, mapped host
+                    // staging (no copy; the upload stays pending for later launches): the caller
+                    // must not change the plan before the launch has finished
+    kKernelCopied   // an earlier kernel on the stream has copied it into the device buffer, so the
+                    // attention kernel must not read it before its grid dependency wait
+};
+
 int prepare_decode(pkv_plan_t p, const void* q, const void* k_pages, const void* v_pages,
                    const int32_t* block_table_d, const int32_t* seq_lens_d, float* out, float* lse, cudaStream_t s,
                    const DevicePlan* dp, pkv::AttnParams* a_out, int* grid_out, bool* need_merge_out,
-                   bool plan_in_place = false) {
+                   PlanSource src = PlanSource::kUpload) {
     if (!q || !k_pages || !v_pages || !block_table_d || !seq_lens_d || !out || !lse) return PKV_EINVAL;
     if (!aligned16(q) || !aligned16(k_pages) || !aligned16(v_pages) || !aligned16(out) ||
         (reinterpret_cast<uintptr_t>(lse) & 3u) || (reinterpret_cast<uintptr_t>(block_table_d) & 3u) ||
@@ -625,7 +631,7 @@ int prepare_decode(pkv_plan_t p, const void* q, const void* k_pages, const void*
     if (dev != p->device) return PKV_EINVAL;
 
     const int32_t* plan_buf = p->dev_buf;
-    if (p->dirty && !dp && plan_in_place && p->host_buf_dev) {
+    if (p->dirty && !dp && src == PlanSource::kInPlace && p->host_buf_dev) {
         plan_buf = p->host_buf_dev;
     } else if (p->dirty && !dp) {
         PKV_CUDA(cudaMemcpyAsync(p->dev_buf, p->host_buf, p->upload_bytes, cudaMemcpyHostToDevice, s));
@@ -674,7 +680,7 @@ int prepare_decode(pkv_plan_t p, const void* q, const void* k_pages, const void*
     a.all_merge = pl.merge == PKV_MERGE_ALL ? 1 : 0;
     a.use_mma = p->opts.math != PKV_MATH_FMA;
     a.copy_lsu = p->opts.copy != PKV_COPY_TMA;
-    a.queue_host_staged = dp ? 0 : 1;
+    a.queue_host_staged = dp || src == PlanSource::kKernelCopied ? 0 : 1;
     a.no_empty_rows = !dp && !pl.any_empty_row ? 1 : 0;
     a.k_pages = static_cast<const uint16_t*>(k_pages);
     a.v_pages = static_cast<const uint16_t*>(v_pages);
@@ -709,13 +715,13 @@ int prepare_decode(pkv_plan_t p, const void* q, const void* k_pages, const void*
 
 int enqueue_decode(pkv_plan_t p, const void* q, const void* k_pages, const void* v_pages,
                    const int32_t* block_table_d, const int32_t* seq_lens_d, float* out, float* lse, cudaStream_t s,
-                   const DevicePlan* dp, bool plan_in_place = false) {
+                   const DevicePlan* dp, PlanSource src = PlanSource::kUpload) {
     if (p->g.batch == 0) return PKV_OK;
     pkv::AttnParams a{};
     int grid = 0;
     bool need_merge = false;
     int rc = prepare_decode(p, q, k_pages, v_pages, block_table_d, seq_lens_d, out, lse, s, dp, &a, &grid, &need_merge,
-                            plan_in_place);
+                            src);
     if (rc) return rc;
 
     if (p->profile) {
@@ -791,7 +797,7 @@ int pkv_decode_host(const void* q_h, const void* k_pages, const void* v_pages, c
     if (stage_lse) lse_d = reinterpret_cast<float*>(p->host_stage_dev + off_lse);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const int rc = enqueue_decode(p, q_d, k_pages, v_pages, block_table_d, seq_lens_d, out_d, lse_d, s, nullptr,
-                                  /*plan_in_place=*/true);
+                                  PlanSource::kInPlace);
     // synchronise even after an error: a launched kernel may still read the
     // staging and the plan in host memory
     const cudaError_t e = cudaStreamSynchronize(s);
@@ -961,8 +967,12 @@ struct pkv_session_s {
     int32_t* rows = nullptr;      // [B] scratch for the pool's touched rows
     int32_t* table_d = nullptr;
     int32_t* lens_d = nullptr;
-    cudaEvent_t copied = nullptr;   // last table-entry upload has read the mirror
+    cudaEvent_t copied = nullptr;   // the last step's table entries (and new_pages) have been read
     bool copy_pending = false;
+    // host-planned steps: per row (table index, page id) of the step's new page,
+    // pinned and mapped; read by the step's append kernel (index -1: none)
+    int32_t* new_pages_h = nullptr;
+    const int32_t* new_pages_d = nullptr;
     // device-planned steps (pkv_session_device_plan)
     bool device_mode = false;
     int32_t* dev_free = nullptr;        // free page ids, handed out in order
@@ -1003,6 +1013,7 @@ void session_free(pkv_session_s* s) {
     cudaFree(s->dev_plan);
     cudaFreeHost(s->lens_h);
     cudaFreeHost(s->table_h);
+    cudaFreeHost(s->new_pages_h);
     delete[] s->rows;
     if (s->copied) cudaEventDestroy(s->copied);
     delete s;
@@ -1030,10 +1041,16 @@ int pkv_session_create(pkv_plan_t plan, pkv_pool_t pool, const int32_t* seq_lens
     s->rows = new (std::nothrow) int32_t[std::max(B, 1)];
     if (!s->rows || cudaMallocHost(&s->lens_h, sizeof(int32_t) * std::max(B, 1)) != cudaSuccess ||
         cudaMallocHost(&s->table_h, sizeof(int32_t) * std::max<size_t>(table_n, 1)) != cudaSuccess ||
+        cudaMallocHost(&s->new_pages_h, sizeof(int32_t) * 2 * std::max(B, 1)) != cudaSuccess ||
         cudaEventCreateWithFlags(&s->copied, cudaEventDisableTiming) != cudaSuccess) {
         session_free(s);
         return PKV_ENOMEM;
     }
+    void* mapped = nullptr;
+    if (cudaHostGetDevicePointer(&mapped, s->new_pages_h, 0) == cudaSuccess)
+        s->new_pages_d = static_cast<const int32_t*>(mapped);
+    else
+        (void)cudaGetLastError();   // not mapped: steps copy table entries with the copy engine
     if (B > 0) {
         memcpy(s->lens_h, seq_lens_h, sizeof(int32_t) * B);
         memcpy(s->table_h, block_table_h, sizeof(int32_t) * table_n);
@@ -1144,6 +1161,11 @@ int pkv_session_step(pkv_session_t s, const void* k_new, const void* v_new, void
     if (B == 0) return PKV_OK;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     if (s->device_mode) return session_step_device(s, k_new, v_new, k_pages, v_pages, q, out, lse, st);
+    // every pointer is checked before the step changes any state
+    if (!k_new || !v_new || !k_pages || !v_pages || !q || !out || !lse || !aligned16(k_new) || !aligned16(v_new) ||
+        !aligned16(k_pages) || !aligned16(v_pages) || !aligned16(q) || !aligned16(out) ||
+        (reinterpret_cast<uintptr_t>(lse) & 3u))
+        return PKV_EINVAL;
     if (s->copy_pending) {
         PKV_CUDA(cudaEventSynchronize(s->copied));
         s->copy_pending = false;
@@ -1151,6 +1173,53 @@ int pkv_session_step(pkv_session_t s, const void* k_new, const void* v_new, void
     int32_t n_rows = 0;
     int rc = pkv_pool_reserve(s->pool, s->lens_h, s->table_h, B, mp, ps, s->rows, &n_rows);
     if (rc) return rc;
+    pkv_plan_s* p = s->plan;
+    if (s->new_pages_d && p->host_buf_dev) {
+        // One launch does the step's host -> device traffic: it enters the new pages
+        // in the table, copies the re-planned queue into the plan's device buffer and
+        // appends the tokens; then the decode.  No copy engine is used.
+        for (int b = 0; b < B; ++b) s->new_pages_h[2 * b] = -1;
+        for (int32_t i = 0; i < n_rows; ++i) {
+            const int b = s->rows[i];
+            s->new_pages_h[2 * b] = s->lens_h[b] / ps;
+            s->new_pages_h[2 * b + 1] = s->table_h[static_cast<size_t>(b) * mp + s->lens_h[b] / ps];
+        }
+        for (int b = 0; b < B; ++b) ++s->lens_h[b];
+        if ((rc = pkv_plan_update(p, s->lens_h, nullptr))) return rc;
+        pkv::AppendStepParams ap{};
+        ap.k_new = static_cast<const uint16_t*>(k_new);
+        ap.v_new = static_cast<const uint16_t*>(v_new);
+        ap.k_pages = static_cast<uint16_t*>(k_pages);
+        ap.v_pages = static_cast<uint16_t*>(v_pages);
+        ap.block_table = s->table_d;
+        ap.seq_lens = s->lens_d;
+        ap.new_pages = s->new_pages_d;
+        // (a plan staging that is not mapped is uploaded by the decode's copy instead)
+        const bool kernel_copies = p->dirty && p->host_buf_dev;
+        if (kernel_copies) {
+            ap.plan_src = p->host_buf_dev;
+            ap.plan_dst = p->dev_buf;
+            ap.plan_words = static_cast<int64_t>(p->upload_bytes / sizeof(int32_t));
+        }
+        ap.status = &p->ctr->status;
+        ap.B = B;
+        ap.Hkv = g.num_kv_heads;
+        ap.D = g.head_dim;
+        ap.page_size = ps;
+        ap.max_pages = mp;
+        ap.num_pages = g.num_pages;
+        PKV_CUDA(pkv::launch_append_step(ap, st));
+        // the host staging (plan, new pages) may be rewritten once this kernel is done
+        PKV_CUDA(cudaEventRecord(s->copied, st));
+        s->copy_pending = true;
+        if (kernel_copies) {
+            PKV_CUDA(cudaEventRecord(p->upload_done, st));
+            p->upload_recorded = true;
+            p->dirty = false;
+        }
+        return enqueue_decode(p, q, k_pages, v_pages, s->table_d, s->lens_d, out, lse, st, nullptr,
+                              PlanSource::kKernelCopied);
+    }
     for (int32_t i = 0; i < n_rows; ++i) {
         const size_t at = static_cast<size_t>(s->rows[i]) * mp + s->lens_h[s->rows[i]] / ps;
         PKV_CUDA(cudaMemcpyAsync(s->table_d + at, s->table_h + at, sizeof(int32_t), cudaMemcpyHostToDevice, st));

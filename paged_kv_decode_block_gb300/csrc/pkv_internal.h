@@ -99,6 +99,27 @@ cudaError_t launch_append(const uint16_t* k_new, const uint16_t* v_new, uint16_t
                           uint16_t* v_pages, const int32_t* block_table, int32_t* seq_lens,
                           int B, int Hkv, int D, int page_size, int max_pages, int num_pages,
                           uint32_t* status, cudaStream_t stream);
+// One step of a host-planned continuous session in one launch: the new page
+// of every row that starts one is entered in the table, the step's plan is
+// copied from its pinned host staging into the plan's device buffer (the
+// decode launched next reads it there), and the new token of every row is
+// appended.  new_pages and plan_src are device views of mapped pinned host
+// memory, read by the kernel over the host link; no copy engine is used.
+struct AppendStepParams {
+    const uint16_t* k_new;      // device bf16 [B][Hkv][D]
+    const uint16_t* v_new;
+    uint16_t* k_pages;
+    uint16_t* v_pages;
+    int32_t* block_table;       // [B][max_pages]
+    int32_t* seq_lens;          // [B]
+    const int32_t* new_pages;   // [B][2]: (table index, page id) of the row's new page, or index -1
+    const int32_t* plan_src;    // plan staging (nullable: nothing to copy)
+    int32_t* plan_dst;
+    int64_t plan_words;         // int32 words of plan to copy
+    uint32_t* status;
+    int32_t B, Hkv, D, page_size, max_pages, num_pages;
+};
+cudaError_t launch_append_step(const AppendStepParams& p, cudaStream_t stream);
 // Bounded-wait self-test (see pkv_selftest_wait): result[3] = {wait returned true,
 // abort flag raised, second wait returned true}.
 cudaError_t launch_wait_selftest(uint32_t* status, uint64_t limit_ns, int* result, cudaStream_t stream);

@@ -4,10 +4,12 @@ One step of the continuous-session workload ("WPK persistent kernel",
 dotwave.ai: a fixed cohort of sessions advancing together; its page arenas are
 fixed pools, "What has to exist instead") is one native call, pkv_session_step:
   1. host: the page pool hands a fresh page to every row whose next token starts
-     a page (pkv_pool_reserve); only those table entries go to the device;
+     a page (pkv_pool_reserve);
   2. host: the plan is rebuilt for the lengths after the append
      (pkv_plan_update, same buffers, so device addresses stay fixed);
-  3. device: pkv_append writes each row's new K/V token and bumps seq_lens;
+  3. device, one launch: the new table entries and the plan are read from
+     pinned host memory and written to the device, and each row's new K/V
+     token is appended (seq_lens += 1);
   4. device: pkv_decode runs attention for every row.
 This module only owns the device tensors and forwards pointers; the sequencing
 and all arithmetic run in the library.

@@ -56,6 +56,7 @@ def test_continuous_sessions(math):
             assert np.array_equal(sess.table_h, table_h), step
             assert np.array_equal(sess.lens_h, lens_h), step
             assert np.array_equal(sess.lens_d.cpu().numpy(), lens_h), step
+            assert np.array_equal(sess.table_d.cpu().numpy(), table_h), step
             ref_out, ref_lse = oracle.decode(p.q, k_h, v_h, table_h, lens_h, nthreads=16)
             assert_close(sess.out.cpu().numpy(), sess.lse.cpu().numpy(), ref_out, ref_lse,
                          what=f"continuous step {step} {math}")
@@ -63,3 +64,35 @@ def test_continuous_sessions(math):
     assert np.array_equal(sess.k.cpu().numpy().view(np.uint16), k_h)
     assert np.array_equal(sess.v.cpu().numpy().view(np.uint16), v_h)
     assert sess.pool.free_count() == len(free)
+
+
+@pytest.mark.parametrize("route,splits", [("split_queue", 3), ("split_padded", 2), ("direct", 0)])
+def test_session_steps_other_routes(route, splits):
+    """Host-planned session steps on the non-persistent routes: the step's plan reaches
+    the device through the append launch, and the queue route then reads it only after
+    its grid dependency wait.  12 rows crossing page boundaries over 40 steps."""
+    lens = np.array([15, 16, 17, 31, 32, 33, 1, 100, 250, 47, 64, 5], np.int32)
+    steps = 40
+    need = int(sum(-(-(int(n) + steps) // 16) for n in lens))
+    max_pages = max(-(-(int(n) + steps) // 16) for n in lens)
+    p = wl.make_problem("sess_routes", lens, Hq=16, Hkv=4, D=128, page_size=16, num_pages=need + 9,
+                        max_pages=max_pages, seed=41)
+    opts = dict(force_mode=route) if route == "direct" else dict(force_mode=route, num_splits=splits)
+    sess = ContinuousSessions(p, **opts)
+    rng = np.random.default_rng(42)
+    k_h, v_h = p.k_pages, p.v_pages
+    lens_h, table_h, free = p.seq_lens.copy(), p.block_table.copy(), list(p.free_pages)
+    for step in range(steps):
+        kn, vn = wl.new_tokens(rng, p.B, p.Hkv, p.D)
+        sess.step(torch.from_numpy(kn.view(np.int16)).cuda(), torch.from_numpy(vn.view(np.int16)).cuda())
+        _expected_reserve(lens_h, table_h, free, p.page_size)
+        oracle.append(kn, vn, k_h, v_h, table_h, lens_h, inplace=True)
+        if step in (0, 16, 39):
+            torch.cuda.synchronize()
+            assert np.array_equal(sess.table_d.cpu().numpy(), table_h), step
+            assert np.array_equal(sess.lens_d.cpu().numpy(), lens_h), step
+            assert_close(sess.out.cpu().numpy(), sess.lse.cpu().numpy(),
+                         *oracle.decode(p.q, k_h, v_h, table_h, lens_h, nthreads=8),
+                         what=f"{route} session step {step}")
+            assert sess.plan.status() == 0
+    assert np.array_equal(sess.k.cpu().numpy().view(np.uint16), k_h)
