@@ -339,12 +339,17 @@ int pkv_decode_static(const void *q, const void *k_pages, const void *v_pages, c
  *                        lengths and table into pinned mirrors owned by the
  *                        session
  *   pkv_session_step     one step on `stream`: the pool hands a page to every row
- *                        whose next token starts one and only those table entries
- *                        are copied to the device; the plan is rebuilt for the
- *                        lengths after the append; then pkv_append (k_new, v_new
- *                        device bf16 [B][Hkv][D]) and pkv_decode (q, out, lse) are
- *                        enqueued back to back.  PKV_ENOSPACE when the pool or a
- *                        row runs out (nothing is enqueued then)
+ *                        whose next token starts one; the plan is rebuilt for the
+ *                        lengths after the append; then two launches: one enters
+ *                        the new pages in the device table, moves the plan to
+ *                        the device (both read in place from mapped pinned host
+ *                        memory, no copy engine) and appends k_new / v_new
+ *                        (device bf16 [B][Hkv][D]); then pkv_decode (q, out,
+ *                        lse).  The host staging is reused by the next step
+ *                        only after the first launch has run.  PKV_EINVAL for
+ *                        a null or misaligned pointer, PKV_ENOSPACE when the
+ *                        pool or a row runs out (nothing changes or is enqueued
+ *                        then)
  *   pkv_session_lengths / pkv_session_table   copy the host mirrors out
  * The session does not own the plan, the pool or any device memory.
  */
