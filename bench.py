@@ -179,6 +179,15 @@ def build_workload(name: str):
     return make(), opts
 
 
+def workload_config(p, name: str, world: int = 1) -> dict:
+    """The workload part of the JSON line's config, shared by both arms."""
+    return {"workload": p.name, "batch": p.B,
+            "seq_lens": "32768" if name == "batch1_long" else f"sum {int(p.seq_lens.sum())}",
+            "q_heads": p.Hq, "kv_heads": p.Hkv, "head_dim": p.D, "page_size": p.page_size,
+            "num_pages": p.num_pages, "requested_splits": int(p.num_splits),
+            "parallelism": f"replicas x{world} (partition by sequence, no collective)"}
+
+
 def parity_gate(p, out, lse, nthreads):
     import oracle
     ref_out, ref_lse = oracle.decode(p.q, p.k_pages, p.v_pages, p.block_table, p.seq_lens, nthreads=nthreads)
@@ -389,9 +398,7 @@ def run_pkv(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(med_ms, 5),
         "us_per_step": round(med_ms * 1e3, 2), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16 in, fp32 accumulate", "data": "synthetic (seeded, bf16 ~N(0,1))",
-        "config": {"workload": p.name, "batch": p.B, "seq_lens": "32768" if args.workload == "batch1_long"
-                   else f"sum {int(p.seq_lens.sum())}", "q_heads": p.Hq, "kv_heads": p.Hkv,
-                   "head_dim": p.D, "page_size": p.page_size, "num_pages": p.num_pages,
+        "config": {**workload_config(p, args.workload, world),
                    "mode": info["mode_name"], "math": args.math, "copy": args.copy,
                    "merge": info["merge_name"],
                    "num_splits": info["max_splits"],
@@ -399,8 +406,7 @@ def run_pkv(args):
                    "launches_per_step": info["launches_per_step"],
                    "l2": (f"cold: {rot} copies of the page pool and q used round robin, >= 6 x L2 bytes "
                           f"read between two reads of a copy; steps back to back, one event pair"
-                          if streamed else "flushed before every timed step (2 x L2 bytes written)"),
-                   "parallelism": f"replicas x{world} (partition by sequence, no collective)"},
+                          if streamed else "flushed before every timed step (2 x L2 bytes written)")},
         "kv_bytes_per_step": kv,
         "isolated_us_per_step": round(iso_med * 1e3, 2),
         "frac_of_nominal_7_9TBs": round(value / NOMINAL_HBM_GBS, 4),
@@ -723,7 +729,7 @@ def run_reference(args):
     p, _ = build_workload(args.workload)
     kv = p.kv_bytes()
     cores = host_cores()
-    budget = max(1.0, args.cpu_budget / max(1, args.steps + args.warmup))
+    budget = args.cpu_budget / max(1, args.steps)   # each step: at least one full oracle decode
     for _ in range(args.warmup):
         time_oracle(p, 0.0, cores)
     per_step = []
@@ -737,8 +743,7 @@ def run_reference(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(sec * 1e3, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded, bf16 ~N(0,1))",
-        "config": {"workload": p.name, "batch": p.B, "q_heads": p.Hq, "kv_heads": p.Hkv, "head_dim": p.D,
-                   "page_size": p.page_size},
+        "config": {**workload_config(p, args.workload, world), "mode": "fp64 CPU oracle (host cores)"},
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
                          "sample": f"each step = full oracle decode of the workload, repeated for ~{budget:.1f} s"},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},

@@ -106,7 +106,7 @@ def test_separate_merge_launch(route):
 
 
 @pytest.mark.parametrize("copy", COPIES)
-@pytest.mark.parametrize("page_size", [32, 64])
+@pytest.mark.parametrize("page_size", [32, 64, 128, 256])
 def test_larger_pages(page_size, copy):
     p = wl.make_problem("pages", [1, 63, 64, 65, 500], Hq=8, Hkv=2, D=128, page_size=page_size,
                         num_pages=24, seed=23)
