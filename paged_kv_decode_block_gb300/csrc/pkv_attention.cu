@@ -232,6 +232,13 @@ __device__ __forceinline__ void fence_sc_sys() { asm volatile("fence.sc.sys;" ::
 // Release / acquire fence at GPU scope (message passing between CTAs).
 __device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
 
+// Atomic add with acquire semantics at GPU scope; returns the old value.
+__device__ __forceinline__ uint32_t atom_add_acquire_gpu(uint32_t* p, uint32_t v) {
+    uint32_t old;
+    asm volatile("atom.acquire.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
+
 // Arrive on `bar` once every cp.async this thread has issued so far has landed
 // (the arrival counts against the barrier's expected count).
 __device__ __forceinline__ void cp_async_arrive_noinc(uint64_t* bar) {
@@ -816,14 +823,18 @@ __device__ void merge_unit_staged(Smem<D, G>& sm, const AttnParams& p, int b, in
         const uint32_t dst = smem_addr(obuf);
         for (int i = tid; i < vecs; i += kThreads) cp_async16_plain(dst + i * 16, src + static_cast<size_t>(i) * 16);
     };
-    issue(0);
     const int warp = tid / 32, lane = tid % 32;
+    // the LSEs of the first heads are requested before the partials, so their
+    // latency overlaps the issue of the copies
+    const float ls_first =
+        ns <= 32 && warp < G && lane < ns ? __ldcg(p.ws_lse + (base + lane) * G + warp) : -INFINITY;
+    issue(0);
     if (ns <= 32) {
         // One warp per head, one split per lane: the LSEs go straight from L2 to
         // registers, the max and sum are shuffles, and the normalised weights land
         // in shared memory while the partials are still arriving.
         for (int g = warp; g < G; g += kThreads / 32) {
-            const float ls = lane < ns ? __ldcg(p.ws_lse + (base + lane) * G + g) : -INFINITY;
+            const float ls = g == warp ? ls_first : lane < ns ? __ldcg(p.ws_lse + (base + lane) * G + g) : -INFINITY;
             const bool nan = __any_sync(kFull, isnan(ls));
             float M = ls;
 #pragma unroll
@@ -1145,19 +1156,18 @@ __device__ void run_tile(Smem<D, G>& sm, const AttnParams& p, TileWork tw, uint3
 template <int D, int G>
 __device__ void merge_if_last(Smem<D, G>& sm, const AttnParams& p, int b, int kvh, int ns) {
     // The CTA's partial is written; after the barrier, thread 0's fence makes those
-    // writes visible device-wide before its arrival is counted (release), and after
-    // the arrival its fence orders the other splits' writes before our reads (acquire).
-    // (The caller has just passed a barrier too; dropping this one measured slower.)
+    // writes visible device-wide before its arrival is counted (release), and the
+    // arrival's acquire orders the other splits' writes before our reads.  The
+    // counter's reset needs no fence: the next launch reads it only after this grid
+    // has completed.  (The caller has just passed a barrier too; dropping this one
+    // measured slower.)
     __syncthreads();
     if (threadIdx.x == 0) {
         const int u = b * p.Hkv + kvh;
         fence_acq_rel_gpu();
-        const uint32_t prev = atomicAdd(&p.arrive[u], 1u);
+        const uint32_t prev = atom_add_acquire_gpu(&p.arrive[u], 1u);
         const int last = prev == static_cast<uint32_t>(ns - 1);
-        if (last) {
-            p.arrive[u] = 0;   // ready for the next launch
-            fence_acq_rel_gpu();
-        }
+        if (last) p.arrive[u] = 0;   // ready for the next launch
         sm.tile_slot[1] = last;
     }
     __syncthreads();
