@@ -218,6 +218,15 @@ def time_oracle(p, budget_s: float, nthreads: int):
     return (time.perf_counter() - t0) / n, n
 
 
+def single_thread_oracle(p, kv_bytes: int, estimate_s: float, limit_s: float = 15.0):
+    """One full oracle step on one thread, when it should take under `limit_s`
+    (estimated from the threaded step); else None."""
+    if estimate_s > limit_s:
+        return None
+    sec, _ = time_oracle(p, 0.0, 1)
+    return {"value": round(kv_bytes / sec / 1e9, 4), "unit": "GB/s", "cores": 1, "ms_per_step": round(sec * 1e3, 1)}
+
+
 # ----------------------------------------------------------------------------- our arm
 
 def run_pkv(args):
@@ -391,6 +400,7 @@ def run_pkv(args):
         cpu = {"value": round(kv / sec / 1e9, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
                "sample": f"{n} full oracle decode step(s) of the same workload (fp64 C, {cores} threads), "
                          f"{sec * 1e3:.0f} ms per step"}
+        cpu["single_thread"] = single_thread_oracle(p, kv, sec * cores)
 
     clocks = clk.summary()
     line = {
