@@ -198,6 +198,24 @@ def parity_gate(p, out, lse, nthreads):
     return ok, err_out, err_lse
 
 
+# what one attention launch does on each route, for the roofline line
+ROUTE_WORDS = {
+    "split_queue": "split partials over the compact queue, LSE merge fused",
+    "split_padded": "split partials over the padded split grid, LSE merge fused",
+    "direct": "one tile per (row, KV head), finalised in place",
+    "persistent": "persistent CTAs draining the queue, LSE merge fused",
+}
+
+
+def route_words(info: dict) -> str:
+    words = ROUTE_WORDS.get(info["mode_name"], info["mode_name"])
+    if info["merge_name"] == "separate":
+        return words.replace("LSE merge fused", "LSE merge in its own launch")
+    if info["merge_name"] == "none":
+        return words.replace(", LSE merge fused", "")
+    return words
+
+
 def host_cores():
     try:
         return len(os.sched_getaffinity(0))
@@ -423,7 +441,7 @@ def run_pkv(args):
         "kernel_ms": {"attention": round(attn_ms, 5), "merge": round(merge_ms, 5)},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_source": peak_src,
-                     "kernel": "attention_kernel (split partial over the compact queue)",
+                     "kernel": f"attention_kernel ({route_words(info)})",
                      "algorithmic_bytes_per_launch": alg_bytes_attn,
                      "traffic": profiled_traffic(args.workload)},
         "e2e": {"value": round(kv * world / e2e_med / 1e9, 2), "unit": "GB/s",
