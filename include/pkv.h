@@ -195,7 +195,11 @@ int pkv_plan_dry_run(const int32_t *seq_lens_h, const int32_t *block_table_h, in
 
 /* Re-plan for new lengths (same geometry, page size and options), reusing the
  * plan's buffers; they grow only when the new tile count needs more room.
- * Waits for the previous upload of the queue to finish before rewriting it. */
+ * Waits for the previous upload of the queue to finish before rewriting it.
+ * Errors: PKV_EINVAL / PKV_EUNSUPPORTED leave the plan as it was.  After
+ * PKV_ENOMEM (or PKV_ECUDA) the plan's buffers may not hold the new tiles: a
+ * decode with it returns PKV_ENOMEM and launches nothing until an update
+ * succeeds. */
 int pkv_plan_update(pkv_plan_t plan, const int32_t *seq_lens_h, const int32_t *block_table_h);
 
 void pkv_plan_destroy(pkv_plan_t plan);
@@ -215,7 +219,8 @@ int pkv_plan_queue(pkv_plan_t plan, pkv_work_item *items, int32_t capacity, int3
  *   seq_lens_d            device int32 [B]; must equal the lengths the plan was built from
  *   out, lse              device fp32 outputs
  * Enqueues 1 or 2 kernels (pkv_plan_info.launches_per_step) on `stream`.
- * Errors: PKV_EINVAL (null pointer, misalignment), PKV_ECUDA (launch failure).
+ * Errors: PKV_EINVAL (null pointer, misalignment), PKV_ENOMEM (a plan whose
+ * last pkv_plan_update ran out of memory), PKV_ECUDA (launch failure).
  * Device-side faults are reported through pkv_status.
  */
 int pkv_decode(const void *q, const void *k_pages, const void *v_pages,

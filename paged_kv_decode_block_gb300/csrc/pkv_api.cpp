@@ -30,6 +30,7 @@
 #include <deque>
 #include <mutex>
 #include <new>
+#include <utility>
 #include <vector>
 
 #include "pkv.h"
@@ -358,6 +359,7 @@ struct pkv_plan_s {
     int ctas_per_sm = 1;
     int64_t resident_ctas = 0;   // attention CTAs the device holds at once
     Plan plan;
+    Plan next;   // pkv_plan_update builds here, then swaps: a failed update leaves `plan` as it was
 
     // host staging (pinned) and device copy: [items][row_start B][row_splits B]
     int32_t* host_buf = nullptr;
@@ -423,6 +425,7 @@ int stage(pkv_plan_s* p) {
         p->host_buf = nullptr;
         p->host_buf_dev = nullptr;
         p->dev_buf = nullptr;
+        p->buf_cap_items = 0;
         const size_t bytes = (cap * 6 + 2 * static_cast<size_t>(B)) * sizeof(int32_t);
         if (cudaMallocHost(&p->host_buf, bytes) != cudaSuccess) return PKV_ENOMEM;
         if (cudaMalloc(&p->dev_buf, bytes) != cudaSuccess) return PKV_ENOMEM;
@@ -441,6 +444,7 @@ int stage(pkv_plan_s* p) {
         cudaFree(p->ws_lse);
         p->ws_o = nullptr;
         p->ws_lse = nullptr;
+        p->ws_cap_slots = 0;
         if (cudaMalloc(&p->ws_o, cap * G * p->g.head_dim * sizeof(float)) != cudaSuccess) return PKV_ENOMEM;
         if (cudaMalloc(&p->ws_lse, cap * G * sizeof(float)) != cudaSuccess) return PKV_ENOMEM;
         p->ws_cap_slots = cap;
@@ -566,8 +570,9 @@ int pkv_plan_update(pkv_plan_t p, const int32_t* seq_lens_h, const int32_t* bloc
     if (rc) return rc;
     if (p->upload_recorded) PKV_CUDA(cudaEventSynchronize(p->upload_done));
     if ((rc = compute_plan(p->g, p->page_size, seq_lens_h, p->opts, p->num_sms, p->ctas_per_sm, p->resident_ctas,
-                           &p->plan)))
+                           &p->next)))
         return rc;
+    std::swap(p->plan, p->next);
     return stage(p);
 }
 
@@ -629,6 +634,10 @@ int prepare_decode(pkv_plan_t p, const void* q, const void* k_pages, const void*
     int dev = -1;
     PKV_CUDA(cudaGetDevice(&dev));
     if (dev != p->device) return PKV_EINVAL;
+    // buffers that do not hold the plan (an update that ran out of memory) launch nothing
+    if (!p->host_buf || !p->dev_buf || !p->ws_o || !p->ws_lse || p->plan.items.size() > p->buf_cap_items ||
+        static_cast<size_t>(std::max(p->plan.ws_slots, 0)) > p->ws_cap_slots)
+        return PKV_ENOMEM;
 
     const int32_t* plan_buf = p->dev_buf;
     if (p->dirty && !dp && src == PlanSource::kInPlace && p->host_buf_dev) {
@@ -1083,6 +1092,7 @@ int pkv_session_device_plan(pkv_session_t s, pkv_stream_t stream) {
         cudaFree(p->ws_lse);
         p->ws_o = nullptr;
         p->ws_lse = nullptr;
+        p->ws_cap_slots = 0;
         if (cudaMalloc(&p->ws_o, cap * G * g.head_dim * sizeof(float)) != cudaSuccess) return PKV_ENOMEM;
         if (cudaMalloc(&p->ws_lse, cap * G * sizeof(float)) != cudaSuccess) return PKV_ENOMEM;
         p->ws_cap_slots = cap;
@@ -1091,8 +1101,15 @@ int pkv_session_device_plan(pkv_session_t s, pkv_stream_t stream) {
     const size_t plan_ints = static_cast<size_t>(cap) * 6 + 2 * static_cast<size_t>(B) + 1;
     if (cudaMalloc(&s->dev_plan, plan_ints * sizeof(int32_t)) != cudaSuccess ||
         cudaMalloc(&s->dev_free, std::max<size_t>(pages.size(), 1) * sizeof(int32_t)) != cudaSuccess ||
-        cudaMalloc(&s->dev_free_state, 2 * sizeof(uint32_t)) != cudaSuccess)
+        cudaMalloc(&s->dev_free_state, 2 * sizeof(uint32_t)) != cudaSuccess) {
+        cudaFree(s->dev_plan);   // none of them is kept: a later call starts over
+        cudaFree(s->dev_free);
+        cudaFree(s->dev_free_state);
+        s->dev_plan = nullptr;
+        s->dev_free = nullptr;
+        s->dev_free_state = nullptr;
         return PKV_ENOMEM;
+    }
     const uint32_t state[2] = {0u, static_cast<uint32_t>(pages.size())};
     PKV_CUDA(cudaMemcpyAsync(s->dev_free, pages.data(), pages.size() * sizeof(int32_t), cudaMemcpyHostToDevice, st));
     PKV_CUDA(cudaMemcpyAsync(s->dev_free_state, state, sizeof(state), cudaMemcpyHostToDevice, st));
