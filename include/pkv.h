@@ -354,7 +354,8 @@ int pkv_decode_static(const void *q, const void *k_pages, const void *v_pages, c
  *                        only after the first launch has run.  PKV_EINVAL for
  *                        a null or misaligned pointer, PKV_ENOSPACE when the
  *                        pool or a row runs out (nothing changes or is enqueued
- *                        then)
+ *                        then).  After PKV_ENOMEM or PKV_ECUDA the host mirrors
+ *                        may be a step ahead of the device: destroy the session
  *   pkv_session_lengths / pkv_session_table   copy the host mirrors out
  * The session does not own the plan, the pool or any device memory.
  */
