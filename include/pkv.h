@@ -289,6 +289,7 @@ int pkv_profile_read(pkv_plan_t plan, float *ms, int32_t capacity, int32_t *coun
  * Host page pool: a FIFO free list of page ids, for callers that grow rows one
  * token at a time (the continuous-session workload).
  *   pkv_pool_create     copies `count` free page ids, handed out in that order
+ *                       (PKV_EINVAL for an id outside [0, num_pages) or listed twice)
  *   pkv_pool_reserve    for every row whose next token (position seq_lens_h[b])
  *                       starts a new page whose table entry is still unassigned
  *                       (negative), pops a page into
@@ -296,7 +297,8 @@ int pkv_profile_read(pkv_plan_t plan, float *ms, int32_t capacity, int32_t *coun
  *                       rows it touched to rows_out (nullable, capacity B) and
  *                       their number to *n_rows.  PKV_ENOSPACE when the pool or
  *                       a row's table runs out (no row is changed then).
- *   pkv_pool_release    returns pages to the back of the free list
+ *   pkv_pool_release    returns pages to the back of the free list; PKV_EINVAL
+ *                       (and no change) for a page that is already free
  */
 int pkv_pool_create(const int32_t *free_pages, int32_t count, int32_t num_pages, pkv_pool_t *pool);
 int pkv_pool_reserve(pkv_pool_t pool, const int32_t *seq_lens_h, int32_t *block_table_h,

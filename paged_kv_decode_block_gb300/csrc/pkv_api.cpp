@@ -896,6 +896,7 @@ int pkv_profile_read(pkv_plan_t p, float* ms, int32_t capacity, int32_t* count) 
 
 struct pkv_pool_s {
     std::deque<int32_t> free_list;
+    std::vector<uint8_t> is_free;   // [num_pages]: the page is in free_list
     int32_t num_pages = 0;
 };
 
@@ -908,6 +909,14 @@ int pkv_pool_create(const int32_t* free_pages, int32_t count, int32_t num_pages,
         if (free_pages[i] < 0 || free_pages[i] >= num_pages) return PKV_EINVAL;
     pkv_pool_s* p = new (std::nothrow) pkv_pool_s;
     if (!p) return PKV_ENOMEM;
+    p->is_free.assign(num_pages, 0);
+    for (int32_t i = 0; i < count; ++i) {
+        if (p->is_free[free_pages[i]]) {   // listed twice
+            delete p;
+            return PKV_EINVAL;
+        }
+        p->is_free[free_pages[i]] = 1;
+    }
     p->free_list.assign(free_pages, free_pages + count);
     p->num_pages = num_pages;
     *pool = p;
@@ -934,9 +943,10 @@ int pkv_pool_reserve(pkv_pool_t pool, const int32_t* seq_lens_h, int32_t* block_
     int32_t k = 0;
     for (int32_t b = 0; b < batch; ++b) {
         if (!wants_page(b)) continue;
-        block_table_h[static_cast<size_t>(b) * max_pages_per_seq + seq_lens_h[b] / page_size] =
-            pool->free_list.front();
+        const int32_t page = pool->free_list.front();
+        block_table_h[static_cast<size_t>(b) * max_pages_per_seq + seq_lens_h[b] / page_size] = page;
         pool->free_list.pop_front();
+        pool->is_free[page] = 0;
         if (rows_out) rows_out[k] = b;
         ++k;
     }
@@ -948,6 +958,14 @@ int pkv_pool_release(pkv_pool_t pool, const int32_t* pages, int32_t count) {
     if (!pool || count < 0 || (count > 0 && !pages)) return PKV_EINVAL;
     for (int32_t i = 0; i < count; ++i)
         if (pages[i] < 0 || pages[i] >= pool->num_pages) return PKV_EINVAL;
+    // a page that is free already (or listed twice) is refused, and nothing changes
+    for (int32_t i = 0; i < count; ++i) {
+        if (pool->is_free[pages[i]]) {
+            for (int32_t j = 0; j < i; ++j) pool->is_free[pages[j]] = 0;
+            return PKV_EINVAL;
+        }
+        pool->is_free[pages[i]] = 1;
+    }
     pool->free_list.insert(pool->free_list.end(), pages, pages + count);
     return PKV_OK;
 }
@@ -1115,6 +1133,7 @@ int pkv_session_device_plan(pkv_session_t s, pkv_stream_t stream) {
     PKV_CUDA(cudaMemcpyAsync(s->dev_free_state, state, sizeof(state), cudaMemcpyHostToDevice, st));
     PKV_CUDA(cudaStreamSynchronize(st));   // the host vectors above go out of scope
     s->pool->free_list.clear();            // those pages now belong to the device allocator
+    std::fill(s->pool->is_free.begin(), s->pool->is_free.end(), uint8_t{0});
     s->free_cap = static_cast<int32_t>(std::max<size_t>(pages.size(), 1));
     s->queue_cap = static_cast<int32_t>(cap);
     s->chunk = chunk;

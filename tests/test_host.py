@@ -203,6 +203,25 @@ def test_pool_exhaustion_changes_nothing():
         pkv.Pool([8], num_pages=8)             # page id outside the pool
 
 
+def test_pool_refuses_a_page_twice():
+    with pytest.raises(pkv.PkvError) as e:
+        pkv.Pool([2, 5, 2], num_pages=8)       # listed twice
+    assert e.value.code == pkv.EINVAL
+    pool = pkv.Pool([2, 5], num_pages=8)
+    for again in ([5], [6, 2], [6, 6]):        # already free, or twice in one call
+        with pytest.raises(pkv.PkvError) as e:
+            pool.release(again)
+        assert e.value.code == pkv.EINVAL
+        assert pool.free_count() == 2          # nothing changed
+    table = np.full((1, 2), -1, np.int32)
+    pool.reserve(np.array([0], np.int32), table, 16)
+    assert table[0, 0] == 2 and pool.free_count() == 1
+    pool.release([2, 6])                       # 2 is in use again, 6 never was free: both come back
+    assert pool.free_count() == 3
+    with pytest.raises(pkv.PkvError):
+        pool.release([2])
+
+
 def test_strerror_covers_every_code():
     lib = pkv.load()
     for code in range(7):
