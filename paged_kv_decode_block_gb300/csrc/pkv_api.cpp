@@ -33,12 +33,24 @@
 #include <utility>
 #include <vector>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "pkv.h"
 #include "pkv_internal.h"
 
 namespace {
 
 thread_local int g_last_cuda_error = 0;
+
+// An NVTX range over one library call, so that a profiler's timeline shows the
+// host side of each call (planning, staging, launches).  Without a profiler
+// attached a push or pop is one test of a null function pointer.
+struct NvtxRange {
+    explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+    ~NvtxRange() { nvtxRangePop(); }
+    NvtxRange(const NvtxRange&) = delete;
+    NvtxRange& operator=(const NvtxRange&) = delete;
+};
 
 int cuda_fail(cudaError_t e) {
     g_last_cuda_error = static_cast<int>(e);
@@ -485,6 +497,7 @@ int pkv_last_cuda_error(void) { return g_last_cuda_error; }
 int pkv_plan_dry_run(const int32_t* seq_lens_h, const int32_t* block_table_h, int32_t page_size,
                      const pkv_geom* geom, const pkv_plan_opts* opts, pkv_plan_info* info,
                      pkv_work_item* items, int32_t capacity, int32_t* count) {
+    NvtxRange range("pkv_plan_dry_run");
     Options o;
     int rc = resolve_options(opts, &o);
     if (rc) return rc;
@@ -504,6 +517,7 @@ int pkv_plan_dry_run(const int32_t* seq_lens_h, const int32_t* block_table_h, in
 
 int pkv_plan(const int32_t* seq_lens_h, const int32_t* block_table_h, int32_t page_size, const pkv_geom* geom,
              const pkv_plan_opts* opts, pkv_plan_t* plan) {
+    NvtxRange range("pkv_plan");
     if (!plan) return PKV_EINVAL;
     *plan = nullptr;
     Options o;
@@ -565,6 +579,7 @@ int pkv_plan(const int32_t* seq_lens_h, const int32_t* block_table_h, int32_t pa
 }
 
 int pkv_plan_update(pkv_plan_t p, const int32_t* seq_lens_h, const int32_t* block_table_h) {
+    NvtxRange range("pkv_plan_update");
     if (!p) return PKV_EINVAL;
     int rc = validate_rows(p->g, p->page_size, seq_lens_h, block_table_h);
     if (rc) return rc;
@@ -767,6 +782,7 @@ extern "C" {
 
 int pkv_decode(const void* q, const void* k_pages, const void* v_pages, const int32_t* block_table_d,
                const int32_t* seq_lens_d, pkv_plan_t p, float* out, float* lse, pkv_stream_t stream) {
+    NvtxRange range("pkv_decode");
     if (!p) return PKV_EINVAL;
     return enqueue_decode(p, q, k_pages, v_pages, block_table_d, seq_lens_d, out, lse,
                           reinterpret_cast<cudaStream_t>(stream), nullptr);
@@ -774,6 +790,7 @@ int pkv_decode(const void* q, const void* k_pages, const void* v_pages, const in
 
 int pkv_decode_host(const void* q_h, const void* k_pages, const void* v_pages, const int32_t* block_table_d,
                     const int32_t* seq_lens_d, pkv_plan_t p, float* out_h, float* lse_h, pkv_stream_t stream) {
+    NvtxRange range("pkv_decode_host");
     if (!p) return PKV_EINVAL;
     if (p->g.batch == 0) return PKV_OK;
     if (!q_h || !out_h || !lse_h) return PKV_EINVAL;
@@ -819,6 +836,7 @@ int pkv_decode_host(const void* q_h, const void* k_pages, const void* v_pages, c
 
 int pkv_append(const void* k_new, const void* v_new, void* k_pages, void* v_pages, const int32_t* block_table_d,
                int32_t* seq_lens_d, pkv_plan_t p, pkv_stream_t stream) {
+    NvtxRange range("pkv_append");
     if (!p) return PKV_EINVAL;
     if (p->g.batch == 0) return PKV_OK;
     if (!k_new || !v_new || !k_pages || !v_pages || !block_table_d || !seq_lens_d) return PKV_EINVAL;
@@ -1087,6 +1105,7 @@ int pkv_session_create(pkv_plan_t plan, pkv_pool_t pool, const int32_t* seq_lens
 }
 
 int pkv_session_device_plan(pkv_session_t s, pkv_stream_t stream) {
+    NvtxRange range("pkv_session_device_plan");
     if (!s) return PKV_EINVAL;
     if (s->device_mode) return PKV_OK;
     pkv_plan_s* p = s->plan;
@@ -1191,6 +1210,7 @@ int session_step_device(pkv_session_t s, const void* k_new, const void* v_new, v
 
 int pkv_session_step(pkv_session_t s, const void* k_new, const void* v_new, void* k_pages, void* v_pages,
                      const void* q, float* out, float* lse, pkv_stream_t stream) {
+    NvtxRange range("pkv_session_step");
     if (!s || s->resident) return PKV_EINVAL;
     const pkv_geom& g = s->plan->g;
     const int B = g.batch, ps = s->plan->page_size, mp = g.max_pages_per_seq;
@@ -1331,6 +1351,7 @@ void host_store(uint32_t* p, uint32_t v) { __atomic_store_n(p, v, __ATOMIC_SEQ_C
 
 int pkv_resident_start(pkv_session_t s, void* k_pages, void* v_pages, void* q_d, void* k_new_d, void* v_new_d,
                        float* out_d, float* lse_d, int64_t idle_limit_ns, int32_t times_cap, pkv_resident_t* out) {
+    NvtxRange range("pkv_resident_start");
     if (!out) return PKV_EINVAL;
     *out = nullptr;
     if (!s || !s->device_mode || s->resident || !k_pages || !v_pages || !q_d || !k_new_d || !v_new_d || !out_d ||
@@ -1417,6 +1438,7 @@ int pkv_resident_start(pkv_session_t s, void* k_pages, void* v_pages, void* q_d,
 
 int pkv_resident_step(pkv_resident_t r, const void* q_h, const void* k_new_h, const void* v_new_h, float* out_h,
                       float* lse_h, int64_t wait_limit_ns) {
+    NvtxRange range("pkv_resident_step");
     if (!r || !r->running || wait_limit_ns <= 0) return PKV_EINVAL;
     if (q_h) PKV_CUDA(cudaMemcpyAsync(r->q_d, q_h, r->q_bytes, cudaMemcpyHostToDevice, r->cstream));
     if (k_new_h) PKV_CUDA(cudaMemcpyAsync(r->k_new_d, k_new_h, r->new_bytes, cudaMemcpyHostToDevice, r->cstream));
