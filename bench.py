@@ -431,6 +431,7 @@ def run_pkv(args):
                    "merge": info["merge_name"],
                    "num_splits": info["max_splits"],
                    "chunk_pages": info["chunk_pages"], "tiles": info["num_work_items"],
+                   "empty_tiles": info["empty_tiles"], "merge_state_bytes": info["workspace_bytes"],
                    "launches_per_step": info["launches_per_step"],
                    "l2": (f"cold: {rot} copies of the page pool and q used round robin, >= 6 x L2 bytes "
                           f"read between two reads of a copy; steps back to back, one event pair"
