@@ -198,6 +198,7 @@ int compute_plan(const pkv_geom& g, int32_t ps, const int32_t* lens, const Optio
     r->kv_bytes = tokens * Hkv * D * 2 * 2;
     r->table_bytes = p_total * Hkv * 4;
     r->items.clear();
+    r->order.clear();   // only the compact-queue routes hand tiles out in an order
     r->row_start.assign(B, 0);
     r->row_splits.assign(B, 0);
     r->empty_tiles = 0;
