@@ -17,7 +17,11 @@ Readings taken where the page is silent:
   * a requested split count S maps to C = ceil(P_max / S), P_max = max_b P_b;
   * queue order is lexicographic in (b, kvh, s);
   * the padded ("rectangular") grid has B * Hkv * S_max slots,
-    S_max = ceil(P_max / C); slots with s >= S_b are empty.
+    S_max = ceil(P_max / C); slots with s >= S_b are empty;
+  * the single-pass route (the summary's unsplit kernel for large batches,
+    Methodology section 2) has one tile per (row, KV head) over the whole row,
+    pages [0, P_b), split index 0, listed for every row in (b, kvh) order (an
+    empty row's tile is empty and stands for its neutral state).
 Each tile is the int32 record (b, kvh, s, page_begin, page_end), end exclusive.
 """
 from __future__ import annotations
@@ -61,4 +65,13 @@ def enumerate_padded_grid(seq_lens, page_size: int, num_kv_heads: int, chunk_pag
                 begin = min(s * chunk_pages, p_b)
                 end = min((s + 1) * chunk_pages, p_b)
                 tiles.append((b, kvh, s, begin, end))
+    return np.array(tiles, dtype=np.int32).reshape(-1, 5)
+
+
+def enumerate_direct(seq_lens, page_size: int, num_kv_heads: int) -> np.ndarray:
+    """Single-pass tiles: one per (b, kvh), the whole row, in (b, kvh) order."""
+    tiles = []
+    for b, n in enumerate(seq_lens):
+        for kvh in range(num_kv_heads):
+            tiles.append((b, kvh, 0, 0, pages_of(n, page_size)))
     return np.array(tiles, dtype=np.int32).reshape(-1, 5)

@@ -66,6 +66,5 @@ def expected_queue(p: wl.Problem, plan_info: dict) -> np.ndarray:
     if mode == pkv.MODE_SPLIT_PADDED:
         return oracle.enumerate_padded_grid(p.seq_lens, p.page_size, p.Hkv, C)
     if mode == pkv.MODE_DIRECT:
-        return np.array([(b, h, 0, 0, -(-int(n) // p.page_size)) for b, n in enumerate(p.seq_lens)
-                         for h in range(p.Hkv)], np.int32).reshape(-1, 5)
+        return oracle.enumerate_direct(p.seq_lens, p.page_size, p.Hkv)
     return oracle.enumerate_queue(p.seq_lens, p.page_size, p.Hkv, C)

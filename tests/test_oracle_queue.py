@@ -16,11 +16,13 @@ GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 
 
 def _golden_queues():
-    rows = [list(map(int, line.split())) for line in open(os.path.join(GOLDEN, "tiny_queue.txt"))
-            if line.strip() and not line.startswith("#")]
+    """{S: tiles} of the split queues and {"direct": tiles} of the single-pass route."""
     out = {}
-    for S, *tile in rows:
-        out.setdefault(S, []).append(tile)
+    for line in open(os.path.join(GOLDEN, "tiny_queue.txt")):
+        if not line.strip() or line.startswith("#"):
+            continue
+        key, *tile = line.split()
+        out.setdefault(key if key == "direct" else int(key), []).append(list(map(int, tile)))
     return out
 
 
@@ -30,6 +32,34 @@ def test_tiny_queue_matches_hand_derivation(S):
     C = oracle.chunk_pages_for_splits(p.seq_lens, p.page_size, S)
     got = oracle.enumerate_queue(p.seq_lens, p.page_size, p.Hkv, C)
     assert got.tolist() == _golden_queues()[S]
+
+
+def test_tiny_direct_tiles_match_hand_derivation():
+    p = wl.tiny()
+    got = oracle.enumerate_direct(p.seq_lens, p.page_size, p.Hkv)
+    assert got.tolist() == _golden_queues()["direct"]
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_direct_tiles_cover_every_row_once(seed):
+    """One tile per (b, kvh) in (b, kvh) order, split 0, pages [0, P_b) with P_b
+    counted by brute force over the tokens; empty rows keep their (empty) tile."""
+    rng = np.random.default_rng(100 + seed)
+    B, Hkv, ps = int(rng.integers(1, 7)), int(rng.integers(1, 5)), int(rng.choice([1, 16, 64]))
+    lens = rng.integers(0, 300, size=B)
+    lens[0] = 0
+    d = oracle.enumerate_direct(lens, ps, Hkv)
+    assert d.shape == (B * Hkv, 5)
+    i = 0
+    for b, n in enumerate(lens):
+        pages = len({t // ps for t in range(int(n))})
+        for kvh in range(Hkv):
+            assert d[i].tolist() == [b, kvh, 0, 0, pages]
+            i += 1
+    # with one chunk covering every row, the compact queue is the direct list minus empty rows
+    C = max(1, int(d[:, 4].max()))
+    q = oracle.enumerate_queue(lens, ps, Hkv, C)
+    assert q.tolist() == d[d[:, 4] > 0].tolist()
 
 
 def _check_queue_properties(lens, ps, Hkv, C):
