@@ -1,25 +1,38 @@
 """Benchmark: paged GQA decode attention on one GB300.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl pkv|reference]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--repeats R] [--workload NAME] [--impl pkv|reference]
+    python bench.py --trace-study [--calibrate]
 
 Default workload: batch-1 long context (1 x 32768 tokens, 32 query / 8 KV heads,
 D 128, 16-token pages scattered over a 4096-page pool, 32 splits).  One step is
 one pkv_decode: the split-partial kernel over the compact queue with the LSE
 merge fused into its last-arriving splits.  Metric: KV-read GB/s (KV bytes of
 the step / device time of the step) and µs per step; roofline fraction against
-the measured HBM copy bandwidth.
+the measured HBM copy bandwidth.  The same JSON line also carries, under
+"workloads", the mixed batch (8 rows, log-uniform lengths), the high batch
+(64 x 4096) and the continuous sessions (56 sessions, 200 steps of append +
+re-plan + decode, p50 / p99), each gated on the fp64 oracle first and sampled
+for clocks on its own (--headline-only leaves them out).
 
 Timing rules: parity against the fp64 oracle before any timing; W >= 3 warm-up
-steps; clocks sampled with nvidia-smi during the timed region.  The K timed
-steps run back to back between one pair of CUDA events on the launching
-stream, on cold inputs: R copies of the page pool and q are used round robin,
-with R chosen so that at least 6 x L2 bytes are read between two reads of the
-same copy (a step that is itself over 6 x L2 needs no copy).  Steps too small
-for that (the tiny case) are timed one by one after an L2 flush (a 2 x L2-size
-buffer written).  Each step is also timed alone, after a flush, between its own
-events ("isolated_us_per_step"), which adds the launch latency to every step.  Multi-GPU (torchrun, one rank per GPU)
+steps; clocks sampled with nvidia-smi during the timed region.  The timed
+region is K steps back to back between one pair of CUDA events on the
+launching stream, repeated R times; the line gives the median per-step time of
+the R regions and their min and max.  Inputs are cold: R copies of the page
+pool and q are used round robin, with R chosen so that at least 6 x L2 bytes
+are read between two reads of the same copy (a step that is itself over 6 x L2
+needs no copy).  Steps too small for that (the tiny case) are timed one by one
+after an L2 flush (a 2 x L2-size buffer written).  Each step is also timed
+alone, after a flush, between its own events ("isolated_us_per_step"), which
+adds the launch latency to every step.  Multi-GPU (torchrun, one rank per GPU)
 runs independent replicas of the workload, partitioned by sequence: no
 collective on the data path, a barrier and max-over-ranks timing only.
+
+--workload trace:<kind>:<B> times one batch of a PersistentKV trace family
+(uniform, bimodal, zipf, bucketed) on the policy's route.  --trace-study runs
+every family at B = 1, 4, 8 on every route (each batch parity-gated), with the
+summary's scheduler counters; --calibrate first fits the policy thresholds on
+the calibration seed.
 
 --impl reference times the fp64 CPU oracle on the host cores on the same
 workload and metric (a bounded sample per step).
@@ -167,8 +180,25 @@ class ClockSampler:
 
 # ----------------------------------------------------------------------------- workloads
 
-def build_workload(name: str):
+WORKLOAD_NAMES = ("batch1_long", "mixed", "mixed_padded", "high_batch", "tiny", "continuous")
+
+
+def parse_trace_name(name: str):
+    """'trace:<kind>:<B>' -> (kind, B); None for the named workloads."""
     from paged_kv_decode_block_gb300 import workloads as wl
+    if not name.startswith("trace:"):
+        return None
+    parts = name.split(":")
+    if len(parts) != 3 or parts[1] not in wl.TRACE_KINDS or not parts[2].isdigit() or int(parts[2]) < 1:
+        raise ValueError(f"bad trace workload {name!r}: want trace:<{'|'.join(wl.TRACE_KINDS)}>:<batch>")
+    return parts[1], int(parts[2])
+
+
+def build_workload(name: str, seed: int | None = None):
+    from paged_kv_decode_block_gb300 import workloads as wl
+    tr = parse_trace_name(name)
+    if tr is not None:   # a trace-family batch on the policy's own route
+        return wl.trace(tr[0], tr[1], wl.HELD_OUT_SEED if seed is None else seed), dict()
     makers = {"batch1_long": (wl.batch1_long, dict(force_mode="split_queue", num_splits=32)),
               "mixed": (wl.mixed, dict(force_mode="split_queue")),
               "mixed_padded": (wl.mixed, dict(force_mode="split_padded")),
@@ -176,7 +206,7 @@ def build_workload(name: str):
               "tiny": (wl.tiny, dict(force_mode="split_queue", num_splits=4)),
               "continuous": (wl.continuous, dict(force_mode="persistent", num_splits=1))}
     make, opts = makers[name]
-    return make(), opts
+    return (make() if seed is None else make(seed)), opts
 
 
 def workload_config(p, name: str, world: int = 1) -> dict:
@@ -247,31 +277,34 @@ def single_thread_oracle(p, kv_bytes: int, estimate_s: float, limit_s: float = 1
 
 # ----------------------------------------------------------------------------- our arm
 
-def run_pkv(args):
+def device_problem(p, dev):
+    """The problem's inputs in device memory, plus fp32 outputs."""
     import torch
-    import torch.distributed as dist
+    return dict(q=torch.from_numpy(p.q.view(np.int16)).to(dev),
+                k=torch.from_numpy(p.k_pages.view(np.int16)).to(dev),
+                v=torch.from_numpy(p.v_pages.view(np.int16)).to(dev),
+                table=torch.from_numpy(p.block_table).to(dev),
+                lens=torch.from_numpy(p.seq_lens).to(dev),
+                out=torch.empty((p.B, p.Hq, p.D), dtype=torch.float32, device=dev),
+                lse=torch.empty((p.B, p.Hq), dtype=torch.float32, device=dev))
+
+
+def decode_line(name, args, ctx, headline=True):
+    """Parity-gate, then time, pkv_decode on one workload; returns its JSON dict.
+    headline=False gives the compact form carried inside the headline line's
+    `workloads` object (no e2e, no CPU baseline, no isolated per-kernel split)."""
+    import torch
     from paged_kv_decode_block_gb300 import pkv
 
-    rank, world, local = dist_env()
-    if world > 1:
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    pkv.load()
-
-    p, opts = build_workload(args.workload)
+    dist, dev, world, rank, local = ctx["dist"], ctx["dev"], ctx["world"], ctx["rank"], ctx["local"]
+    p, opts = build_workload(name)
     opts = dict(opts, math=args.math, separate_merge=args.separate_merge, copy=args.copy, merge=args.merge)
-    if args.num_splits is not None:
+    if headline and args.num_splits is not None:
         opts["num_splits"] = args.num_splits
-    if args.mode is not None:
+    if headline and args.mode is not None:
         opts["force_mode"] = args.mode
-    q = torch.from_numpy(p.q.view(np.int16)).to(dev)
-    k = torch.from_numpy(p.k_pages.view(np.int16)).to(dev)
-    v = torch.from_numpy(p.v_pages.view(np.int16)).to(dev)
-    table = torch.from_numpy(p.block_table).to(dev)
-    lens = torch.from_numpy(p.seq_lens).to(dev)
-    out = torch.empty((p.B, p.Hq, p.D), dtype=torch.float32, device=dev)
-    lse = torch.empty((p.B, p.Hq), dtype=torch.float32, device=dev)
+    d = device_problem(p, dev)
+    q, k, v, table, lens, out, lse = (d[x] for x in ("q", "k", "v", "table", "lens", "out", "lse"))
     plan = pkv.Plan(p.seq_lens, p.block_table, p.page_size, B=p.B, Hq=p.Hq, Hkv=p.Hkv, D=p.D,
                     max_pages=p.max_pages, num_pages=p.num_pages, **opts)
     info = plan.info()
@@ -281,11 +314,11 @@ def run_pkv(args):
     pkv.decode(q, k, v, table, lens, plan, out, lse)
     torch.cuda.synchronize()
     if plan.status() != 0:
-        raise SystemExit("device status word set on the parity run")
+        raise SystemExit(f"{name}: device status word set on the parity run")
     ok, err_out, err_lse = parity_gate(p, out.cpu().numpy(), lse.cpu().numpy(), host_cores())
-    log(f"parity vs oracle: max|out|={err_out:.3g} max|lse|={err_lse:.3g} -> {'ok' if ok else 'FAIL'}")
+    log(f"{name}: parity vs oracle: max|out|={err_out:.3g} max|lse|={err_lse:.3g} -> {'ok' if ok else 'FAIL'}")
     if not ok:
-        raise SystemExit("parity gate failed; not timing")
+        raise SystemExit(f"{name}: parity gate failed; not timing")
 
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
@@ -315,18 +348,21 @@ def run_pkv(args):
         step(i)
     torch.cuda.synchronize()
 
-    # (1) the timed region: K steps back to back on cold copies (or, when the
-    # step is too small for that, with an L2 flush before every step)
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    # (1) the timed region, repeated: K steps back to back on cold copies between
+    # one event pair (or, when the step is too small for that, with an L2 flush
+    # before every step, each step between its own events)
+    K, R = args.steps, args.repeats
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(R)]
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    region_ms = []
     with ClockSampler(smi_index(local)) as clk:
         time.sleep(0.3)
-        # a one-second soak of the same steps right before the timed region, so
-        # that the 200 ms clock samples see the GPU under this load
+        # a soak of the same steps right before the timed region, so that the
+        # 200 ms clock samples see the GPU under this load
         t_soak = time.perf_counter()
         i = 0
-        while time.perf_counter() - t_soak < 1.0:
+        while time.perf_counter() - t_soak < args.soak:
             for _ in range(100):
                 step(i)
                 i += 1
@@ -335,39 +371,41 @@ def run_pkv(args):
             dist.barrier()
         torch.cuda.synchronize()
         t_wall0 = time.perf_counter()
-        if streamed:
-            ev0.record(stream)
-            for i in range(args.steps):
-                step(i)
-            ev1.record(stream)
-        else:
-            for i in range(args.steps):
-                flush.zero_()
-                starts[i].record(stream)
-                step(i)
-                ends[i].record(stream)
+        for r in range(R):
+            if streamed:
+                ev[r][0].record(stream)
+                for i in range(K):
+                    step(r * K + i)
+                ev[r][1].record(stream)
+            else:
+                for i in range(K):
+                    flush.zero_()
+                    starts[i].record(stream)
+                    step(i)
+                    ends[i].record(stream)
+                torch.cuda.synchronize()
+                region_ms.append(statistics.median(s.elapsed_time(e) for s, e in zip(starts, ends)))
         torch.cuda.synchronize()
         if world > 1:
             dist.barrier()
         t_wall = time.perf_counter() - t_wall0
         time.sleep(0.3)
     if streamed:
-        med_ms = ev0.elapsed_time(ev1) / args.steps
-    else:
-        med_ms = statistics.median(s.elapsed_time(e) for s, e in zip(starts, ends))
+        region_ms = [a.elapsed_time(b) / K for a, b in ev]
+    med_ms = statistics.median(region_ms)
 
     # (2) for reference: every step alone, after an L2 flush, between its own
     # events (adds the launch latency to each step); per-kernel events when the
     # step has two launches
     plan.profile(per_kernel_events)
     iso_ms, kernel_ms = [], []
-    for i in range(max(args.steps, 5)):
+    for i in range(max(min(K, 50), 5)):
         flush.zero_()
-        starts[i % args.steps].record(stream)
+        starts[i % K].record(stream)
         step(i)
-        ends[i % args.steps].record(stream)
-        ends[i % args.steps].synchronize()
-        iso_ms.append(starts[i % args.steps].elapsed_time(ends[i % args.steps]))
+        ends[i % K].record(stream)
+        ends[i % K].synchronize()
+        iso_ms.append(starts[i % K].elapsed_time(ends[i % K]))
         if per_kernel_events:
             kernel_ms.append(plan.profile_read())
     plan.profile(False)
@@ -379,8 +417,8 @@ def run_pkv(args):
         attn_ms = med_ms
         merge_ms = 0.0
 
-    med_ms, attn_ms, iso_med = reduce_max([med_ms, attn_ms, iso_med], dist, dev)
-
+    med_ms, attn_ms, iso_med, lo_ms, hi_ms = reduce_max([med_ms, attn_ms, iso_med, min(region_ms), max(region_ms)],
+                                                        dist, dev)
     kv = info["kv_bytes"]
     q_bytes = p.B * p.Hq * p.D * 2
     o_bytes = p.B * p.Hq * (p.D + 1) * 4
@@ -388,6 +426,27 @@ def run_pkv(args):
     value = kv * world / (med_ms * 1e-3) / 1e9
     peak, peak_src = hbm_peak()
     achieved = alg_bytes_attn / (attn_ms * 1e-3) / 1e9
+    clocks = clk.summary()
+    clocks = {"sm_mhz": clocks["sm_mhz"], "sm_max_mhz": clocks["sm_max_mhz"], "reasons": clocks["reasons"],
+              "samples": clocks["samples"]}
+    us = {"median": round(med_ms * 1e3, 2), "min": round(lo_ms * 1e3, 2), "max": round(hi_ms * 1e3, 2),
+          "repeats": R, "steps_per_repeat": K}
+    l2_words = (f"cold: {rot} copies of the page pool and q used round robin, >= 6 x L2 bytes read between "
+                f"two reads of a copy; {R} repeats of {K} steps back to back, one event pair each"
+                if streamed else f"flushed before every timed step (2 x L2 bytes written); {R} repeats of "
+                                 f"{K} steps, median step of each")
+    roofline = {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
+                "frac": round(achieved / peak, 4), "peak_source": peak_src,
+                "kernel": f"attention_kernel ({route_words(info)})",
+                "algorithmic_bytes_per_launch": alg_bytes_attn, "traffic": profiled_traffic(name)}
+    if not headline:
+        return {"workload": p.name, "mode": info["mode_name"], "merge": info["merge_name"],
+                "tiles": info["num_work_items"], "chunk_pages": info["chunk_pages"],
+                "kv_bytes_per_step": kv, "us_per_step": us, "isolated_us_per_step": round(iso_med * 1e3, 2),
+                "kv_gbs": round(value, 2), "frac_of_measured": round(value / peak, 4),
+                "frac_of_nominal_7_9TBs": round(value / NOMINAL_HBM_GBS, 4), "roofline": roofline,
+                "l2": l2_words, "clocks": clocks,
+                "parity": {"max_abs_out": err_out, "max_abs_lse": err_lse}}
 
     # end to end through the C ABI with host buffers: host re-plan, then
     # pkv_decode_host, which synchronises: the kernel reads the new plan and q in
@@ -397,7 +456,7 @@ def run_pkv(args):
     out_host = torch.empty(out.shape, dtype=torch.float32).pin_memory()
     lse_host = torch.empty(lse.shape, dtype=torch.float32).pin_memory()
     e2e_s = []
-    for i in range(args.warmup + args.steps):
+    for i in range(args.warmup + K):
         flush.zero_()
         torch.cuda.synchronize()
         t0 = time.perf_counter()
@@ -420,52 +479,86 @@ def run_pkv(args):
                          f"{sec * 1e3:.0f} ms per step"}
         cpu["single_thread"] = single_thread_oracle(p, kv, sec * cores)
 
-    clocks = clk.summary()
-    line = {
+    return {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(med_ms, 5),
-        "us_per_step": round(med_ms * 1e3, 2), "higher_is_better": True, "scaling": "weak",
+        "steps": K, "warmup": args.warmup, "ms_per_step": round(med_ms, 5),
+        "us_per_step": round(med_ms * 1e3, 2), "us_per_step_spread": us,
+        "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16 in, fp32 accumulate", "data": "synthetic (seeded, bf16 ~N(0,1))",
-        "config": {**workload_config(p, args.workload, world),
+        "config": {**workload_config(p, name, world),
                    "mode": info["mode_name"], "math": args.math, "copy": args.copy,
                    "merge": info["merge_name"],
                    "num_splits": info["max_splits"],
                    "chunk_pages": info["chunk_pages"], "tiles": info["num_work_items"],
                    "empty_tiles": info["empty_tiles"], "merge_state_bytes": info["workspace_bytes"],
-                   "launches_per_step": info["launches_per_step"],
-                   "l2": (f"cold: {rot} copies of the page pool and q used round robin, >= 6 x L2 bytes "
-                          f"read between two reads of a copy; steps back to back, one event pair"
-                          if streamed else "flushed before every timed step (2 x L2 bytes written)")},
+                   "launches_per_step": info["launches_per_step"], "l2": l2_words},
         "kv_bytes_per_step": kv,
         "isolated_us_per_step": round(iso_med * 1e3, 2),
         "frac_of_nominal_7_9TBs": round(value / NOMINAL_HBM_GBS, 4),
         "kernel_ms": {"attention": round(attn_ms, 5), "merge": round(merge_ms, 5)},
-        "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
-                     "frac": round(achieved / peak, 4), "peak_source": peak_src,
-                     "kernel": f"attention_kernel ({route_words(info)})",
-                     "algorithmic_bytes_per_launch": alg_bytes_attn,
-                     "traffic": profiled_traffic(args.workload)},
+        "roofline": roofline,
         "e2e": {"value": round(kv * world / e2e_med / 1e9, 2), "unit": "GB/s",
                 "us_per_step": round(e2e_med * 1e6, 2), "h2d_bytes_per_step": q_bytes + upload,
                 "d2h_bytes_per_step": o_bytes,
                 "path": "host re-plan + pkv_decode_host: the kernel reads the plan and q from pinned host "
                         "memory and writes out/lse to pinned host memory (NVLink-C2C), then a synchronise"},
-        "gpu_launches": n_launch * args.steps,
+        "gpu_launches": n_launch * K * R,
         "cpu_baseline": cpu,
-        "clocks": {"sm_mhz": clocks["sm_mhz"], "sm_max_mhz": clocks["sm_max_mhz"],
-                   "reasons": clocks["reasons"], "samples": clocks["samples"]},
+        "clocks": clocks,
         "timed_region_wall_s": round(t_wall, 4),
         "parity": {"max_abs_out": err_out, "max_abs_lse": err_lse},
     }
-    if rank == 0:
+
+
+def dist_context(args):
+    import torch
+    import torch.distributed as dist
+    rank, world, local = dist_env()
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    return {"dist": dist, "dev": torch.device("cuda", local), "world": world, "rank": rank, "local": local}
+
+
+def release_memory():
+    import gc
+    import torch
+    gc.collect()
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+
+
+# the other workloads the headline line carries (each parity-gated, with its own clocks)
+SIDE_WORKLOADS = ("mixed", "high_batch", "continuous")
+
+
+def run_pkv(args):
+    from paged_kv_decode_block_gb300 import pkv
+
+    ctx = dist_context(args)
+    pkv.load()
+    line = decode_line(args.workload, args, ctx)
+    if args.workload == "batch1_long" and not args.headline_only:
+        side = {}
+        for name in SIDE_WORKLOADS:
+            release_memory()
+            if name == "continuous":
+                side[name] = continuous_line(args, ctx, steps=200, warmup=max(args.warmup, 5), headline=False)
+            else:
+                side[name] = decode_line(name, args, ctx, headline=False)
+        line["workloads"] = side
+        line["gpu_launches"] += sum(w.get("gpu_launches", 0) for w in side.values())
+        for w in side.values():
+            w.pop("gpu_launches", None)
+    if ctx["rank"] == 0:
         print(json.dumps(line), flush=True)
-    if world > 1:
-        dist.destroy_process_group()
+    if ctx["world"] > 1:
+        ctx["dist"].destroy_process_group()
 
 
 # ----------------------------------------------------------------------------- continuous sessions
 
-def run_continuous(args):
+def continuous_line(args, ctx, steps=None, warmup=None, headline=True):
     """56 sessions; every step appends one K/V token per session (a fresh page from
     the pool when one fills), re-plans on the host and decodes with the persistent
     queue kernel.  Device time per step covers append + host re-plan + decode (the
@@ -477,14 +570,15 @@ def run_continuous(args):
     from paged_kv_decode_block_gb300 import workloads as wl
     from paged_kv_decode_block_gb300.session import ContinuousSessions
 
-    rank, world, local = dist_env()
-    torch.cuda.set_device(local)
-    pkv.load()
-    steps = args.steps
-    total = args.warmup + steps
+    local = ctx["local"]
+    steps = args.steps if steps is None else steps
+    warmup = args.warmup if warmup is None else warmup
+    total = warmup + steps
     e2e_steps = min(8, steps)
     p = wl.continuous(steps=total + e2e_steps + 1)   # room for every appended token (e2e and profiling steps too)
-    splits = 1 if args.num_splits is None else args.num_splits
+    splits = 1 if (args.num_splits is None or not headline) else args.num_splits
+    device_plan = headline and (args.device_plan or args.graph)
+    use_graph = headline and args.graph
     sess = ContinuousSessions(p, force_mode="persistent", num_splits=splits, math=args.math, copy=args.copy)
     rng = np.random.default_rng(wl.HELD_OUT_SEED + 1)
     toks = [wl.new_tokens(rng, p.B, p.Hkv, p.D) for _ in range(total)]
@@ -496,7 +590,7 @@ def run_continuous(args):
     sess.step(k_new[0], v_new[0])
     torch.cuda.synchronize()
     if sess.plan.status() != 0:
-        raise SystemExit("device status word set on the parity step")
+        raise SystemExit("continuous: device status word set on the parity step")
     import oracle
     table0 = sess.table_h.copy()
     k0, v0, lens0 = oracle.append(toks[0][0], toks[0][1], p.k_pages, p.v_pages, table0, p.seq_lens)
@@ -504,11 +598,11 @@ def run_continuous(args):
     del k0, v0
     err_out = float(np.max(np.abs(sess.out.cpu().numpy() - ref_out)))
     err_lse = float(np.max(np.abs(sess.lse.cpu().numpy() - ref_lse)))
-    log(f"parity vs oracle (step 0): max|out|={err_out:.3g} max|lse|={err_lse:.3g}")
+    log(f"continuous: parity vs oracle (step 0): max|out|={err_out:.3g} max|lse|={err_lse:.3g}")
     if err_out > 2e-3 or err_lse > 1e-4:
-        raise SystemExit("parity gate failed; not timing")
+        raise SystemExit("continuous: parity gate failed; not timing")
 
-    if args.device_plan or args.graph:
+    if device_plan:
         sess.session.device_plan()
     kbuf = torch.empty_like(k_new[0])
     vbuf = torch.empty_like(v_new[0])
@@ -522,10 +616,10 @@ def run_continuous(args):
             vbuf.copy_(v_new[i])
             graph.replay()
 
-    for i in range(1, args.warmup):
+    for i in range(1, warmup):
         one_step(i)
     torch.cuda.synchronize()
-    if args.graph:
+    if use_graph:
         side = torch.cuda.Stream()
         side.wait_stream(stream)
         graph = torch.cuda.CUDAGraph()
@@ -535,13 +629,13 @@ def run_continuous(args):
         stream.wait_stream(side)
         # capturing enqueued nothing; the lengths still match the host's count
     lens0 = sess.lens_h.astype(np.int64).sum()
-    sess.plan.profile(not args.graph)
+    sess.plan.profile(not use_graph)
     dev_us, wall_us, kv, attn_ms = [], [], [], []
     with ClockSampler(smi_index(local)) as clk:
         time.sleep(0.3)
         torch.cuda.synchronize()
         t_region = time.perf_counter()
-        for n, i in enumerate(range(args.warmup, total)):
+        for n, i in enumerate(range(warmup, total)):
             a = torch.cuda.Event(enable_timing=True)
             b = torch.cuda.Event(enable_timing=True)
             t0 = time.perf_counter()
@@ -551,13 +645,13 @@ def run_continuous(args):
             b.synchronize()
             wall_us.append((time.perf_counter() - t0) * 1e6)
             dev_us.append(a.elapsed_time(b) * 1e3)
-            if not args.graph:
+            if not use_graph:
                 attn_ms.append(sess.plan.profile_read()[0])
             kv.append(int(lens0 + (n + 1) * p.B) * p.Hkv * p.D * 4)
         t_region = time.perf_counter() - t_region
         time.sleep(0.3)
     sess.plan.profile(False)
-    if args.graph:   # kernel time of the attention launch, from one more profiled eager step
+    if use_graph:   # kernel time of the attention launch, from one more profiled eager step
         sess.plan.profile(True)
         torch.cuda.synchronize()
         sess.step(k_new[total - 1], v_new[total - 1])
@@ -566,8 +660,33 @@ def run_continuous(args):
     kv_total = float(np.sum(kv))
     value = kv_total / (np.sum(dev_us) * 1e-6) / 1e9
     peak, peak_src = hbm_peak()
-    achieved = float(np.mean([(k + p.B * p.Hq * p.D * 2) / (t * 1e-3) / 1e9 for k, t in zip(kv, attn_ms)]))
+    q_bytes = p.B * p.Hq * p.D * 2
+    achieved = float(np.mean([(k + q_bytes) / (t * 1e-3) / 1e9 for k, t in zip(kv, attn_ms)]))
     clocks = clk.summary()
+    clocks = {"sm_mhz": clocks["sm_mhz"], "sm_max_mhz": clocks["sm_max_mhz"], "reasons": clocks["reasons"],
+              "samples": clocks["samples"]}
+    p50, p99 = float(np.percentile(dev_us, 50)), float(np.percentile(dev_us, 99))
+    info = sess.plan.info()
+    launches = 1 + info["launches_per_step"] + (1 if device_plan else 0)
+    roofline = {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
+                "frac": round(achieved / peak, 4), "peak_source": peak_src,
+                "kernel": "attention_kernel (persistent queue drain)",
+                "algorithmic_bytes_per_launch": int(np.mean(kv)) + q_bytes,
+                "traffic": profiled_traffic("continuous")}
+    step_words = ("CUDA-graph replay of device plan + append + persistent decode" if use_graph else
+                  "device plan + append + persistent decode" if device_plan else
+                  "append + host re-plan + persistent decode")
+    if not headline:
+        return {"workload": p.name, "mode": info["mode_name"], "sessions": p.B, "steps": steps,
+                "step": step_words, "tiles": info["num_work_items"], "kv_bytes_per_step": int(np.mean(kv)),
+                "us_per_step": {"device_p50": round(p50, 2), "device_p99": round(p99, 2),
+                                "wall_p50": round(float(np.percentile(wall_us, 50)), 2),
+                                "wall_p99": round(float(np.percentile(wall_us, 99)), 2),
+                                "decode_kernel_mean": round(float(np.mean(attn_ms)) * 1e3, 2)},
+                "decode_frac_of_measured": round(achieved / peak, 4),
+                "step_frac_of_measured": round(float(np.mean(kv)) / (p50 * 1e-6) / 1e9 / peak, 4),
+                "roofline": roofline, "clocks": clocks, "gpu_launches": launches * steps,
+                "parity": {"max_abs_out": err_out, "max_abs_lse": err_lse, "checked_step": 0}}
 
     # end to end: new tokens and q from pinned host memory each step, outputs back to the host
     kh = torch.from_numpy(np.stack([t[0] for t in toks[:8]]).view(np.int16)).pin_memory()
@@ -590,12 +709,10 @@ def run_continuous(args):
         e2e.append(time.perf_counter() - t0)
     e2e_med = statistics.median(e2e)
 
-    info = sess.plan.info()
-    line = {
-        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": steps,
-        "warmup": args.warmup, "ms_per_step": round(statistics.median(dev_us) / 1e3, 5),
-        "us_per_step": {"device_p50": round(float(np.percentile(dev_us, 50)), 2),
-                        "device_p99": round(float(np.percentile(dev_us, 99)), 2),
+    return {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": ctx["world"], "steps": steps,
+        "warmup": warmup, "ms_per_step": round(p50 / 1e3, 5),
+        "us_per_step": {"device_p50": round(p50, 2), "device_p99": round(p99, 2),
                         "wall_p50": round(float(np.percentile(wall_us, 50)), 2),
                         "wall_p99": round(float(np.percentile(wall_us, 99)), 2)},
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
@@ -604,31 +721,29 @@ def run_continuous(args):
                    "q_heads": p.Hq, "kv_heads": p.Hkv, "head_dim": p.D, "page_size": p.page_size,
                    "num_pages": p.num_pages, "mode": info["mode_name"], "math": args.math, "copy": args.copy,
                    "num_splits": info["max_splits"], "tiles": info["num_work_items"],
-                   "grid_ctas": info["grid_ctas"],
-                   "launches_per_step": 1 + info["launches_per_step"] + (1 if args.device_plan or args.graph else 0),
-                   "l2": "not flushed: each step reads ~1 GB of KV, far above L2",
-                   "step": ("CUDA-graph replay of device plan + append + persistent decode" if args.graph else
-                            "device plan + append + persistent decode" if args.device_plan else
-                            "append + host re-plan + persistent decode")},
+                   "grid_ctas": info["grid_ctas"], "launches_per_step": launches,
+                   "l2": "not flushed: each step reads ~1 GB of KV, far above L2", "step": step_words},
         "kv_bytes_per_step": int(np.mean(kv)),
         "kernel_ms": {"attention_mean": round(float(np.mean(attn_ms)), 5)},
-        "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
-                     "frac": round(achieved / peak, 4), "peak_source": peak_src,
-                     "kernel": "attention_kernel (persistent queue drain)",
-                     "algorithmic_bytes_per_launch": int(np.mean(kv)) + p.B * p.Hq * p.D * 2,
-                     "traffic": profiled_traffic(args.workload)},
+        "roofline": roofline,
         "e2e": {"value": round(float(np.mean(kv)) / e2e_med / 1e9, 2), "unit": "GB/s",
                 "us_per_step": round(e2e_med * 1e6, 2),
-                "h2d_bytes_per_step": 2 * p.B * p.Hkv * p.D * 2 + p.B * p.Hq * p.D * 2,
+                "h2d_bytes_per_step": 2 * p.B * p.Hkv * p.D * 2 + q_bytes,
                 "d2h_bytes_per_step": p.B * p.Hq * (p.D + 1) * 4},
-        "gpu_launches": (1 + info["launches_per_step"] + (1 if args.device_plan or args.graph else 0)) * steps,
+        "gpu_launches": launches * steps,
         "cpu_baseline": None,
-        "clocks": {"sm_mhz": clocks["sm_mhz"], "sm_max_mhz": clocks["sm_max_mhz"],
-                   "reasons": clocks["reasons"], "samples": clocks["samples"]},
+        "clocks": clocks,
         "timed_region_wall_s": round(t_region, 4),
         "parity": {"max_abs_out": err_out, "max_abs_lse": err_lse, "checked_step": 0},
     }
-    if rank == 0:
+
+
+def run_continuous(args):
+    from paged_kv_decode_block_gb300 import pkv
+    ctx = dist_context(args)
+    pkv.load()
+    line = continuous_line(args, ctx)
+    if ctx["rank"] == 0:
         print(json.dumps(line), flush=True)
 
 
@@ -749,6 +864,129 @@ def run_resident(args):
         print(json.dumps(line), flush=True)
 
 
+# ----------------------------------------------------------------------------- trace-family study
+
+STUDY_ROUTES = ("auto", "split_queue", "split_padded", "direct", "persistent")
+STUDY_BATCHES = (1, 4, 8)
+
+
+def _study_time_route(p, dev, route, policy, steps, flush):
+    """Median device µs of one pkv_decode on `route`, each step alone after an L2 flush."""
+    import torch
+    from paged_kv_decode_block_gb300 import pkv
+    opts = dict(policy)
+    if route != "auto":
+        opts["force_mode"] = route
+    plan = pkv.Plan(p.seq_lens, p.block_table, p.page_size, B=p.B, Hq=p.Hq, Hkv=p.Hkv, D=p.D,
+                    max_pages=p.max_pages, num_pages=p.num_pages, **opts)
+    stream = torch.cuda.current_stream()
+    for _ in range(3):
+        flush.zero_()
+        pkv.decode(dev["q"], dev["k"], dev["v"], dev["table"], dev["lens"], plan, dev["out"], dev["lse"])
+    ts = []
+    for _ in range(steps):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        pkv.decode(dev["q"], dev["k"], dev["v"], dev["table"], dev["lens"], plan, dev["out"], dev["lse"])
+        b.record(stream)
+        b.synchronize()
+        ts.append(a.elapsed_time(b) * 1e3)
+    if plan.status() != 0:
+        raise SystemExit(f"device status set ({p.name}, {route})")
+    info = plan.info()
+    plan.close()
+    return statistics.median(ts), info
+
+
+def _study_parity(p, dev, policy):
+    """The policy route against the oracle (exits on a mismatch)."""
+    from paged_kv_decode_block_gb300 import pkv
+    plan = pkv.Plan(p.seq_lens, p.block_table, p.page_size, B=p.B, Hq=p.Hq, Hkv=p.Hkv, D=p.D,
+                    max_pages=p.max_pages, num_pages=p.num_pages, **policy)
+    pkv.decode(dev["q"], dev["k"], dev["v"], dev["table"], dev["lens"], plan, dev["out"], dev["lse"])
+    ok, err_out, err_lse = parity_gate(p, dev["out"].cpu().numpy(), dev["lse"].cpu().numpy(), host_cores())
+    plan.close()
+    if not ok:
+        raise SystemExit(f"parity failed on {p.name}: {err_out}, {err_lse}")
+    return err_out, err_lse
+
+
+def trace_study(seed, policy, steps, dev, routes=STUDY_ROUTES, batches=STUDY_BATCHES, emit=print):
+    """Every trace family at every batch size: parity of the policy route, then the
+    step time of every route, with the PersistentKV summary's scheduler counters
+    (launches per step against 2 per distinct length for exact-length buckets,
+    tiles, empty tiles of the padded grid, merge-state bytes)."""
+    import torch
+    from paged_kv_decode_block_gb300 import workloads as wl
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    rows = []
+    for kind in wl.TRACE_KINDS:
+        for B in batches:
+            p = wl.trace(kind, B, seed)
+            d = device_problem(p, dev)
+            errs = _study_parity(p, d, policy)
+            kv = p.kv_bytes()
+            for route in routes:
+                us, info = _study_time_route(p, d, route, policy, steps, flush)
+                row = dict(seed=seed, trace=kind, batch=B, route=route, mode=info["mode_name"],
+                           us_per_step=round(us, 2), kv_gbs=round(kv / (us * 1e-6) / 1e9, 1),
+                           launches=info["launches_per_step"],
+                           exact_bucket_launches=2 * len(set(int(n) for n in p.seq_lens)),
+                           tiles=info["num_work_items"], empty_tiles=info["empty_tiles"],
+                           chunk_pages=info["chunk_pages"], merge_state_bytes=info["workspace_bytes"],
+                           kv_bytes=kv, lens=[int(n) for n in p.seq_lens], parity_out=errs[0],
+                           parity_lse=errs[1])
+                rows.append(row)
+                emit(json.dumps(row))
+            del d
+            release_memory()
+    return rows
+
+
+def calibrate_policy(seed, steps, dev, emit=print):
+    """Pick (target_ctas_per_sm, min_chunk_pages) minimising the geometric mean of the
+    policy route's step time over every trace family and batch size at `seed` (the
+    summary's calibration seed; thresholds fitted on one seed, reported on the other)."""
+    import itertools
+    import math
+    import torch
+    from paged_kv_decode_block_gb300 import workloads as wl
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    grid = list(itertools.product((1, 2, 3, 4), (4, 8, 16, 32)))
+    scores = {g: [] for g in grid}
+    for kind in wl.TRACE_KINDS:
+        for B in STUDY_BATCHES:
+            p = wl.trace(kind, B, seed)
+            d = device_problem(p, dev)
+            for tc, mc in grid:
+                us, _ = _study_time_route(p, d, "auto", dict(target_ctas_per_sm=tc, min_chunk_pages=mc), steps,
+                                          flush)
+                scores[(tc, mc)].append(us)
+            del d
+            release_memory()
+    geo = {g: math.exp(statistics.mean(math.log(x) for x in v)) for g, v in scores.items()}
+    for g in sorted(geo, key=geo.get):
+        emit(json.dumps(dict(seed=seed, target_ctas_per_sm=g[0], min_chunk_pages=g[1], geomean_us=round(geo[g], 2))))
+    best = min(geo, key=geo.get)
+    return dict(target_ctas_per_sm=best[0], min_chunk_pages=best[1])
+
+
+def run_trace_study(args):
+    """--trace-study [--calibrate]: one JSON row per (trace, batch, route) on stdout."""
+    from paged_kv_decode_block_gb300 import pkv
+    from paged_kv_decode_block_gb300 import workloads as wl
+    ctx = dist_context(args)
+    if ctx["rank"] != 0:
+        return
+    pkv.load()
+    policy = {}
+    if args.calibrate:
+        policy = calibrate_policy(wl.CALIBRATION_SEED, args.study_steps, ctx["dev"])
+        print(json.dumps({"calibration": policy, "seed": wl.CALIBRATION_SEED}), flush=True)
+    trace_study(wl.HELD_OUT_SEED, policy, args.study_steps, ctx["dev"])
+
+
 # ----------------------------------------------------------------------------- reference arm
 
 def run_reference(args):
@@ -785,8 +1023,13 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--repeats", type=int, default=5,
+                    help="timed regions of --steps steps each; the line reports their median, min and max")
+    ap.add_argument("--soak", type=float, default=1.0, help="seconds of untimed steps before each timed region")
     ap.add_argument("--workload", default="batch1_long",
-                    choices=["batch1_long", "mixed", "mixed_padded", "high_batch", "tiny", "continuous"])
+                    help=f"one of {', '.join(WORKLOAD_NAMES)}, or trace:<kind>:<batch>")
+    ap.add_argument("--headline-only", action="store_true",
+                    help="batch1_long: leave out the other workloads the line otherwise carries")
     ap.add_argument("--impl", default="pkv", choices=["pkv", "reference"])
     ap.add_argument("--math", default="auto", choices=["auto", "fma", "mma"],
                     help="block reduction: tensor cores (mma.sync) or CUDA-core FMA")
@@ -809,11 +1052,26 @@ def main():
                     help="copies of the inputs used round robin (default: enough for >= 6 x L2 between reuses)")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time for the CPU baseline")
     ap.add_argument("--skip-cpu", action="store_true")
+    ap.add_argument("--trace-study", action="store_true",
+                    help="every trace family x batch 1/4/8 x route, parity-gated; one JSON row each")
+    ap.add_argument("--calibrate", action="store_true",
+                    help="with --trace-study: fit the policy thresholds on the calibration seed first")
+    ap.add_argument("--study-steps", type=int, default=15, help="timed steps per route in the trace study")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.repeats < 1 or args.steps < 1:
+        ap.error("--repeats and --steps must be >= 1")
+    if args.workload not in WORKLOAD_NAMES:
+        try:
+            if parse_trace_name(args.workload) is None:
+                raise ValueError(f"unknown workload {args.workload!r}")
+        except ValueError as e:
+            ap.error(str(e))
     if args.impl == "reference":
         run_reference(args)
+    elif args.trace_study:
+        run_trace_study(args)
     elif args.workload == "continuous" and args.resident:
         run_resident(args)
     elif args.workload == "continuous":

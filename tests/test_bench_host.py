@@ -66,3 +66,25 @@ def test_parity_gate_passes_the_oracle_and_catches_an_error():
     bad = out.copy()
     bad[1, 2, 3] += 3e-3
     assert not bench.parity_gate(p, bad, lse, 1)[0]
+
+
+def test_trace_workload_names():
+    assert bench.parse_trace_name("batch1_long") is None
+    assert bench.parse_trace_name("trace:zipf:8") == ("zipf", 8)
+    for bad in ("trace:zipf", "trace:normal:4", "trace:uniform:0", "trace:uniform:x"):
+        with pytest.raises(ValueError):
+            bench.parse_trace_name(bad)
+    p, opts = bench.build_workload("trace:bimodal:4")
+    ref = wl.trace("bimodal", 4)
+    assert opts == {} and p.name == "bimodal_b4" and np.array_equal(p.seq_lens, ref.seq_lens)
+
+
+def test_product_package_never_imports_the_oracle():
+    """Only the tests, the smoke entry and bench.py may import oracle/."""
+    pkg = os.path.join(ROOT, "paged_kv_decode_block_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cpp", ".cu", ".cuh", ".h")):
+                text = open(os.path.join(dirpath, f)).read()
+                assert "import oracle" not in text and "from oracle" not in text, f
+                assert "pkv_oracle" not in text, f
