@@ -78,7 +78,10 @@ enum pkv_device_status_bits {
     PKV_DEV_PAGE_OOB = 1u,       /* a block-table entry outside [0, num_pages) */
     PKV_DEV_PLAN_MISMATCH = 2u,  /* the device seq_lens disagree with the plan */
     PKV_DEV_TIMEOUT = 4u,        /* a bounded wait inside a kernel ran out */
-    PKV_DEV_ROW_FULL = 8u        /* pkv_append found no page slot for a row */
+    PKV_DEV_ROW_FULL = 8u        /* an append found no page for a row's new token: the row's
+                                    table is full, or its entry for that position is unassigned
+                                    (negative); an entry naming a page outside the pool sets
+                                    PKV_DEV_PAGE_OOB instead */
 };
 
 /* Execution routes (Methodology section 2 of the PersistentKV summary). */
@@ -247,8 +250,10 @@ int pkv_decode_host(const void *q_h, const void *k_pages, const void *v_pages, c
  * k_new[b][kvh][:] / v_new[b][kvh][:] (device bf16 [B][Hkv][D]) at position
  * seq_lens_d[b] -- page block_table_d[b][pos / page_size], slot
  * pos % page_size -- and then increment seq_lens_d[b].  The page for a new
- * position must already be in the table (see pkv_pool_reserve).  A row with no
- * valid page sets PKV_DEV_ROW_FULL or PKV_DEV_PAGE_OOB and is left unchanged.
+ * position must already be in the table (see pkv_pool_reserve).  A row whose
+ * table is full or whose entry for the position is negative sets
+ * PKV_DEV_ROW_FULL, one whose entry is >= num_pages sets PKV_DEV_PAGE_OOB; such
+ * a row is left unchanged (no page byte written, length not incremented).
  * Only the plan's geometry and page size are used.  One kernel on `stream`.
  */
 int pkv_append(const void *k_new, const void *v_new, void *k_pages, void *v_pages,
@@ -320,17 +325,27 @@ void pkv_pool_destroy(pkv_pool_t pool);
  * that loads the library holds it until the process exits).  It calls no
  * allocating routine.
  *   q, k_pages, v_pages, block_table_d, seq_lens_d, out, lse: as in pkv_decode
- *   max_seq_len  host upper bound on every seq_lens_d[b]; rows longer than it
- *                are poisoned with NaN
- *   num_splits   S; chunk C = ceil(ceil(max_seq_len / page_size) / S) pages
+ *   max_seq_len  host bound on seq_lens_d[b] that sizes the split grid: with
+ *                P = ceil(max_seq_len / page_size) pages and S splits, the chunk
+ *                is C = ceil(P / S) pages (raised if needed so that S_max * G
+ *                stays within the merge's 4096-float scratch) and S_max =
+ *                ceil(P / C) splits cover S_max * C >= P pages per row.  A row
+ *                whose pages fit in S_max * C is decoded exactly, even if it is
+ *                a little longer than max_seq_len; a row with more pages than
+ *                that (or negative, or longer than max_pages_per_seq *
+ *                page_size) reads no KV and gets NaN out and lse
+ *   num_splits   S (> 0)
  * Needs B * Hkv * S_max * G * (D + 1) * 4 bytes of workspace plus a few KB of
- * counters within PKV_STATIC_SCRATCH_BYTES; larger problems get PKV_ENOSPACE.
- * The first call on a device (with that device current) looks the array's
- * device address up with cudaGetSymbolAddress; make that first call before any
- * stream capture.  All calls on a device share the array and it keeps the last
- * call's contents (counters are cleared on `stream` by each call), so calls
- * that overlap on the GPU race: keep them ordered on one stream.  Device-side
- * faults poison outputs with NaN; there is no status read-back.
+ * counters within PKV_STATIC_SCRATCH_BYTES; larger problems get PKV_ENOSPACE
+ * before anything is enqueued.  The first call with a device current looks the
+ * array's device address up with cudaGetSymbolAddress and keeps it for that
+ * device's current context (a device reset brings a new context and a new
+ * look-up); make that first call before any stream capture.  All calls on a
+ * device share the array and it keeps the last call's contents (counters are
+ * cleared on `stream` by each call), so calls that overlap on the GPU race:
+ * keep them ordered on one stream.  Device-side faults poison outputs with NaN;
+ * there is no status read-back.  PKV_ECUDA records the CUDA error for
+ * pkv_last_cuda_error.
  */
 #define PKV_STATIC_SCRATCH_BYTES (8u * 1024u * 1024u)
 int pkv_decode_static(const void *q, const void *k_pages, const void *v_pages, const int32_t *block_table_d,

@@ -39,8 +39,18 @@
 #include "pkv_internal.h"
 
 namespace {
-
 thread_local int g_last_cuda_error = 0;
+}  // namespace
+
+namespace pkv {
+int cuda_fail(cudaError_t e) {
+    g_last_cuda_error = static_cast<int>(e);
+    return PKV_ECUDA;
+}
+}  // namespace pkv
+using pkv::cuda_fail;
+
+namespace {
 
 // An NVTX range over one library call, so that a profiler's timeline shows the
 // host side of each call (planning, staging, launches).  Without a profiler
@@ -52,10 +62,6 @@ struct NvtxRange {
     NvtxRange& operator=(const NvtxRange&) = delete;
 };
 
-int cuda_fail(cudaError_t e) {
-    g_last_cuda_error = static_cast<int>(e);
-    return PKV_ECUDA;
-}
 
 #define PKV_CUDA(call)                                 \
     do {                                               \

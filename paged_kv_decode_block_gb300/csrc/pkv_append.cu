@@ -8,8 +8,9 @@
 // seq_lens[b], then the length grows by one.
 //
 // One CTA per row; each thread moves 16-byte vectors of the row's
-// Hkv * D bf16 K and V values.  A row whose position has no page (table full or
-// entry out of range) sets a status bit and is left unchanged.  The step variant
+// Hkv * D bf16 K and V values.  A row whose position has no page (table full,
+// or the entry unassigned) sets PKV_DEV_ROW_FULL, one whose entry names a page
+// outside the pool sets PKV_DEV_PAGE_OOB; either row is left unchanged.  The step variant
 // (append_step_kernel) also enters the rows' new pages in the table and moves
 // the step's plan from mapped pinned host memory into device memory, so that a
 // host-planned session step needs no copy-engine transfer.
@@ -42,7 +43,10 @@ __device__ __forceinline__ void append_row(const uint16_t* __restrict__ k_new, c
             } else {
                 page = *entry;
             }
-            if (page < 0 || page >= num_pages) {
+            if (page < 0) {   // no page assigned for the new position
+                atomicOr(status, static_cast<uint32_t>(PKV_DEV_ROW_FULL));
+                page = -1;
+            } else if (page >= num_pages) {
                 atomicOr(status, static_cast<uint32_t>(PKV_DEV_PAGE_OOB));
                 page = -1;
             }

@@ -1570,7 +1570,10 @@ __global__ void __launch_bounds__(kThreads, MMA ? 2 : 1) resident_kernel(const R
                     atomicOr(status, static_cast<uint32_t>(PKV_DEV_ROW_FULL));
                 } else {
                     page = p.block_table[static_cast<size_t>(b) * p.max_pages + pos / p.page_size];
-                    if (page < 0 || page >= p.num_pages) {
+                    if (page < 0) {   // no page assigned for the new position
+                        atomicOr(status, static_cast<uint32_t>(PKV_DEV_ROW_FULL));
+                        page = -1;
+                    } else if (page >= p.num_pages) {
                         atomicOr(status, static_cast<uint32_t>(PKV_DEV_PAGE_OOB));
                         page = -1;
                     }

@@ -10,6 +10,10 @@
 
 namespace pkv {
 
+// Record `e` as this thread's last CUDA error (what pkv_last_cuda_error
+// returns) and return PKV_ECUDA.
+int cuda_fail(cudaError_t e);
+
 // Tokens per pipeline stage.  A page of page_size tokens is streamed as
 // page_size / kBlockRows stages; page_size must be a multiple of it.
 constexpr int kBlockRows = 16;

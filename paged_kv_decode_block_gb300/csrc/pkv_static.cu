@@ -11,9 +11,11 @@
 // caller passes only inputs and outputs.
 //
 // Set-up: the array's host-side name is only a stand-in for the device
-// object, so its device address is fetched with cudaGetSymbolAddress, once per
-// device, on the first call made while that device is current.  That first
-// call should therefore come before any stream capture.
+// object, so its device address is fetched with cudaGetSymbolAddress on the
+// first call made while a device is current, and kept for that device's
+// current context (keyed by the context's unique id, so a device reset, which
+// brings a new context and reloads the module, triggers a fresh look-up).  That
+// first call should therefore come before any stream capture.
 //
 // Sharing: every call on a device uses the same array, which keeps the last
 // call's contents.  The counters that must start at zero are cleared on the
@@ -40,7 +42,37 @@ static __device__ __align__(256) uint8_t g_static_scratch[kStaticScratchBytes];
 
 constexpr int kMaxDevices = 64;
 std::mutex g_setup_mutex;
-uint8_t* g_scratch_addr[kMaxDevices] = {};
+struct ScratchAddr {
+    unsigned long long ctx_id;   // unique id of the context the address belongs to (0: none yet)
+    uint8_t* addr;
+};
+ScratchAddr g_scratch_addr[kMaxDevices] = {};
+
+// Unique id of the calling thread's current context (cuCtxGetCurrent +
+// cuCtxGetId, reached through the runtime's driver entry points); 0 if the
+// driver does not provide them.
+unsigned long long current_context_id() {
+    typedef CUresult (*GetCurrentFn)(CUcontext*);
+    typedef CUresult (*GetIdFn)(CUcontext, unsigned long long*);
+    static GetCurrentFn get_current = nullptr;
+    static GetIdFn get_id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<GetCurrentFn>(p);
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<GetIdFn>(p);
+    });
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (!get_current || !get_id || get_current(&ctx) != CUDA_SUCCESS || !ctx || get_id(ctx, &id) != CUDA_SUCCESS)
+        return 0;
+    return id;
+}
 
 size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
 
@@ -95,16 +127,25 @@ extern "C" int pkv_decode_static(const void* q, const void* k_pages, const void*
     if (total > kStaticScratchBytes) return PKV_ENOSPACE;
 
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return PKV_ECUDA;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (dev < 0 || dev >= kMaxDevices) return cuda_fail(cudaErrorInvalidDevice);
     uint8_t* base = nullptr;
     {
+        // the first call with this device current (in this context) looks the
+        // array's device address up; a context without an id is looked up every call
+        const unsigned long long ctx_id = current_context_id();
         std::lock_guard<std::mutex> lock(g_setup_mutex);
-        if (!g_scratch_addr[dev]) {
+        ScratchAddr& slot = g_scratch_addr[dev];
+        if (ctx_id == 0 || slot.ctx_id != ctx_id || !slot.addr) {
             void* addr = nullptr;
-            if (cudaGetSymbolAddress(&addr, g_static_scratch) != cudaSuccess || !addr) return PKV_ECUDA;
-            g_scratch_addr[dev] = static_cast<uint8_t*>(addr);
+            e = cudaGetSymbolAddress(&addr, g_static_scratch);
+            if (e != cudaSuccess) return cuda_fail(e);
+            if (!addr) return cuda_fail(cudaErrorInvalidSymbol);
+            slot.addr = static_cast<uint8_t*>(addr);
+            slot.ctx_id = ctx_id;
         }
-        base = g_scratch_addr[dev];
+        base = slot.addr;
     }
 
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -140,12 +181,20 @@ extern "C" int pkv_decode_static(const void* q, const void* k_pages, const void*
     a.scale_log2 = static_cast<float>(1.4426950408889634 / sqrt(static_cast<double>(D)));
 
     // arrival counters and the status word must start at zero
-    if (cudaMemsetAsync(base, 0, off_rows, s) != cudaSuccess) return PKV_ECUDA;
-    fill_padded_rows<<<1, 256, 0, s>>>(const_cast<int32_t*>(a.row_start), const_cast<int32_t*>(a.row_splits),
-                                       g->batch, g->num_kv_heads, static_cast<int>(s_max));
-    if (cudaGetLastError() != cudaSuccess) return PKV_ECUDA;
+    e = cudaMemsetAsync(base, 0, off_rows, s);
+    if (e != cudaSuccess) return cuda_fail(e);
+    // the launch's own result (an earlier, unrelated error is not picked up here)
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(1);
+    cfg.blockDim = dim3(256);
+    cfg.stream = s;
+    e = cudaLaunchKernelEx(&cfg, fill_padded_rows, const_cast<int32_t*>(a.row_start),
+                           const_cast<int32_t*>(a.row_splits), static_cast<int>(g->batch),
+                           static_cast<int>(g->num_kv_heads), static_cast<int>(s_max));
+    if (e != cudaSuccess) return cuda_fail(e);
     CUtensorMap unused;
     memset(&unused, 0, sizeof(unused));
-    if (launch_attention(a, unused, unused, static_cast<int>(slots), s) != cudaSuccess) return PKV_ECUDA;
+    e = launch_attention(a, unused, unused, static_cast<int>(slots), s);
+    if (e != cudaSuccess) return cuda_fail(e);
     return PKV_OK;
 }
