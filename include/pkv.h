@@ -284,6 +284,28 @@ int pkv_read_workspace(pkv_plan_t plan, pkv_stream_t stream, float *o_h, float *
  */
 int pkv_selftest_wait(int64_t limit_ns, uint32_t *status_h, int32_t *result_h);
 
+/*
+ * Per-CTA timeline of the attention launch, a diagnostic (the debug per-CTA
+ * tile counter and phase stamps).  While enabled, every attention launch of
+ * pkv_decode / pkv_decode_host writes one row of PKV_TRACE_WORDS uint64 per CTA
+ * into a device buffer owned by the plan (grown, synchronously, when a launch
+ * has more CTAs than it holds); pkv_trace_read synchronises the device and
+ * copies the last traced launch's rows out (row = blockIdx.x; *count = its
+ * CTAs; no event is recorded between launches, so tracing leaves the overlap of
+ * back-to-back launches as it is).  Word i of a
+ * row: 0 tiles the CTA ran; 1 its SM; then %globaltimer ns of 2 kernel entry,
+ * 3 grid dependency wait released, 4 consumer warp 0 holds its first block,
+ * 5 consumer warp 0 has reduced its last block, 6 the last tile's warp states
+ * combined and written, 7 split arrival counted, 8 merge done (only a CTA that
+ * merged), 9 CTA done; 10 (b << 40) | (kvh << 20) | split of its last tile;
+ * 0 where a phase did not occur.  Rows are written after the grid dependency
+ * wait, so back-to-back launches do not mix.  Off: one uniform branch per
+ * phase.  Results are unchanged by tracing.
+ */
+#define PKV_TRACE_WORDS 12
+int pkv_trace_enable(pkv_plan_t plan, int32_t enable);
+int pkv_trace_read(pkv_plan_t plan, uint64_t *rows_h, int32_t capacity, int32_t *count);
+
 /* Per-launch timing.  While enabled, pkv_decode brackets each kernel it
  * launches with CUDA events; pkv_profile_read waits for them and returns the
  * durations in milliseconds of the last pkv_decode's launches, in launch order. */

@@ -38,6 +38,8 @@
 #include "pkv.h"
 #include "pkv_internal.h"
 
+static_assert(PKV_TRACE_WORDS == pkv::kTraceWords, "trace row layout");
+
 namespace {
 thread_local int g_last_cuda_error = 0;
 }  // namespace
@@ -403,6 +405,12 @@ struct pkv_plan_s {
     cudaEvent_t ev[3] = {nullptr, nullptr, nullptr};
     int ev_launches = 0;
 
+    // per-CTA timeline of the attention launch (pkv_trace_enable)
+    bool trace_on = false;
+    uint64_t* trace = nullptr;   // device [trace_cap][kTraceWords]
+    int trace_cap = 0;           // rows allocated
+    int trace_rows = 0;          // CTAs of the last traced launch
+
     // Device address of host_buf (pinned memory is mapped into the GPU's
     // address space), so pkv_decode_host can read a fresh plan in place.
     const int32_t* host_buf_dev = nullptr;
@@ -424,6 +432,7 @@ void release(pkv_plan_s* p) {
     cudaFree(p->ws_lse);
     cudaFree(p->arrive);
     cudaFree(p->ctr);
+    cudaFree(p->trace);
     cudaFreeHost(p->host_stage);
     if (p->upload_done) cudaEventDestroy(p->upload_done);
     for (auto& e : p->ev)
@@ -760,6 +769,18 @@ int enqueue_decode(pkv_plan_t p, const void* q, const void* k_pages, const void*
             if (!ev) PKV_CUDA(cudaEventCreate(&ev));
         PKV_CUDA(cudaEventRecord(p->ev[0], s));
     }
+    if (p->trace_on && grid > 0) {
+        if (grid > p->trace_cap) {   // tracing is a diagnostic: its buffer grows here, synchronously
+            PKV_CUDA(cudaStreamSynchronize(s));
+            cudaFree(p->trace);
+            p->trace = nullptr;
+            p->trace_cap = 0;
+            PKV_CUDA(cudaMalloc(&p->trace, static_cast<size_t>(grid) * pkv::kTraceWords * sizeof(uint64_t)));
+            p->trace_cap = grid;
+        }
+        a.trace = p->trace;
+        p->trace_rows = grid;
+    }
     int n = 0;
     if (grid > 0) {
         cudaError_t e = pkv::launch_attention(a, p->kmap, p->vmap, grid, s, a.all_merge != 0);
@@ -901,6 +922,24 @@ int pkv_selftest_wait(int64_t limit_ns, uint32_t* status_h, int32_t* result_h) {
 int pkv_profile_enable(pkv_plan_t p, int32_t enable) {
     if (!p) return PKV_EINVAL;
     p->profile = enable != 0;
+    return PKV_OK;
+}
+
+int pkv_trace_enable(pkv_plan_t p, int32_t enable) {
+    if (!p) return PKV_EINVAL;
+    p->trace_on = enable != 0;
+    return PKV_OK;
+}
+
+int pkv_trace_read(pkv_plan_t p, uint64_t* rows_h, int32_t capacity, int32_t* count) {
+    if (!p || !count) return PKV_EINVAL;
+    *count = p->trace ? p->trace_rows : 0;
+    if (!*count || !rows_h) return PKV_OK;
+    PKV_CUDA(cudaDeviceSynchronize());
+    const int n = std::min(*count, std::max(capacity, 0));
+    if (n > 0)
+        PKV_CUDA(cudaMemcpy(rows_h, p->trace, static_cast<size_t>(n) * pkv::kTraceWords * sizeof(uint64_t),
+                            cudaMemcpyDeviceToHost));
     return PKV_OK;
 }
 

@@ -39,6 +39,25 @@ enum Route : int32_t {
     kRoutePersistent = 3  // tiles from an atomic counter over the queue
 };
 
+// Per-CTA timeline of one attention launch (pkv_trace_enable): row blockIdx.x
+// of kTraceWords words.  Times are %globaltimer ns (0: the phase did not occur).
+// Every CTA writes its whole row, after the grid dependency wait, on every
+// launch, so rows never mix two launches and need no reset between them.
+enum TraceSlot : int {
+    kTrTiles = 0,      // tiles this CTA ran
+    kTrSm = 1,         // SM the CTA ran on
+    kTrEntry = 2,      // kernel entry (before the grid dependency wait)
+    kTrWaitDone = 3,   // grid dependency wait released
+    kTrFirstBlock = 4, // consumer warp 0 holds its first block of the CTA's first tile
+    kTrStreamEnd = 5,  // consumer warp 0 has reduced its last block of the last tile
+    kTrCombineEnd = 6, // the last tile's four warp states are combined and written
+    kTrArrived = 7,    // the last split tile's arrival counted (split routes)
+    kTrMergeEnd = 8,   // this CTA merged a (row, KV head) as the last arrival: merge done
+    kTrExit = 9,       // CTA done
+    kTrLastTile = 10,  // (b << 40) | (kvh << 20) | split of the last tile
+    kTraceWords = 12
+};
+
 struct AttnParams {
     const uint16_t* q;            // bf16 [B][Hq][D]
     const uint16_t* k_pages;      // bf16 [num_pages][page_size][Hkv][D]
@@ -70,6 +89,7 @@ struct AttnParams {
     int32_t no_empty_rows;        // queue / persistent routes: every row has tokens, so there is no
                                   // neutral state to write (0: look for empty rows after the tiles)
     float scale_log2;             // log2(e) / sqrt(D)
+    uint64_t* trace;              // [grid][kTraceWords] per-CTA timeline, or null (off)
 };
 
 // Device planner of a continuous-decoding step (pkv_devplan.cu): page

@@ -26,6 +26,10 @@ MERGE_NAMES = {0: "none", 1: "last", 2: "all", 3: "separate"}
 
 OK, EINVAL, ENOMEM, ECUDA, EUNSUPPORTED, EDEVICE, ENOSPACE = range(7)
 DEV_PAGE_OOB, DEV_PLAN_MISMATCH, DEV_TIMEOUT, DEV_ROW_FULL = 1, 2, 4, 8
+# per-CTA timeline rows (pkv_trace_read): word index of each field
+TRACE_WORDS = 12
+(TR_TILES, TR_SM, TR_ENTRY, TR_WAIT_DONE, TR_FIRST_BLOCK, TR_STREAM_END, TR_COMBINE_END, TR_ARRIVED,
+ TR_MERGE_END, TR_EXIT, TR_LAST_TILE) = range(11)
 
 
 class Geom(ctypes.Structure):
@@ -82,6 +86,8 @@ SIGNATURES = {
     "pkv_read_workspace": (ctypes.c_int, [_P, _P, _P, _P, _I32, _I32P]),
     "pkv_profile_enable": (ctypes.c_int, [_P, _I32]),
     "pkv_profile_read": (ctypes.c_int, [_P, ctypes.POINTER(ctypes.c_float), _I32, _I32P]),
+    "pkv_trace_enable": (ctypes.c_int, [_P, _I32]),
+    "pkv_trace_read": (ctypes.c_int, [_P, _P, _I32, _I32P]),
     "pkv_pool_create": (ctypes.c_int, [_I32P, _I32, _I32, ctypes.POINTER(ctypes.c_void_p)]),
     "pkv_pool_reserve": (ctypes.c_int, [_P, _I32P, _I32P, _I32, _I32, _I32, _I32P, _I32P]),
     "pkv_pool_release": (ctypes.c_int, [_P, _I32P, _I32]),
@@ -263,6 +269,19 @@ class Plan:
         n = ctypes.c_int32(0)
         _check(load().pkv_profile_read(self.handle, ms, 4, ctypes.byref(n)), "pkv_profile_read")
         return [ms[i] for i in range(n.value)]
+
+    def trace(self, enable: bool = True):
+        """Per-CTA timeline of the attention launches (pkv_trace_enable)."""
+        _check(load().pkv_trace_enable(self.handle, int(enable)), "pkv_trace_enable")
+
+    def read_trace(self) -> np.ndarray:
+        """uint64 [CTAs][TRACE_WORDS] rows of the last traced launch (pkv_trace_read)."""
+        n = ctypes.c_int32(0)
+        _check(load().pkv_trace_read(self.handle, None, 0, ctypes.byref(n)), "pkv_trace_read")
+        rows = np.zeros((n.value, TRACE_WORDS), np.uint64)
+        if n.value:
+            _check(load().pkv_trace_read(self.handle, rows.ctypes.data, n.value, ctypes.byref(n)), "pkv_trace_read")
+        return rows
 
     def close(self):
         if getattr(self, "_h", None) is not None and _lib is not None:
