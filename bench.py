@@ -277,6 +277,35 @@ def single_thread_oracle(p, kv_bytes: int, estimate_s: float, limit_s: float = 1
 
 # ----------------------------------------------------------------------------- our arm
 
+def phase_summary(rows, pkv):
+    """Median phase durations (µs) of one traced attention launch, from its
+    per-CTA timeline rows (pkv_trace_read)."""
+    t = rows.astype(np.int64)
+    ran = t[:, pkv.TR_TILES] > 0
+    streamed = ran & (t[:, pkv.TR_FIRST_BLOCK] > 0)
+    t0 = int(t[:, pkv.TR_WAIT_DONE].min())
+
+    def med(a, b, sel):
+        v = (t[sel, b] - t[sel, a]) / 1e3
+        return round(float(np.median(v)), 3) if v.size else None
+
+    merged = t[:, pkv.TR_MERGE_END] > 0
+    arrived = t[:, pkv.TR_ARRIVED] > 0
+    out = {"ctas": int(len(t)), "ctas_with_tiles": int(ran.sum()),
+           "wait_released_spread": round(float((t[:, pkv.TR_WAIT_DONE].max() - t0) / 1e3), 3),
+           "wait_to_first_block": med(pkv.TR_WAIT_DONE, pkv.TR_FIRST_BLOCK, streamed),
+           "stream": med(pkv.TR_FIRST_BLOCK, pkv.TR_STREAM_END, streamed),
+           "combine": med(pkv.TR_STREAM_END, pkv.TR_COMBINE_END, ran),
+           "arrival": med(pkv.TR_COMBINE_END, pkv.TR_ARRIVED, ran & arrived),
+           "merge": med(pkv.TR_ARRIVED, pkv.TR_MERGE_END, merged),
+           "stream_end_median_to_last": round(float((t[streamed, pkv.TR_STREAM_END].max()
+                                                     - np.median(t[streamed, pkv.TR_STREAM_END])) / 1e3), 3)
+           if streamed.any() else None,
+           "launch_span": round(float((t[:, pkv.TR_EXIT].max() - t0) / 1e3), 3)}
+    if merged.any():
+        out["last_merge_end"] = round(float((t[merged, pkv.TR_MERGE_END].max() - t0) / 1e3), 3)
+    return out
+
 def device_problem(p, dev):
     """The problem's inputs in device memory, plus fp32 outputs."""
     import torch
@@ -394,22 +423,35 @@ def decode_line(name, args, ctx, headline=True):
         region_ms = [a.elapsed_time(b) / K for a, b in ev]
     med_ms = statistics.median(region_ms)
 
-    # (2) for reference: every step alone, after an L2 flush, between its own
-    # events (adds the launch latency to each step); per-kernel events when the
-    # step has two launches
+    # (2) for reference: every step alone, between its own events (adds the
+    # launch latency to each step), after one of two L2 flushes: writing a
+    # 2 x L2 buffer (the L2 is then full of dirty lines, whose write-back to HBM
+    # lands inside the timed kernel as it evicts them), or reading a 2 x L2
+    # buffer that is never written (the L2 then holds clean lines of another
+    # buffer, and the previous step's dirty lines were written back during the
+    # sweep); per-kernel events when the step has two launches
+    clean = torch.empty(max(2 * l2, 256 << 20) // 4, dtype=torch.int32, device=dev)
     plan.profile(per_kernel_events)
-    iso_ms, kernel_ms = [], []
+    iso_ms, iso_clean_ms, kernel_ms = [], [], []
     for i in range(max(min(K, 50), 5)):
-        flush.zero_()
-        starts[i % K].record(stream)
-        step(i)
-        ends[i % K].record(stream)
-        ends[i % K].synchronize()
-        iso_ms.append(starts[i % K].elapsed_time(ends[i % K]))
-        if per_kernel_events:
-            kernel_ms.append(plan.profile_read())
+        for dirty, acc in ((True, iso_ms), (False, iso_clean_ms)):
+            if dirty:
+                flush.zero_()
+            else:
+                clean.sum()
+            starts[i % K].record(stream)
+            step(i)
+            ends[i % K].record(stream)
+            ends[i % K].synchronize()
+            acc.append(starts[i % K].elapsed_time(ends[i % K]))
+            if per_kernel_events and dirty:
+                kernel_ms.append(plan.profile_read())
+            elif per_kernel_events:
+                plan.profile_read()
     plan.profile(False)
+    del clean
     iso_med = statistics.median(iso_ms)
+    iso_clean_med = statistics.median(iso_clean_ms)
     if per_kernel_events:
         attn_ms = statistics.mean(km[0] for km in kernel_ms)
         merge_ms = statistics.mean(km[1] for km in kernel_ms)
@@ -417,8 +459,8 @@ def decode_line(name, args, ctx, headline=True):
         attn_ms = med_ms
         merge_ms = 0.0
 
-    med_ms, attn_ms, iso_med, lo_ms, hi_ms = reduce_max([med_ms, attn_ms, iso_med, min(region_ms), max(region_ms)],
-                                                        dist, dev)
+    med_ms, attn_ms, iso_med, iso_clean_med, lo_ms, hi_ms = reduce_max(
+        [med_ms, attn_ms, iso_med, iso_clean_med, min(region_ms), max(region_ms)], dist, dev)
     kv = info["kv_bytes"]
     q_bytes = p.B * p.Hq * p.D * 2
     o_bytes = p.B * p.Hq * (p.D + 1) * 4
@@ -431,7 +473,7 @@ def decode_line(name, args, ctx, headline=True):
               "samples": clocks["samples"]}
     us = {"median": round(med_ms * 1e3, 2), "min": round(lo_ms * 1e3, 2), "max": round(hi_ms * 1e3, 2),
           "repeats": R, "steps_per_repeat": K}
-    l2_words = (f"cold: {rot} copies of the page pool and q used round robin, >= 6 x L2 bytes read between "
+    l2_words = (f"cold: {rot} cop{'y' if rot == 1 else 'ies'} of the page pool and q used round robin, >= 6 x L2 bytes read between "
                 f"two reads of a copy; {R} repeats of {K} steps back to back, one event pair each"
                 if streamed else f"flushed before every timed step (2 x L2 bytes written); {R} repeats of "
                                  f"{K} steps, median step of each")
@@ -443,10 +485,26 @@ def decode_line(name, args, ctx, headline=True):
         return {"workload": p.name, "mode": info["mode_name"], "merge": info["merge_name"],
                 "tiles": info["num_work_items"], "chunk_pages": info["chunk_pages"],
                 "kv_bytes_per_step": kv, "us_per_step": us, "isolated_us_per_step": round(iso_med * 1e3, 2),
+                "isolated_clean_l2_us_per_step": round(iso_clean_med * 1e3, 2),
                 "kv_gbs": round(value, 2), "frac_of_measured": round(value / peak, 4),
                 "frac_of_nominal_7_9TBs": round(value / NOMINAL_HBM_GBS, 4), "roofline": roofline,
                 "l2": l2_words, "clocks": clocks,
                 "parity": {"max_abs_out": err_out, "max_abs_lse": err_lse}}
+
+    phases = None
+    if args.phase_trace:
+        # per-CTA timelines of the last step of a back-to-back run, repeated
+        plan.trace(True)
+        runs = []
+        for r in range(R):
+            for i in range(K):
+                step(i)
+            runs.append(phase_summary(plan.read_trace(), pkv))
+        plan.trace(False)
+        phases = {k: (round(statistics.median(x[k] for x in runs), 3) if isinstance(runs[0][k], float) else runs[0][k])
+                  for k in runs[0] if all(r.get(k) is not None for r in runs)}
+        phases["note"] = (f"median over {R} traced launches (each the last of {K} back-to-back steps) of per-CTA "
+                          "median phase durations in us; times from the grid dependency wait's release")
 
     # end to end through the C ABI with host buffers: host re-plan, then
     # pkv_decode_host, which synchronises: the kernel reads the new plan and q in
@@ -494,6 +552,11 @@ def decode_line(name, args, ctx, headline=True):
                    "launches_per_step": info["launches_per_step"], "l2": l2_words},
         "kv_bytes_per_step": kv,
         "isolated_us_per_step": round(iso_med * 1e3, 2),
+        "isolated_clean_l2_us_per_step": round(iso_clean_med * 1e3, 2),
+        "isolated_note": ("each step alone between its own events, launch latency included, after an L2 flush: "
+                          "isolated_us_per_step after writing 2 x L2 (its dirty lines are written back inside "
+                          "the timed kernel), isolated_clean_l2_us_per_step after reading 2 x L2 of a buffer "
+                          "never written (clean lines)"),
         "frac_of_nominal_7_9TBs": round(value / NOMINAL_HBM_GBS, 4),
         "kernel_ms": {"attention": round(attn_ms, 5), "merge": round(merge_ms, 5)},
         "roofline": roofline,
@@ -507,6 +570,7 @@ def decode_line(name, args, ctx, headline=True):
         "clocks": clocks,
         "timed_region_wall_s": round(t_wall, 4),
         "parity": {"max_abs_out": err_out, "max_abs_lse": err_lse},
+        **({"phases_us": phases} if phases else {}),
     }
 
 
@@ -1057,6 +1121,8 @@ def main():
     ap.add_argument("--calibrate", action="store_true",
                     help="with --trace-study: fit the policy thresholds on the calibration seed first")
     ap.add_argument("--study-steps", type=int, default=15, help="timed steps per route in the trace study")
+    ap.add_argument("--phase-trace", action="store_true",
+                    help="add the per-CTA phase timeline (pkv_trace_*) of back-to-back steps to the line")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

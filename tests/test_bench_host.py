@@ -88,3 +88,19 @@ def test_product_package_never_imports_the_oracle():
                 text = open(os.path.join(dirpath, f)).read()
                 assert "import oracle" not in text and "from oracle" not in text, f
                 assert "pkv_oracle" not in text, f
+
+
+def test_phase_summary_of_synthetic_rows():
+    """Two CTAs: one streams and merges, one streams and only arrives."""
+    rows = np.zeros((2, pkv.TRACE_WORDS), np.uint64)
+    base = 10_000_000
+    # tiles, sm, entry, wait, first, stream_end, combine, arrived, merge_end, exit
+    rows[0, :10] = [1, 3, base - 500, base, base + 1500, base + 20500, base + 21000, base + 22000, base + 24000,
+                    base + 24100]
+    rows[1, :10] = [1, 4, base - 400, base + 100, base + 1700, base + 20300, base + 20700, base + 21500, 0,
+                    base + 21600]
+    s = bench.phase_summary(rows, pkv)
+    assert s["ctas"] == 2 and s["ctas_with_tiles"] == 2
+    assert s["wait_to_first_block"] == 1.55 and s["stream"] == 18.8 and s["combine"] == 0.45
+    assert s["arrival"] == 0.9 and s["merge"] == 2.0 and s["launch_span"] == 24.1 and s["last_merge_end"] == 24.0
+    assert s["wait_released_spread"] == 0.1 and s["stream_end_median_to_last"] == 0.1
