@@ -427,6 +427,47 @@ int pkv_session_device_queue(pkv_session_t session, pkv_work_item *items, int32_
                              int32_t *count);
 
 /*
+ * Slot admit / evict at step boundaries.  The rows of a session are fixed
+ * slots, as the per-session state of "WPK persistent kernel" (dotwave.ai,
+ * "What has to exist instead") lives in fixed arenas whose slots are reset at
+ * a beat boundary.  A slot is active (it takes one token per step) or idle:
+ * length 0, no pages, skipped by the append and by page allocation, and decoded
+ * to the neutral state (out 0, lse -inf).  Every row is active when the session
+ * is created.
+ *   pkv_session_evict   makes the n listed active rows idle: their pages (every
+ *                       non-negative entry of the row's table, in table order,
+ *                       rows in the order listed) go to the back of the free
+ *                       list, their table entries become -1 and their lengths 0
+ *   pkv_session_admit   gives each of the n listed idle rows a new session of
+ *                       lens_h[i] >= 0 tokens: ceil(lens_h[i] / page_size) pages
+ *                       from the front of the free list (rows in the order
+ *                       listed, pages in table order), that length, and its
+ *                       prompt's K/V copied into those pages from k_src / v_src
+ *                       (device bf16 [sum_i lens_h[i]][Hkv][D], the rows' tokens
+ *                       one after another in the order listed)
+ * The free list is the session's host pool, or, after pkv_session_device_plan,
+ * the device free list, which then lives on the GPU: the requests go to the
+ * device through a pinned, mapped slot table and one kernel applies them (a
+ * graph-captured step needs no re-capture); an admission the device free list
+ * cannot serve sets PKV_DEV_ROW_FULL and leaves that row and the rows listed
+ * after it idle.  Both calls enqueue their device work on `stream`, to run
+ * between two steps.  Errors (nothing changes): PKV_EINVAL for a row out of
+ * range, listed twice, or in the wrong state (evict: not active; admit: not
+ * idle), a null or misaligned pointer, a length above max_pages_per_seq *
+ * page_size; PKV_ENOSPACE when the host pool holds too few pages; PKV_EINVAL
+ * while a resident kernel runs (use pkv_resident_evict / pkv_resident_admit).
+ */
+int pkv_session_evict(pkv_session_t session, const int32_t *rows_h, int32_t n, pkv_stream_t stream);
+int pkv_session_admit(pkv_session_t session, const int32_t *rows_h, const int32_t *lens_h, int32_t n,
+                      const void *k_src, const void *v_src, void *k_pages, void *v_pages, pkv_stream_t stream);
+/* Copy the session's free list, front first (the host pool, or the device free
+ * list in device-plan mode, which synchronises the device); *count receives its
+ * length, at most `capacity` ids are written.  active_h (nullable, [B]) receives
+ * 1 for an active row, 0 for an idle one. */
+int pkv_session_free_pages(pkv_session_t session, int32_t *pages_h, int32_t capacity, int32_t *count,
+                           int32_t *active_h);
+
+/*
  * Resident steps (a continuous session kept on the GPU by one launch).
  * pkv_resident_start launches one cooperative kernel over every SM on a stream
  * of its own; the kernel stays resident and runs one step each time the host
@@ -471,6 +512,15 @@ int pkv_resident_step(pkv_resident_t resident, const void *q_h, const void *k_ne
 int pkv_resident_stop(pkv_resident_t resident);
 int pkv_resident_times(pkv_resident_t resident, uint64_t *stamps_ns, int32_t capacity, int32_t *count);
 void pkv_resident_destroy(pkv_resident_t resident);
+/* Slot requests for a running resident kernel, applied at the start of the next
+ * pkv_resident_step, before its page allocation and plan: the same evictions and
+ * admissions as pkv_session_evict / pkv_session_admit (device free list; k_src /
+ * v_src device memory that must stay valid until that step returns).  Up to
+ * PKV_RESIDENT_MAX_REQUESTS rows per step; PKV_EINVAL / PKV_ENOSPACE as there. */
+#define PKV_RESIDENT_MAX_REQUESTS 64
+int pkv_resident_evict(pkv_resident_t resident, const int32_t *rows_h, int32_t n);
+int pkv_resident_admit(pkv_resident_t resident, const int32_t *rows_h, const int32_t *lens_h, int32_t n,
+                       const void *k_src, const void *v_src);
 
 const char *pkv_strerror(int code);
 /* The CUDA error code behind the last PKV_ECUDA on this thread (0 if none). */

@@ -987,20 +987,28 @@ int pkv_pool_create(const int32_t* free_pages, int32_t count, int32_t num_pages,
     return PKV_OK;
 }
 
-int pkv_pool_reserve(pkv_pool_t pool, const int32_t* seq_lens_h, int32_t* block_table_h, int32_t batch,
-                     int32_t max_pages_per_seq, int32_t page_size, int32_t* rows_out, int32_t* n_rows) {
+}  // extern "C"
+
+namespace {
+// pkv_pool_reserve over the rows whose `active` entry is non-zero (all rows
+// when `active` is null): idle slots of a session take no page.
+int pool_reserve_rows(pkv_pool_t pool, const int32_t* seq_lens_h, int32_t* block_table_h, int32_t batch,
+                      int32_t max_pages_per_seq, int32_t page_size, const uint8_t* active, int32_t* rows_out,
+                      int32_t* n_rows) {
     if (!pool || batch < 0 || (batch > 0 && (!seq_lens_h || !block_table_h)) || max_pages_per_seq <= 0 ||
         page_size <= 0)
         return PKV_EINVAL;
     // first pass: count and check, so that failure changes nothing
     auto wants_page = [&](int32_t b) {
-        return seq_lens_h[b] % page_size == 0 &&
+        return (!active || active[b]) && seq_lens_h[b] % page_size == 0 &&
                block_table_h[static_cast<size_t>(b) * max_pages_per_seq + seq_lens_h[b] / page_size] < 0;
     };
     int32_t need = 0;
     for (int32_t b = 0; b < batch; ++b) {
         if (seq_lens_h[b] < 0) return PKV_EINVAL;
-        if (seq_lens_h[b] % page_size == 0 && seq_lens_h[b] / page_size >= max_pages_per_seq) return PKV_ENOSPACE;
+        if ((!active || active[b]) && seq_lens_h[b] % page_size == 0 &&
+            seq_lens_h[b] / page_size >= max_pages_per_seq)
+            return PKV_ENOSPACE;
         if (wants_page(b)) ++need;
     }
     if (static_cast<size_t>(need) > pool->free_list.size()) return PKV_ENOSPACE;
@@ -1016,6 +1024,15 @@ int pkv_pool_reserve(pkv_pool_t pool, const int32_t* seq_lens_h, int32_t* block_
     }
     if (n_rows) *n_rows = k;
     return PKV_OK;
+}
+}  // namespace
+
+extern "C" {
+
+int pkv_pool_reserve(pkv_pool_t pool, const int32_t* seq_lens_h, int32_t* block_table_h, int32_t batch,
+                     int32_t max_pages_per_seq, int32_t page_size, int32_t* rows_out, int32_t* n_rows) {
+    return pool_reserve_rows(pool, seq_lens_h, block_table_h, batch, max_pages_per_seq, page_size, nullptr, rows_out,
+                             n_rows);
 }
 
 int pkv_pool_release(pkv_pool_t pool, const int32_t* pages, int32_t count) {
@@ -1074,6 +1091,14 @@ struct pkv_session_s {
     int32_t chunk = 0;
     int32_t max_splits = 0;
     pkv_resident_s* resident = nullptr;   // a resident kernel owns the session's device state
+    // slots: active rows take a token each step, idle ones (evicted) are left alone
+    int32_t* active_d = nullptr;             // [B] device, 1 active / 0 idle
+    std::vector<uint8_t> active_h;            // the host's view of the same
+    pkv::SlotRequest* req_h = nullptr;        // pinned, mapped [B] slot requests of one call
+    const pkv::SlotRequest* req_d = nullptr;
+    int32_t* req_pages_h = nullptr;           // pinned, mapped page ids chosen by the host pool
+    const int32_t* req_pages_d = nullptr;
+    size_t req_pages_cap = 0;
 };
 
 struct pkv_resident_s {
@@ -1093,6 +1118,9 @@ struct pkv_resident_s {
     size_t q_bytes = 0, new_bytes = 0, out_bytes = 0, lse_bytes = 0;
     uint32_t step = 0;
     bool running = false;
+    pkv::SlotRequest* req_h = nullptr;   // pinned, mapped slot requests for the next step
+    const pkv::SlotRequest* req_d = nullptr;
+    int32_t n_req = 0;
 };
 
 namespace {
@@ -1102,6 +1130,9 @@ void session_free(pkv_session_s* s) {
     cudaFree(s->dev_free);
     cudaFree(s->dev_free_state);
     cudaFree(s->dev_plan);
+    cudaFree(s->active_d);
+    cudaFreeHost(s->req_h);
+    cudaFreeHost(s->req_pages_h);
     cudaFreeHost(s->lens_h);
     cudaFreeHost(s->table_h);
     cudaFreeHost(s->new_pages_h);
@@ -1146,6 +1177,21 @@ int pkv_session_create(pkv_plan_t plan, pkv_pool_t pool, const int32_t* seq_lens
         memcpy(s->lens_h, seq_lens_h, sizeof(int32_t) * B);
         memcpy(s->table_h, block_table_h, sizeof(int32_t) * table_n);
     }
+    // every row starts active
+    s->active_h.assign(B, 1);
+    const std::vector<int32_t> ones(std::max(B, 1), 1);
+    if (cudaMalloc(&s->active_d, sizeof(int32_t) * std::max(B, 1)) != cudaSuccess ||
+        cudaHostAlloc(&s->req_h, sizeof(pkv::SlotRequest) * std::max(B, 1), cudaHostAllocMapped) != cudaSuccess) {
+        session_free(s);
+        return PKV_ENOMEM;
+    }
+    cudaError_t e = cudaMemcpy(s->active_d, ones.data(), sizeof(int32_t) * std::max(B, 1), cudaMemcpyHostToDevice);
+    if (e == cudaSuccess) e = cudaHostGetDevicePointer(&mapped, s->req_h, 0);
+    if (e != cudaSuccess) {
+        session_free(s);
+        return cuda_fail(e);
+    }
+    s->req_d = static_cast<const pkv::SlotRequest*>(mapped);
     *session = s;
     return PKV_OK;
 }
@@ -1182,8 +1228,10 @@ int pkv_session_device_plan(pkv_session_t s, pkv_stream_t stream) {
     }
     std::vector<int32_t> pages(s->pool->free_list.begin(), s->pool->free_list.end());
     const size_t plan_ints = static_cast<size_t>(cap) * 6 + 2 * static_cast<size_t>(B) + 1;
+    // the free list is a ring that can hold every page of the pool (evicted rows give theirs back)
+    const size_t ring = std::max<size_t>(std::max<size_t>(pages.size(), static_cast<size_t>(g.num_pages)), 1);
     if (cudaMalloc(&s->dev_plan, plan_ints * sizeof(int32_t)) != cudaSuccess ||
-        cudaMalloc(&s->dev_free, std::max<size_t>(pages.size(), 1) * sizeof(int32_t)) != cudaSuccess ||
+        cudaMalloc(&s->dev_free, ring * sizeof(int32_t)) != cudaSuccess ||
         cudaMalloc(&s->dev_free_state, 2 * sizeof(uint32_t)) != cudaSuccess) {
         cudaFree(s->dev_plan);   // none of them is kept: a later call starts over
         cudaFree(s->dev_free);
@@ -1199,7 +1247,7 @@ int pkv_session_device_plan(pkv_session_t s, pkv_stream_t stream) {
     PKV_CUDA(cudaStreamSynchronize(st));   // the host vectors above go out of scope
     s->pool->free_list.clear();            // those pages now belong to the device allocator
     std::fill(s->pool->is_free.begin(), s->pool->is_free.end(), uint8_t{0});
-    s->free_cap = static_cast<int32_t>(std::max<size_t>(pages.size(), 1));
+    s->free_cap = static_cast<int32_t>(ring);
     s->queue_cap = static_cast<int32_t>(cap);
     s->chunk = chunk;
     s->max_splits = s_max;
@@ -1220,6 +1268,7 @@ void device_plan_views(pkv_session_t s, pkv::DevPlanParams* dp_out, DevicePlan* 
     int32_t* tiles = order + s->queue_cap;
     pkv::DevPlanParams dp{};
     dp.lens = s->lens_d;
+    dp.active = s->active_d;
     dp.table = s->table_d;
     dp.free_list = s->dev_free;
     dp.free_state = s->dev_free_state;
@@ -1247,9 +1296,15 @@ int session_step_device(pkv_session_t s, const void* k_new, const void* v_new, v
     pkv::DevPlanParams dp{};
     DevicePlan plan{};
     device_plan_views(s, &dp, &plan);
+    if (!k_new || !v_new || !k_pages || !v_pages || !aligned16(k_new) || !aligned16(v_new) || !aligned16(k_pages) ||
+        !aligned16(v_pages))
+        return PKV_EINVAL;
     PKV_CUDA(pkv::launch_plan_step(dp, st));
-    int rc = pkv_append(k_new, v_new, k_pages, v_pages, s->table_d, s->lens_d, p, reinterpret_cast<pkv_stream_t>(st));
-    if (rc) return rc;
+    const pkv_geom& g = p->g;
+    PKV_CUDA(pkv::launch_append(static_cast<const uint16_t*>(k_new), static_cast<const uint16_t*>(v_new),
+                                static_cast<uint16_t*>(k_pages), static_cast<uint16_t*>(v_pages), s->table_d,
+                                s->lens_d, g.batch, g.num_kv_heads, g.head_dim, p->page_size, g.max_pages_per_seq,
+                                g.num_pages, &p->ctr->status, st, s->active_d));
     return enqueue_decode(p, q, k_pages, v_pages, s->table_d, s->lens_d, out, lse, st, &plan);
 }
 }  // namespace
@@ -1273,7 +1328,7 @@ int pkv_session_step(pkv_session_t s, const void* k_new, const void* v_new, void
         s->copy_pending = false;
     }
     int32_t n_rows = 0;
-    int rc = pkv_pool_reserve(s->pool, s->lens_h, s->table_h, B, mp, ps, s->rows, &n_rows);
+    int rc = pool_reserve_rows(s->pool, s->lens_h, s->table_h, B, mp, ps, s->active_h.data(), s->rows, &n_rows);
     if (rc) return rc;
     pkv_plan_s* p = s->plan;
     if (s->new_pages_d && p->host_buf_dev) {
@@ -1286,7 +1341,7 @@ int pkv_session_step(pkv_session_t s, const void* k_new, const void* v_new, void
             s->new_pages_h[2 * b] = s->lens_h[b] / ps;
             s->new_pages_h[2 * b + 1] = s->table_h[static_cast<size_t>(b) * mp + s->lens_h[b] / ps];
         }
-        for (int b = 0; b < B; ++b) ++s->lens_h[b];
+        for (int b = 0; b < B; ++b) s->lens_h[b] += s->active_h[b];   // idle slots do not grow
         if ((rc = pkv_plan_update(p, s->lens_h, nullptr))) return rc;
         pkv::AppendStepParams ap{};
         ap.k_new = static_cast<const uint16_t*>(k_new);
@@ -1296,6 +1351,7 @@ int pkv_session_step(pkv_session_t s, const void* k_new, const void* v_new, void
         ap.block_table = s->table_d;
         ap.seq_lens = s->lens_d;
         ap.new_pages = s->new_pages_d;
+        ap.active = s->active_d;
         // (a plan staging that is not mapped is uploaded by the decode's copy instead)
         const bool kernel_copies = p->dirty && p->host_buf_dev;
         if (kernel_copies) {
@@ -1330,9 +1386,12 @@ int pkv_session_step(pkv_session_t s, const void* k_new, const void* v_new, void
         PKV_CUDA(cudaEventRecord(s->copied, st));
         s->copy_pending = true;
     }
-    for (int b = 0; b < B; ++b) ++s->lens_h[b];
+    for (int b = 0; b < B; ++b) s->lens_h[b] += s->active_h[b];   // idle slots do not grow
     if ((rc = pkv_plan_update(s->plan, s->lens_h, nullptr))) return rc;
-    if ((rc = pkv_append(k_new, v_new, k_pages, v_pages, s->table_d, s->lens_d, s->plan, stream))) return rc;
+    PKV_CUDA(pkv::launch_append(static_cast<const uint16_t*>(k_new), static_cast<const uint16_t*>(v_new),
+                                static_cast<uint16_t*>(k_pages), static_cast<uint16_t*>(v_pages), s->table_d,
+                                s->lens_d, B, g.num_kv_heads, g.head_dim, ps, mp, g.num_pages, &p->ctr->status, st,
+                                s->active_d));
     return pkv_decode(q, k_pages, v_pages, s->table_d, s->lens_d, s->plan, out, lse, stream);
 }
 
@@ -1378,12 +1437,209 @@ int pkv_session_device_queue(pkv_session_t s, pkv_work_item* items, int32_t* ord
     return PKV_OK;
 }
 
+// ------------------------------------------------------------------ slot admit / evict
+//
+// A session's rows are fixed slots, reset at a step boundary as the per-session
+// arenas of "WPK persistent kernel" (dotwave.ai, "What has to exist instead")
+// are.  The host pool's bookkeeping runs here; with a device free list
+// (device-plan mode) the slot kernel does it (pkv_slots.cuh).
+
+namespace {
+
+// Checks shared by the session and resident calls: rows in range, not listed
+// twice, in the state the request needs (`want_active`: evictions need an
+// active row, admissions an idle one); lengths fit the table; prompt pointers.
+int check_slot_rows(const std::vector<uint8_t>& active, int B, const int32_t* rows_h, int32_t n, bool want_active) {
+    if (n < 0 || (n > 0 && !rows_h)) return PKV_EINVAL;
+    std::vector<uint8_t> seen(B, 0);
+    for (int32_t i = 0; i < n; ++i) {
+        const int32_t b = rows_h[i];
+        if (b < 0 || b >= B || seen[b] || (active[b] != 0) != want_active) return PKV_EINVAL;
+        seen[b] = 1;
+    }
+    return PKV_OK;
+}
+
+int check_admit_args(const pkv_plan_s* p, const int32_t* lens_h, int32_t n, const void* k_src, const void* v_src,
+                     int64_t* tokens) {
+    int64_t total = 0;
+    for (int32_t i = 0; i < n; ++i) {
+        if (!lens_h || lens_h[i] < 0 ||
+            static_cast<int64_t>(lens_h[i]) > static_cast<int64_t>(p->g.max_pages_per_seq) * p->page_size)
+            return PKV_EINVAL;
+        total += lens_h[i];
+    }
+    if (total > 0 && (!k_src || !v_src || !aligned16(k_src) || !aligned16(v_src))) return PKV_EINVAL;
+    if (total > INT32_MAX) return PKV_EINVAL;
+    *tokens = total;
+    return PKV_OK;
+}
+
+pkv::SlotParams slot_params(pkv_session_t s, void* k_pages, void* v_pages, int32_t n) {
+    pkv_plan_s* p = s->plan;
+    pkv::SlotParams sp{};
+    sp.req = s->req_d;
+    sp.n = n;
+    sp.pages = s->req_pages_d;
+    if (s->device_mode) {
+        sp.free_list = s->dev_free;
+        sp.free_state = s->dev_free_state;
+        sp.free_cap = s->free_cap;
+    }
+    sp.table = s->table_d;
+    sp.lens = s->lens_d;
+    sp.active = s->active_d;
+    sp.k_pages = static_cast<uint16_t*>(k_pages);
+    sp.v_pages = static_cast<uint16_t*>(v_pages);
+    sp.status = &p->ctr->status;
+    sp.B = p->g.batch;
+    sp.Hkv = p->g.num_kv_heads;
+    sp.D = p->g.head_dim;
+    sp.page_size = p->page_size;
+    sp.max_pages = p->g.max_pages_per_seq;
+    sp.num_pages = p->g.num_pages;
+    return sp;
+}
+
+// The staging of the last slot call (or step) may still be read by the GPU.
+int wait_session_staging(pkv_session_t s) {
+    if (s->copy_pending) {
+        PKV_CUDA(cudaEventSynchronize(s->copied));
+        s->copy_pending = false;
+    }
+    return PKV_OK;
+}
+
+int launch_slots(pkv_session_t s, void* k_pages, void* v_pages, int32_t n, cudaStream_t st) {
+    PKV_CUDA(pkv::launch_slot_requests(slot_params(s, k_pages, v_pages, n), st));
+    PKV_CUDA(cudaEventRecord(s->copied, st));   // the requests (and page ids) are read by then
+    s->copy_pending = true;
+    return PKV_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int pkv_session_evict(pkv_session_t s, const int32_t* rows_h, int32_t n, pkv_stream_t stream) {
+    NvtxRange range("pkv_session_evict");
+    if (!s || s->resident) return PKV_EINVAL;
+    const int B = s->plan->g.batch, mp = s->plan->g.max_pages_per_seq;
+    int rc = check_slot_rows(s->active_h, B, rows_h, n, true);
+    if (rc || n == 0) return rc;
+    if ((rc = wait_session_staging(s))) return rc;
+    if (!s->device_mode) {   // the host pool takes the pages back, in table order, rows in the order listed
+        std::vector<int32_t> pages;
+        for (int32_t i = 0; i < n; ++i)
+            for (int j = 0; j < mp; ++j) {
+                const int32_t page = s->table_h[static_cast<size_t>(rows_h[i]) * mp + j];
+                if (page >= 0) pages.push_back(page);
+            }
+        if ((rc = pkv_pool_release(s->pool, pages.data(), static_cast<int32_t>(pages.size())))) return rc;
+        for (int32_t i = 0; i < n; ++i) {
+            std::fill(s->table_h + static_cast<size_t>(rows_h[i]) * mp,
+                      s->table_h + static_cast<size_t>(rows_h[i] + 1) * mp, -1);
+            s->lens_h[rows_h[i]] = 0;
+        }
+    }
+    for (int32_t i = 0; i < n; ++i) {
+        s->req_h[i] = pkv::SlotRequest{rows_h[i], -1, 0, 0, nullptr, nullptr};
+        s->active_h[rows_h[i]] = 0;
+    }
+    return launch_slots(s, nullptr, nullptr, n, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int pkv_session_admit(pkv_session_t s, const int32_t* rows_h, const int32_t* lens_h, int32_t n, const void* k_src,
+                      const void* v_src, void* k_pages, void* v_pages, pkv_stream_t stream) {
+    NvtxRange range("pkv_session_admit");
+    if (!s || s->resident) return PKV_EINVAL;
+    pkv_plan_s* p = s->plan;
+    const int B = p->g.batch, mp = p->g.max_pages_per_seq, ps = p->page_size;
+    int rc = check_slot_rows(s->active_h, B, rows_h, n, false);
+    if (rc || n == 0) return rc;
+    int64_t tokens = 0;
+    if ((rc = check_admit_args(p, lens_h, n, k_src, v_src, &tokens))) return rc;
+    if (!k_pages || !v_pages || !aligned16(k_pages) || !aligned16(v_pages)) return PKV_EINVAL;
+    if ((rc = wait_session_staging(s))) return rc;
+    int32_t src_tok = 0;
+    if (!s->device_mode) {   // the host pool hands the pages out
+        int64_t need = 0;
+        for (int32_t i = 0; i < n; ++i) need += ceil_div(lens_h[i], ps);
+        if (static_cast<size_t>(need) > s->pool->free_list.size()) return PKV_ENOSPACE;
+        if (static_cast<size_t>(need) > s->req_pages_cap) {
+            cudaFreeHost(s->req_pages_h);
+            s->req_pages_h = nullptr;
+            s->req_pages_d = nullptr;
+            s->req_pages_cap = 0;
+            const size_t cap = std::max<size_t>(static_cast<size_t>(need), 64);
+            if (cudaHostAlloc(&s->req_pages_h, cap * sizeof(int32_t), cudaHostAllocMapped) != cudaSuccess)
+                return PKV_ENOMEM;
+            void* mapped = nullptr;
+            PKV_CUDA(cudaHostGetDevicePointer(&mapped, s->req_pages_h, 0));
+            s->req_pages_d = static_cast<const int32_t*>(mapped);
+            s->req_pages_cap = cap;
+        }
+        int32_t off = 0;
+        for (int32_t i = 0; i < n; ++i) {
+            const int32_t b = rows_h[i];
+            const int32_t want = static_cast<int32_t>(ceil_div(lens_h[i], ps));
+            for (int32_t j = 0; j < want; ++j) {
+                const int32_t page = s->pool->free_list.front();
+                s->pool->free_list.pop_front();
+                s->pool->is_free[page] = 0;
+                s->table_h[static_cast<size_t>(b) * mp + j] = page;
+                s->req_pages_h[off + j] = page;
+            }
+            s->lens_h[b] = lens_h[i];
+            s->req_h[i] = pkv::SlotRequest{b, lens_h[i], src_tok, off, static_cast<const uint16_t*>(k_src),
+                                           static_cast<const uint16_t*>(v_src)};
+            off += want;
+            src_tok += lens_h[i];
+            s->active_h[b] = 1;
+        }
+    } else {   // the device free list hands them out, in the slot kernel
+        for (int32_t i = 0; i < n; ++i) {
+            s->req_h[i] = pkv::SlotRequest{rows_h[i], lens_h[i], src_tok, -1, static_cast<const uint16_t*>(k_src),
+                                           static_cast<const uint16_t*>(v_src)};
+            src_tok += lens_h[i];
+            s->active_h[rows_h[i]] = 1;
+        }
+    }
+    return launch_slots(s, k_pages, v_pages, n, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int pkv_session_free_pages(pkv_session_t s, int32_t* pages_h, int32_t capacity, int32_t* count, int32_t* active_h) {
+    if (!s || !count || s->resident || capacity < 0 || (capacity > 0 && !pages_h)) return PKV_EINVAL;
+    const int B = s->plan->g.batch;
+    if (!s->device_mode) {
+        *count = static_cast<int32_t>(s->pool->free_list.size());
+        int32_t i = 0;
+        for (auto it = s->pool->free_list.begin(); it != s->pool->free_list.end() && i < capacity; ++it) pages_h[i++] = *it;
+        if (active_h)
+            for (int b = 0; b < B; ++b) active_h[b] = s->active_h[b];
+        return PKV_OK;
+    }
+    PKV_CUDA(cudaDeviceSynchronize());
+    uint32_t state[2] = {0, 0};
+    PKV_CUDA(cudaMemcpy(state, s->dev_free_state, sizeof(state), cudaMemcpyDeviceToHost));
+    std::vector<int32_t> ring(s->free_cap);
+    PKV_CUDA(cudaMemcpy(ring.data(), s->dev_free, ring.size() * sizeof(int32_t), cudaMemcpyDeviceToHost));
+    *count = static_cast<int32_t>(state[1]);
+    for (uint32_t i = 0; i < state[1] && static_cast<int32_t>(i) < capacity; ++i)
+        pages_h[i] = ring[(state[0] + i) % static_cast<uint32_t>(s->free_cap)];
+    if (active_h && B > 0) PKV_CUDA(cudaMemcpy(active_h, s->active_d, sizeof(int32_t) * B, cudaMemcpyDeviceToHost));
+    return PKV_OK;
+}
+
+}  // extern "C"
+
 // ------------------------------------------------------------------ resident steps
 
 namespace {
 void resident_free(pkv_resident_s* r) {
     if (!r) return;
     cudaFreeHost(r->ctl_h);
+    cudaFreeHost(r->req_h);
     cudaFree(r->grid_sync);
     cudaFree(r->times_d);
     if (r->kstream) cudaStreamDestroy(r->kstream);
@@ -1430,6 +1686,8 @@ int pkv_resident_start(pkv_session_t s, void* k_pages, void* v_pages, void* q_d,
     if (cudaStreamCreateWithFlags(&r->kstream, cudaStreamNonBlocking) != cudaSuccess ||
         cudaStreamCreateWithFlags(&r->cstream, cudaStreamNonBlocking) != cudaSuccess ||
         cudaHostAlloc(&r->ctl_h, sizeof(pkv::ResidentCtl), cudaHostAllocMapped) != cudaSuccess ||
+        cudaHostAlloc(&r->req_h, sizeof(pkv::SlotRequest) * PKV_RESIDENT_MAX_REQUESTS, cudaHostAllocMapped) !=
+            cudaSuccess ||
         cudaMalloc(&r->grid_sync, sizeof(uint32_t) * pkv::kSyncWords) != cudaSuccess ||
         cudaMalloc(&r->times_d, times_bytes) != cudaSuccess) {
         resident_free(r);
@@ -1437,6 +1695,9 @@ int pkv_resident_start(pkv_session_t s, void* k_pages, void* v_pages, void* q_d,
     }
     memset(r->ctl_h, 0, sizeof(pkv::ResidentCtl));
     cudaError_t e = cudaHostGetDevicePointer(reinterpret_cast<void**>(&r->ctl_d), r->ctl_h, 0);
+    void* req_mapped = nullptr;
+    if (e == cudaSuccess) e = cudaHostGetDevicePointer(&req_mapped, r->req_h, 0);
+    r->req_d = static_cast<const pkv::SlotRequest*>(req_mapped);
     if (e == cudaSuccess) e = cudaMemset(r->grid_sync, 0, sizeof(uint32_t) * pkv::kSyncWords);
     if (e == cudaSuccess) e = cudaMemset(r->times_d, 0, times_bytes);
     // the kernel takes over the session's device state: earlier work on any stream must be done
@@ -1461,6 +1722,8 @@ int pkv_resident_start(pkv_session_t s, void* k_pages, void* v_pages, void* q_d,
     pkv::ResidentParams rp{};
     rp.attn = a;
     rp.plan = dp;
+    rp.slots = slot_params(s, k_pages, v_pages, 0);
+    rp.slots.req = r->req_d;
     rp.k_new = static_cast<const uint16_t*>(k_new_d);
     rp.v_new = static_cast<const uint16_t*>(v_new_d);
     rp.k_pages_w = static_cast<uint16_t*>(k_pages);
@@ -1490,6 +1753,7 @@ int pkv_resident_step(pkv_resident_t r, const void* q_h, const void* k_new_h, co
     if (k_new_h) PKV_CUDA(cudaMemcpyAsync(r->k_new_d, k_new_h, r->new_bytes, cudaMemcpyHostToDevice, r->cstream));
     if (v_new_h) PKV_CUDA(cudaMemcpyAsync(r->v_new_d, v_new_h, r->new_bytes, cudaMemcpyHostToDevice, r->cstream));
     PKV_CUDA(cudaStreamSynchronize(r->cstream));
+    host_store(&r->ctl_h->requests, static_cast<uint32_t>(r->n_req));   // the requests staged for this step
     const uint32_t step = ++r->step;
     host_store(&r->ctl_h->step, step);
     const auto t0 = std::chrono::steady_clock::now();
@@ -1497,9 +1761,43 @@ int pkv_resident_step(pkv_resident_t r, const void* q_h, const void* k_new_h, co
         if (host_load(&r->ctl_h->exited)) return PKV_EDEVICE;   // the kernel left its loop (see pkv_status)
         if (std::chrono::steady_clock::now() - t0 > std::chrono::nanoseconds(wait_limit_ns)) return PKV_EDEVICE;
     }
+    r->n_req = 0;   // applied by the step
+    host_store(&r->ctl_h->requests, 0u);
     if (out_h) PKV_CUDA(cudaMemcpyAsync(out_h, r->out_d, r->out_bytes, cudaMemcpyDeviceToHost, r->cstream));
     if (lse_h) PKV_CUDA(cudaMemcpyAsync(lse_h, r->lse_d, r->lse_bytes, cudaMemcpyDeviceToHost, r->cstream));
     if (out_h || lse_h) PKV_CUDA(cudaStreamSynchronize(r->cstream));
+    return PKV_OK;
+}
+
+int pkv_resident_evict(pkv_resident_t r, const int32_t* rows_h, int32_t n) {
+    if (!r || !r->running) return PKV_EINVAL;
+    pkv_session_t s = r->session;
+    int rc = check_slot_rows(s->active_h, s->plan->g.batch, rows_h, n, true);
+    if (rc) return rc;
+    if (r->n_req + n > PKV_RESIDENT_MAX_REQUESTS) return PKV_ENOSPACE;
+    for (int32_t i = 0; i < n; ++i) {
+        r->req_h[r->n_req++] = pkv::SlotRequest{rows_h[i], -1, 0, 0, nullptr, nullptr};
+        s->active_h[rows_h[i]] = 0;
+    }
+    return PKV_OK;
+}
+
+int pkv_resident_admit(pkv_resident_t r, const int32_t* rows_h, const int32_t* lens_h, int32_t n, const void* k_src,
+                       const void* v_src) {
+    if (!r || !r->running) return PKV_EINVAL;
+    pkv_session_t s = r->session;
+    int rc = check_slot_rows(s->active_h, s->plan->g.batch, rows_h, n, false);
+    if (rc) return rc;
+    int64_t tokens = 0;
+    if ((rc = check_admit_args(s->plan, lens_h, n, k_src, v_src, &tokens))) return rc;
+    if (r->n_req + n > PKV_RESIDENT_MAX_REQUESTS) return PKV_ENOSPACE;
+    int32_t src_tok = 0;
+    for (int32_t i = 0; i < n; ++i) {
+        r->req_h[r->n_req++] = pkv::SlotRequest{rows_h[i], lens_h[i], src_tok, -1, static_cast<const uint16_t*>(k_src),
+                                                static_cast<const uint16_t*>(v_src)};
+        src_tok += lens_h[i];
+        s->active_h[rows_h[i]] = 1;
+    }
     return PKV_OK;
 }
 

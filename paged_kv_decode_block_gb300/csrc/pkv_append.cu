@@ -13,14 +13,20 @@
 // outside the pool sets PKV_DEV_PAGE_OOB; either row is left unchanged.  The step variant
 // (append_step_kernel) also enters the rows' new pages in the table and moves
 // the step's plan from mapped pinned host memory into device memory, so that a
-// host-planned session step needs no copy-engine transfer.
+// host-planned session step needs no copy-engine transfer.  Rows marked idle in
+// an `active` mask (slots of a session between an eviction and an admission)
+// are skipped.  The slot kernels apply a batch of admissions and evictions
+// (pkv_slots.cuh).
 #include <cuda_runtime.h>
 #include <stdint.h>
 
 #include "pkv_internal.h"
+#include "pkv_slots.cuh"
 
 namespace pkv {
 namespace {
+
+constexpr int kSlotCopyCtas = 256;   // grid of the prompt copy (grid-stride over the tokens)
 
 // Append the new token of row b (all threads of the CTA).  `new_idx` / `new_page`:
 // a table entry to fill first (new_idx -1: none).
@@ -71,9 +77,20 @@ __global__ void __launch_bounds__(128) append_kernel(const uint16_t* __restrict_
                                                      uint16_t* __restrict__ k_pages, uint16_t* __restrict__ v_pages,
                                                      const int32_t* __restrict__ block_table,
                                                      int32_t* __restrict__ seq_lens, int Hkv, int D, int page_size,
-                                                     int max_pages, int num_pages, uint32_t* status) {
+                                                     int max_pages, int num_pages, uint32_t* status,
+                                                     const int32_t* __restrict__ active) {
+    if (active && !active[blockIdx.x]) return;   // an idle slot
     append_row(k_new, v_new, k_pages, v_pages, const_cast<int32_t*>(block_table), seq_lens, blockIdx.x, Hkv, D,
                page_size, max_pages, num_pages, status, -1, -1);
+}
+
+__global__ void __launch_bounds__(32) slot_apply_kernel(const SlotParams p) {
+    if (threadIdx.x == 0) slots::apply_requests(p);
+}
+
+__global__ void __launch_bounds__(256) slot_copy_kernel(const SlotParams p) {
+    slots::copy_prompts(p, static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x,
+                        static_cast<int64_t>(gridDim.x) * blockDim.x);
 }
 
 __global__ void __launch_bounds__(128) append_step_kernel(const AppendStepParams p) {
@@ -89,6 +106,7 @@ __global__ void __launch_bounds__(128) append_step_kernel(const AppendStepParams
         for (int64_t i = n4 * 4 + tid; i < p.plan_words; i += nth) p.plan_dst[i] = p.plan_src[i];
     }
     const int b = blockIdx.x;
+    if (p.active && !p.active[b]) return;   // an idle slot
     const int new_idx = p.new_pages[2 * b], new_page = p.new_pages[2 * b + 1];
     append_row(p.k_new, p.v_new, p.k_pages, p.v_pages, p.block_table, p.seq_lens, b, p.Hkv, p.D, p.page_size,
                p.max_pages, p.num_pages, p.status, new_idx, new_page);
@@ -98,10 +116,20 @@ __global__ void __launch_bounds__(128) append_step_kernel(const AppendStepParams
 
 cudaError_t launch_append(const uint16_t* k_new, const uint16_t* v_new, uint16_t* k_pages, uint16_t* v_pages,
                           const int32_t* block_table, int32_t* seq_lens, int B, int Hkv, int D, int page_size,
-                          int max_pages, int num_pages, uint32_t* status, cudaStream_t stream) {
+                          int max_pages, int num_pages, uint32_t* status, cudaStream_t stream,
+                          const int32_t* active) {
     if (B == 0) return cudaSuccess;
     append_kernel<<<B, 128, 0, stream>>>(k_new, v_new, k_pages, v_pages, block_table, seq_lens, Hkv, D, page_size,
-                                         max_pages, num_pages, status);
+                                         max_pages, num_pages, status, active);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_slot_requests(const SlotParams& p, cudaStream_t stream) {
+    if (p.n <= 0) return cudaSuccess;
+    slot_apply_kernel<<<1, 32, 0, stream>>>(p);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    slot_copy_kernel<<<kSlotCopyCtas, 256, 0, stream>>>(p);
     return cudaGetLastError();
 }
 

@@ -60,6 +60,7 @@
 
 #include "pkv_devplan.cuh"
 #include "pkv_internal.h"
+#include "pkv_slots.cuh"
 
 namespace pkv {
 namespace {
@@ -1597,6 +1598,18 @@ __global__ void __launch_bounds__(kThreads, MMA ? 2 : 1) resident_kernel(const R
             }
             __syncthreads();
             if (sm.tile_slot[0] == kCmdGo) {
+                // the step's slot requests (evictions, admissions) before its allocation and plan
+                if (threadIdx.x == 0) {
+                    const uint32_t n = min(*reinterpret_cast<volatile uint32_t*>(&rp.ctl->requests),
+                                           static_cast<uint32_t>(PKV_RESIDENT_MAX_REQUESTS));
+                    gs[kSyncReq] = n;
+                    if (n) {
+                        SlotParams sp = rp.slots;
+                        sp.n = static_cast<int32_t>(n);
+                        slots::apply_requests(sp);
+                    }
+                }
+                __syncthreads();
                 int* scratch = reinterpret_cast<int*>(&sm.k[0][0]);   // the idle ring
                 devplan::plan_step<kThreads>(rp.plan, scratch, scratch + kDevPlanMaxRows,
                                              scratch + 2 * kDevPlanMaxRows);
@@ -1611,8 +1624,16 @@ __global__ void __launch_bounds__(kThreads, MMA ? 2 : 1) resident_kernel(const R
         if (*reinterpret_cast<volatile uint32_t*>(gs + kSyncCmd) != kCmdGo) break;
         if (blockIdx.x == 0 && threadIdx.x == 0 && rp.times) rp.times[4 * ((step - 1) % rp.times_cap) + 1] = globaltimer_ns();
 
-        // ---- 2. append: every CTA takes rows blockIdx.x, blockIdx.x + gridDim.x, ...
+        // ---- 2. the admitted rows' prompts, then the append: every CTA takes rows
+        // blockIdx.x, blockIdx.x + gridDim.x, ... (idle slots are left alone)
+        if (const int nreq = static_cast<int>(*reinterpret_cast<volatile uint32_t*>(gs + kSyncReq))) {
+            SlotParams sp = rp.slots;
+            sp.n = nreq;
+            slots::copy_prompts(sp, static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x,
+                                static_cast<int64_t>(gridDim.x) * kThreads);
+        }
         for (int b = blockIdx.x; b < p.B; b += gridDim.x) {
+            if (rp.plan.active && !rp.plan.active[b]) continue;   // uniform over the CTA
             if (threadIdx.x == 0) {
                 const int pos = rp.lens_w[b];
                 int page = -1;

@@ -62,7 +62,7 @@ __device__ void plan_step(const DevPlanParams& p, int* s_pages, int* s_partial, 
     for (int i = 0; i < kRowsPerThread; ++i) {
         const int b = r0 + i;
         need[i] = 0;
-        if (b < B) {
+        if (b < B && (!p.active || p.active[b])) {   // idle slots take no page
             const int n = p.lens[b];
             if (n >= 0 && n % ps == 0) {
                 if (n / ps >= p.max_pages)
@@ -104,7 +104,7 @@ __device__ void plan_step(const DevPlanParams& p, int* s_pages, int* s_partial, 
         const int b = r0 + i;
         splits[i] = fulls[i] = 0;
         if (b < B) {
-            const int n = max(p.lens[b], 0) + 1;
+            const int n = max(p.lens[b], 0) + (!p.active || p.active[b] ? 1 : 0);   // idle slots do not grow
             const int pages = (n + ps - 1) / ps;
             splits[i] = (pages + C - 1) / C;
             const int rem = pages % C;

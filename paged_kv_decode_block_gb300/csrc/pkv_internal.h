@@ -98,6 +98,7 @@ struct AttnParams {
 constexpr int kDevPlanMaxRows = 2048;
 struct DevPlanParams {
     const int32_t* lens;        // [B] lengths before the append
+    const int32_t* active;      // [B] 1: the row takes this step's token; 0: idle slot (null: all active)
     int32_t* table;             // [B][max_pages] device block table (entries filled in)
     const int32_t* free_list;   // [free_cap] free page ids, handed out in order
     uint32_t* free_state;       // {next index into free_list, pages still free}
@@ -119,10 +120,11 @@ cudaError_t launch_plan_step(const DevPlanParams& p, cudaStream_t stream);
 cudaError_t launch_attention(const AttnParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap,
                              int grid, cudaStream_t stream, bool cooperative = false);
 cudaError_t launch_merge(const AttnParams& p, cudaStream_t stream);
+// `active` (nullable, [B]): rows with 0 are idle slots and are left alone.
 cudaError_t launch_append(const uint16_t* k_new, const uint16_t* v_new, uint16_t* k_pages,
                           uint16_t* v_pages, const int32_t* block_table, int32_t* seq_lens,
                           int B, int Hkv, int D, int page_size, int max_pages, int num_pages,
-                          uint32_t* status, cudaStream_t stream);
+                          uint32_t* status, cudaStream_t stream, const int32_t* active = nullptr);
 // One step of a host-planned continuous session in one launch: the new page
 // of every row that starts one is entered in the table, the step's plan is
 // copied from its pinned host staging into the plan's device buffer (the
@@ -137,6 +139,7 @@ struct AppendStepParams {
     int32_t* block_table;       // [B][max_pages]
     int32_t* seq_lens;          // [B]
     const int32_t* new_pages;   // [B][2]: (table index, page id) of the row's new page, or index -1
+    const int32_t* active;      // [B] 0: idle slot, left alone (null: all active)
     const int32_t* plan_src;    // plan staging (nullable: nothing to copy)
     int32_t* plan_dst;
     int64_t plan_words;         // int32 words of plan to copy
@@ -144,6 +147,35 @@ struct AppendStepParams {
     int32_t B, Hkv, D, page_size, max_pages, num_pages;
 };
 cudaError_t launch_append_step(const AppendStepParams& p, cudaStream_t stream);
+// Slot admit / evict (pkv_session_evict / pkv_session_admit / pkv_resident_*).
+// One request per row; evictions are applied before admissions, each in the
+// order listed.  32 bytes.
+struct SlotRequest {
+    int32_t row;
+    int32_t len;                // -1: evict; >= 0: admit with a prompt of this many tokens
+    int32_t src_tok;            // admit: the row's first token in k_src / v_src
+    int32_t page_off;           // admit from the host pool: the row's first page in SlotParams::pages
+    const uint16_t* k_src;      // admit: bf16 [tokens][Hkv][D] prompt K (device memory)
+    const uint16_t* v_src;
+};
+struct SlotParams {
+    const SlotRequest* req;     // [n] (device view; mapped pinned host memory)
+    int32_t n;
+    const int32_t* pages;       // host-pool admissions: the page ids chosen on the host (device view)
+    int32_t* free_list;         // device free list ring [free_cap] (null: the host pool chose the pages)
+    uint32_t* free_state;       // {index of its front, pages in it}
+    int32_t free_cap;
+    int32_t* table;             // [B][max_pages]
+    int32_t* lens;              // [B]
+    int32_t* active;            // [B]
+    uint16_t* k_pages;
+    uint16_t* v_pages;
+    uint32_t* status;
+    int32_t B, Hkv, D, page_size, max_pages, num_pages;
+};
+// The bookkeeping (one CTA), then the copy of the admitted prompts (a grid).
+cudaError_t launch_slot_requests(const SlotParams& p, cudaStream_t stream);
+
 // Bounded-wait self-test (see pkv_selftest_wait): result[3] = {wait returned true,
 // abort flag raised, second wait returned true}.
 cudaError_t launch_wait_selftest(uint32_t* status, uint64_t limit_ns, int* result, cudaStream_t stream);
@@ -152,16 +184,19 @@ cudaError_t launch_wait_selftest(uint32_t* status, uint64_t limit_ns, int* resul
 // stays on the GPU and runs a step (plan, append, decode) each time the host
 // publishes one.  The control block lives in mapped pinned host memory.
 struct ResidentCtl {
-    uint32_t step;     // host: the last step it has published (1, 2, ...)
-    uint32_t stop;     // host: 1 = leave the loop instead of waiting for another step
-    uint32_t done;     // kernel: the last step whose outputs are written
-    uint32_t exited;   // kernel: 1 once it has left the loop; 2 if it left on an error
+    uint32_t step;       // host: the last step it has published (1, 2, ...)
+    uint32_t stop;       // host: 1 = leave the loop instead of waiting for another step
+    uint32_t done;       // kernel: the last step whose outputs are written
+    uint32_t exited;     // kernel: 1 once it has left the loop; 2 if it left on an error
+    uint32_t requests;   // host: slot requests to apply at the start of the published step
+    uint32_t pad[3];
 };
 // grid_sync words (device memory, zero before the launch)
-enum ResidentSync { kSyncCount = 0, kSyncGen = 1, kSyncCmd = 2, kSyncAbort = 3, kSyncWords = 4 };
+enum ResidentSync { kSyncCount = 0, kSyncGen = 1, kSyncCmd = 2, kSyncAbort = 3, kSyncReq = 4, kSyncWords = 5 };
 struct ResidentParams {
     AttnParams attn;            // persistent route over the device plan below
     DevPlanParams plan;         // allocation + plan of each step (lengths before its append)
+    SlotParams slots;           // the step's slot requests (req, n from the control block)
     const uint16_t* k_new;      // device bf16 [B][Hkv][D]: the step's new token per row
     const uint16_t* v_new;
     uint16_t* k_pages_w;        // the pools and lengths, writable (the append)

@@ -107,6 +107,11 @@ SIGNATURES = {
     "pkv_resident_stop": (ctypes.c_int, [_P]),
     "pkv_resident_times": (ctypes.c_int, [_P, ctypes.POINTER(ctypes.c_uint64), _I32, _I32P]),
     "pkv_resident_destroy": (None, [_P]),
+    "pkv_session_evict": (ctypes.c_int, [_P, _I32P, _I32, _P]),
+    "pkv_session_admit": (ctypes.c_int, [_P, _I32P, _I32P, _I32, _P, _P, _P, _P, _P]),
+    "pkv_session_free_pages": (ctypes.c_int, [_P, _I32P, _I32, _I32P, _I32P]),
+    "pkv_resident_evict": (ctypes.c_int, [_P, _I32P, _I32]),
+    "pkv_resident_admit": (ctypes.c_int, [_P, _I32P, _I32P, _I32, _P, _P]),
     "pkv_strerror": (ctypes.c_char_p, [ctypes.c_int]),
     "pkv_last_cuda_error": (ctypes.c_int, []),
 }
@@ -479,6 +484,35 @@ class Session:
         arr = np.ctypeslib.as_array(ctypes.cast(items, _I32P), shape=(max(n.value, 1) * 5,))
         return arr[: n.value * 5].reshape(-1, 5).copy(), order[: n.value].copy()
 
+    def evict(self, rows, stream=None):
+        """pkv_session_evict: the rows become idle; their pages go back to the free list."""
+        r = _i32(rows)
+        _check(load().pkv_session_evict(self._h, _ptr_i32(r), len(r), _stream_handle(stream)), "pkv_session_evict")
+
+    def admit(self, rows, lens, k_src, v_src, k_pages, v_pages, stream=None):
+        """pkv_session_admit: idle rows take new sessions of `lens` tokens whose K/V
+        (device bf16 [sum(lens)][Hkv][D], rows one after another) is copied into fresh pages."""
+        bf = _bf16_types()
+        r, n = _i32(rows), _i32(lens)
+        if len(r) != len(n):
+            raise ValueError("rows and lens differ in length")
+        _check(load().pkv_session_admit(self._h, _ptr_i32(r), _ptr_i32(n), len(r),
+                                        _dev_ptr(k_src, "k_src", bf) if k_src is not None else None,
+                                        _dev_ptr(v_src, "v_src", bf) if v_src is not None else None,
+                                        _dev_ptr(k_pages, "k_pages", bf), _dev_ptr(v_pages, "v_pages", bf),
+                                        _stream_handle(stream)), "pkv_session_admit")
+
+    def free_pages(self):
+        """(free list front first, active flags [B]) -- pkv_session_free_pages."""
+        n = ctypes.c_int32(0)
+        active = np.zeros(max(self.B, 1), np.int32)
+        _check(load().pkv_session_free_pages(self._h, None, 0, ctypes.byref(n), _ptr_i32(active)),
+               "pkv_session_free_pages")
+        pages = np.zeros(max(n.value, 1), np.int32)
+        _check(load().pkv_session_free_pages(self._h, _ptr_i32(pages), n.value, ctypes.byref(n), None),
+               "pkv_session_free_pages")
+        return pages[: n.value].copy(), active[: self.B].copy()
+
     def close(self):
         if getattr(self, "_h", None) is not None and _lib is not None:
             _lib.pkv_session_destroy(self._h)
@@ -533,6 +567,24 @@ class Resident:
 
     def stop(self):
         _check(load().pkv_resident_stop(self._h), "pkv_resident_stop")
+
+    def evict(self, rows):
+        """pkv_resident_evict: applied at the start of the next step."""
+        r = _i32(rows)
+        _check(load().pkv_resident_evict(self._h, _ptr_i32(r), len(r)), "pkv_resident_evict")
+
+    def admit(self, rows, lens, k_src, v_src):
+        """pkv_resident_admit: applied at the start of the next step (k_src / v_src device
+        bf16 [sum(lens)][Hkv][D], kept alive until that step returns)."""
+        bf = _bf16_types()
+        r, n = _i32(rows), _i32(lens)
+        if len(r) != len(n):
+            raise ValueError("rows and lens differ in length")
+        self._admit_src = (k_src, v_src)
+        _check(load().pkv_resident_admit(self._h, _ptr_i32(r), _ptr_i32(n), len(r),
+                                         _dev_ptr(k_src, "k_src", bf) if k_src is not None else None,
+                                         _dev_ptr(v_src, "v_src", bf) if v_src is not None else None),
+               "pkv_resident_admit")
 
     def times(self) -> np.ndarray:
         """[steps][4] globaltimer ns of each step (after stop): seen, planned, appended,
