@@ -474,19 +474,25 @@ int pkv_session_free_pages(pkv_session_t session, int32_t *pages_h, int32_t capa
  * publishes one through a control block in mapped pinned host memory.  A step
  * is what a device-planned pkv_session_step enqueues -- page allocation and
  * plan (the device planner), the append of k_new / v_new, the persistent
- * decode of q into out / lse -- separated by grid-wide barriers instead of
- * launches, in the spirit of the persistent worker of "GPUOS" (arXiv
- * 2604.17861, section 4.1) and the resident beat of "WPK persistent kernel"
- * (dotwave.ai).
+ * decode of q into out / lse -- with one grid-wide barrier (after the plan)
+ * instead of launches: each row is marked ready once its token is appended and
+ * its tiles wait for that mark, and the last CTA to finish the decode
+ * publishes the step; in the spirit of the persistent worker of "GPUOS"
+ * (arXiv 2604.17861, section 4.1) and the resident beat of "WPK persistent
+ * kernel" (dotwave.ai).  yield_every (the GPUOS host API's set_yield_every,
+ * section 4, Table 1) bounds how long the kernel holds the GPU: after that many
+ * steps it leaves, and the next pkv_resident_step launches it again (0: it
+ * stays until pkv_resident_stop).
  *   pkv_resident_start   session in device-plan mode; k_pages / v_pages the
  *                        pools; q_d, k_new_d, v_new_d, out_d, lse_d device
  *                        buffers of the step's inputs and outputs (caller
  *                        owned, bound for the kernel's life); idle_limit_ns
  *                        (0, 60 s]: the longest the kernel waits for the next
  *                        step before leaving with PKV_DEV_TIMEOUT; times_cap:
- *                        steps whose device start / end times are kept.
- *                        Synchronises the device first.  PKV_EUNSUPPORTED if
- *                        the kernel cannot be resident on this device
+ *                        steps whose device start / end times are kept;
+ *                        yield_every >= 0 as above.  Synchronises the device
+ *                        first.  PKV_EUNSUPPORTED if the kernel cannot be
+ *                        resident on this device
  *   pkv_resident_step    copies the host inputs given (pinned host pointers, or
  *                        NULL to keep the device buffer) to the bound buffers,
  *                        publishes the step, waits (at most wait_limit_ns) for
@@ -501,16 +507,19 @@ int pkv_session_free_pages(pkv_session_t session, int32_t *pages_h, int32_t capa
  *                        step index modulo times_cap)
  * While a resident kernel runs, the session refuses pkv_session_step and its
  * read-back calls (PKV_EINVAL), and no other kernel should be queued behind it
- * on the device: it holds every SM until it is stopped.
+ * on the device: it holds every SM until it is stopped or yields.  Between a
+ * yield and the next step the GPU is free for other work.
  */
 typedef struct pkv_resident_s *pkv_resident_t;
 int pkv_resident_start(pkv_session_t session, void *k_pages, void *v_pages, void *q_d, void *k_new_d,
                        void *v_new_d, float *out_d, float *lse_d, int64_t idle_limit_ns, int32_t times_cap,
-                       pkv_resident_t *resident);
+                       int32_t yield_every, pkv_resident_t *resident);
 int pkv_resident_step(pkv_resident_t resident, const void *q_h, const void *k_new_h, const void *v_new_h,
                       float *out_h, float *lse_h, int64_t wait_limit_ns);
 int pkv_resident_stop(pkv_resident_t resident);
 int pkv_resident_times(pkv_resident_t resident, uint64_t *stamps_ns, int32_t capacity, int32_t *count);
+/* Launches of the resident kernel so far (1 + the relaunches after yields). */
+int pkv_resident_launches(pkv_resident_t resident, int32_t *launches);
 void pkv_resident_destroy(pkv_resident_t resident);
 /* Slot requests for a running resident kernel, applied at the start of the next
  * pkv_resident_step, before its page allocation and plan: the same evictions and

@@ -1121,6 +1121,13 @@ struct pkv_resident_s {
     pkv::SlotRequest* req_h = nullptr;   // pinned, mapped slot requests for the next step
     const pkv::SlotRequest* req_d = nullptr;
     int32_t n_req = 0;
+    uint32_t* row_ready = nullptr;       // device [B]: the last step whose append of the row landed
+    pkv::ResidentParams rp{};            // the launch's parameters (relaunched after a yield)
+    int grid = 0;
+    int32_t yield_every = 0;
+    uint32_t launch_first = 1;           // the first step of the current launch
+    bool yielded = false;                // the kernel left the GPU after yield_every steps
+    int32_t launches = 0;
 };
 
 namespace {
@@ -1640,6 +1647,7 @@ void resident_free(pkv_resident_s* r) {
     if (!r) return;
     cudaFreeHost(r->ctl_h);
     cudaFreeHost(r->req_h);
+    cudaFree(r->row_ready);
     cudaFree(r->grid_sync);
     cudaFree(r->times_d);
     if (r->kstream) cudaStreamDestroy(r->kstream);
@@ -1652,12 +1660,13 @@ void host_store(uint32_t* p, uint32_t v) { __atomic_store_n(p, v, __ATOMIC_SEQ_C
 }  // namespace
 
 int pkv_resident_start(pkv_session_t s, void* k_pages, void* v_pages, void* q_d, void* k_new_d, void* v_new_d,
-                       float* out_d, float* lse_d, int64_t idle_limit_ns, int32_t times_cap, pkv_resident_t* out) {
+                       float* out_d, float* lse_d, int64_t idle_limit_ns, int32_t times_cap, int32_t yield_every,
+                       pkv_resident_t* out) {
     NvtxRange range("pkv_resident_start");
     if (!out) return PKV_EINVAL;
     *out = nullptr;
     if (!s || !s->device_mode || s->resident || !k_pages || !v_pages || !q_d || !k_new_d || !v_new_d || !out_d ||
-        !lse_d || idle_limit_ns <= 0 || idle_limit_ns > 60000000000ll || times_cap < 0)
+        !lse_d || idle_limit_ns <= 0 || idle_limit_ns > 60000000000ll || times_cap < 0 || yield_every < 0)
         return PKV_EINVAL;
     if (!aligned16(k_new_d) || !aligned16(v_new_d)) return PKV_EINVAL;
     pkv_plan_s* p = s->plan;
@@ -1689,6 +1698,7 @@ int pkv_resident_start(pkv_session_t s, void* k_pages, void* v_pages, void* q_d,
         cudaHostAlloc(&r->req_h, sizeof(pkv::SlotRequest) * PKV_RESIDENT_MAX_REQUESTS, cudaHostAllocMapped) !=
             cudaSuccess ||
         cudaMalloc(&r->grid_sync, sizeof(uint32_t) * pkv::kSyncWords) != cudaSuccess ||
+        cudaMalloc(&r->row_ready, sizeof(uint32_t) * g.batch) != cudaSuccess ||
         cudaMalloc(&r->times_d, times_bytes) != cudaSuccess) {
         resident_free(r);
         return PKV_ENOMEM;
@@ -1699,6 +1709,7 @@ int pkv_resident_start(pkv_session_t s, void* k_pages, void* v_pages, void* q_d,
     if (e == cudaSuccess) e = cudaHostGetDevicePointer(&req_mapped, r->req_h, 0);
     r->req_d = static_cast<const pkv::SlotRequest*>(req_mapped);
     if (e == cudaSuccess) e = cudaMemset(r->grid_sync, 0, sizeof(uint32_t) * pkv::kSyncWords);
+    if (e == cudaSuccess) e = cudaMemset(r->row_ready, 0, sizeof(uint32_t) * g.batch);
     if (e == cudaSuccess) e = cudaMemset(r->times_d, 0, times_bytes);
     // the kernel takes over the session's device state: earlier work on any stream must be done
     if (e == cudaSuccess) e = cudaDeviceSynchronize();
@@ -1734,11 +1745,18 @@ int pkv_resident_start(pkv_session_t s, void* k_pages, void* v_pages, void* q_d,
     rp.times = times_cap > 0 ? r->times_d : nullptr;
     rp.times_cap = std::max(times_cap, 1);
     rp.idle_limit_ns = static_cast<uint64_t>(idle_limit_ns);
-    e = pkv::launch_resident(rp, p->kmap, p->vmap, dev_sms * per_sm, r->kstream);
+    rp.row_ready = r->row_ready;
+    rp.first_step = 1;
+    rp.yield_every = yield_every;
+    r->rp = rp;
+    r->grid = dev_sms * per_sm;
+    r->yield_every = yield_every;
+    e = pkv::launch_resident(rp, p->kmap, p->vmap, r->grid, r->kstream);
     if (e != cudaSuccess) {
         resident_free(r);
         return cuda_fail(e);
     }
+    r->launches = 1;
     r->running = true;
     s->resident = r;
     *out = r;
@@ -1753,16 +1771,34 @@ int pkv_resident_step(pkv_resident_t r, const void* q_h, const void* k_new_h, co
     if (k_new_h) PKV_CUDA(cudaMemcpyAsync(r->k_new_d, k_new_h, r->new_bytes, cudaMemcpyHostToDevice, r->cstream));
     if (v_new_h) PKV_CUDA(cudaMemcpyAsync(r->v_new_d, v_new_h, r->new_bytes, cudaMemcpyHostToDevice, r->cstream));
     PKV_CUDA(cudaStreamSynchronize(r->cstream));
+    if (r->yielded) {   // the kernel left the GPU after its last step: launch it again from this step
+        pkv_plan_s* p = r->session->plan;
+        r->rp.first_step = r->step + 1;
+        host_store(&r->ctl_h->exited, 0u);
+        PKV_CUDA(pkv::launch_resident(r->rp, p->kmap, p->vmap, r->grid, r->kstream));
+        r->launch_first = r->step + 1;
+        r->yielded = false;
+        ++r->launches;
+    }
     host_store(&r->ctl_h->requests, static_cast<uint32_t>(r->n_req));   // the requests staged for this step
     const uint32_t step = ++r->step;
     host_store(&r->ctl_h->step, step);
     const auto t0 = std::chrono::steady_clock::now();
     while (host_load(&r->ctl_h->done) < step) {
-        if (host_load(&r->ctl_h->exited)) return PKV_EDEVICE;   // the kernel left its loop (see pkv_status)
+        // the kernel left its loop on an error (see pkv_status); a yield (3) comes only after this
+        // step, whose outputs its last CTA is still publishing
+        const uint32_t ex = host_load(&r->ctl_h->exited);
+        if (ex != 0u && ex != 3u) return PKV_EDEVICE;
         if (std::chrono::steady_clock::now() - t0 > std::chrono::nanoseconds(wait_limit_ns)) return PKV_EDEVICE;
     }
     r->n_req = 0;   // applied by the step
     host_store(&r->ctl_h->requests, 0u);
+    if (r->yield_every > 0 && (step - r->launch_first + 1) % static_cast<uint32_t>(r->yield_every) == 0) {
+        // this launch's last step: the kernel is leaving; the GPU is free until the next step
+        PKV_CUDA(cudaStreamSynchronize(r->kstream));
+        if (host_load(&r->ctl_h->exited) != 3u) return PKV_EDEVICE;
+        r->yielded = true;
+    }
     if (out_h) PKV_CUDA(cudaMemcpyAsync(out_h, r->out_d, r->out_bytes, cudaMemcpyDeviceToHost, r->cstream));
     if (lse_h) PKV_CUDA(cudaMemcpyAsync(lse_h, r->lse_d, r->lse_bytes, cudaMemcpyDeviceToHost, r->cstream));
     if (out_h || lse_h) PKV_CUDA(cudaStreamSynchronize(r->cstream));
@@ -1805,7 +1841,7 @@ int pkv_resident_stop(pkv_resident_t r) {
     if (!r) return PKV_EINVAL;
     if (!r->running) return PKV_OK;
     host_store(&r->ctl_h->stop, 1u);
-    cudaError_t e = cudaStreamSynchronize(r->kstream);
+    cudaError_t e = cudaStreamSynchronize(r->kstream);   // returns at once after a yield
     r->running = false;
     r->session->resident = nullptr;
     // the persistent route expects its queue counters rewound
@@ -1813,6 +1849,12 @@ int pkv_resident_stop(pkv_resident_t r) {
     if (e == cudaSuccess) e = cudaDeviceSynchronize();
     if (e != cudaSuccess) return cuda_fail(e);
     return host_load(&r->ctl_h->exited) == 2u ? PKV_EDEVICE : PKV_OK;
+}
+
+int pkv_resident_launches(pkv_resident_t r, int32_t* launches) {
+    if (!r || !launches) return PKV_EINVAL;
+    *launches = r->launches;
+    return PKV_OK;
 }
 
 int pkv_resident_times(pkv_resident_t r, uint64_t* stamps_ns, int32_t capacity, int32_t* count) {

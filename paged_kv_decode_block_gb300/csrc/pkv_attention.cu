@@ -235,6 +235,10 @@ __device__ __forceinline__ void st_release_sys(uint32_t* p, uint32_t v) {
 
 __device__ __forceinline__ void fence_sc_sys() { asm volatile("fence.sc.sys;" ::: "memory"); }
 
+// Order earlier generic-proxy accesses (as acquired from another CTA) before
+// later async-proxy (TMA) accesses to global memory.
+__device__ __forceinline__ void fence_proxy_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
+
 // Release / acquire fence at GPU scope (message passing between CTAs).
 __device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
 
@@ -1498,11 +1502,18 @@ __global__ void __launch_bounds__(kThreads, MMA ? 2 : 1) attention_kernel(const 
 // as the persistent worker of "GPUOS" (arXiv 2604.17861, section 4.1) and the
 // resident beat of "WPK persistent kernel" (dotwave.ai) do.  Per step:
 //   CTA 0 waits (bounded) for the host to publish the step in the mapped
-//   control block, then allocates pages and builds the plan (the device
-//   planner of pkv_devplan.cuh) -- grid barrier -- every CTA appends the new
-//   tokens of its rows -- grid barrier -- the CTAs drain the step's queue as
-//   the persistent route does (fused last-arriver merge) -- grid barrier --
-//   CTA 0 publishes the step's outputs to the host (system-scope release).
+//   control block, applies its slot requests, then allocates pages and builds
+//   the plan (the device planner of pkv_devplan.cuh) -- grid barrier -- every
+//   CTA appends the new tokens of its rows and marks each row ready (a release
+//   store of the step number) -- the CTAs drain the step's queue as the
+//   persistent route does (fused last-arriver merge), each tile first waiting
+//   (acquire, bounded) until its row is marked ready -- the last CTA to finish
+//   publishes the step's outputs to the host (system-scope release).  One grid
+//   barrier per step; a step that admits new sessions also has one after the
+//   prompt copy, which every CTA shares.  The host publishes the next step only
+//   after this one, so the next plan never overwrites a queue still in use.
+// With yield_every > 0 the kernel leaves the GPU after that many steps (exited =
+// 3), so that a long session does not hold every SM; the host relaunches it.
 // Every wait is bounded: the host wait by idle_limit_ns, a grid barrier by
 // kWaitLimitNs; on expiry the status word gets PKV_DEV_TIMEOUT, the abort word
 // is raised and every CTA leaves the loop at its next barrier.
@@ -1582,8 +1593,8 @@ __global__ void __launch_bounds__(kThreads, MMA ? 2 : 1) resident_kernel(const R
     }
     __syncthreads();
     uint32_t pipe = 0;
-    bool failed = false;
-    for (uint32_t step = 1;; ++step) {
+    bool failed = false, yielded = false;
+    for (uint32_t step = rp.first_step;; ++step) {
         // ---- 1. CTA 0: the host's step, then allocation and plan
         if (blockIdx.x == 0) {
             if (threadIdx.x == 0) {
@@ -1663,9 +1674,12 @@ __global__ void __launch_bounds__(kThreads, MMA ? 2 : 1) resident_kernel(const R
                 }
                 if (threadIdx.x == 0) rp.lens_w[b] = sm.append_pos + 1;
             }
-            __syncthreads();
+            __syncthreads();   // the row's writes are done: mark it ready for the drain
+            if (threadIdx.x == 0) st_release_gpu(rp.row_ready + b, step);
         }
-        if (!grid_barrier<D, G>(sm, gs, status)) {
+        // admitted prompts are copied by every CTA: the drain waits for all of them
+        const bool prompts = *reinterpret_cast<volatile uint32_t*>(gs + kSyncReq) != 0;
+        if (prompts && !grid_barrier<D, G>(sm, gs, status)) {
             failed = true;
             break;
         }
@@ -1674,7 +1688,16 @@ __global__ void __launch_bounds__(kThreads, MMA ? 2 : 1) resident_kernel(const R
         if (blockIdx.x == 0 && threadIdx.x == 0 && rp.times) rp.times[4 * ((step - 1) % rp.times_cap) + 2] = globaltimer_ns();
         const int num_tiles = *p.tiles_d;
         while (true) {
-            if (threadIdx.x == 0) sm.tile_slot[0] = static_cast<int>(atomicAdd(&p.ctr->next_tile, 1u));
+            if (threadIdx.x == 0) {
+                const int t = static_cast<int>(atomicAdd(&p.ctr->next_tile, 1u));
+                sm.tile_slot[0] = t;
+                // the tile's row must have its new token (acquire of the appender's release)
+                if (t < num_tiles && !prompts) {
+                    const uint32_t* flag = rp.row_ready + p.queue[p.order[t]].b;
+                    if (ld_acquire_gpu(flag) < step) wait_count(flag, step, status, &sm.abort);
+                    if (!p.copy_lsu) fence_proxy_async_global();   // TMA reads what plain stores wrote
+                }
+            }
             __syncthreads();
             const int t = sm.tile_slot[0];
             if (t >= num_tiles) break;
@@ -1688,22 +1711,28 @@ __global__ void __launch_bounds__(kThreads, MMA ? 2 : 1) resident_kernel(const R
         for (int b = blockIdx.x; b < p.B; b += gridDim.x)
             if (p.row_splits[b] == 0) write_neutral_row(p, b, threadIdx.x, blockDim.x);
         if (sm.abort) atomicExch(gs + kSyncAbort, 1u);   // a bounded wait of this CTA ran out
-        if (!grid_barrier<D, G>(sm, gs, status)) {
-            failed = true;
-            break;
-        }
+        __syncthreads();   // this CTA's outputs of the step are written
 
-        // ---- 4. CTA 0: the step's outputs are written; tell the host
-        if (blockIdx.x == 0 && threadIdx.x == 0) {
-            if (rp.times) rp.times[4 * ((step - 1) % rp.times_cap) + 3] = globaltimer_ns();
-            fence_sc_sys();
-            st_release_sys(&rp.ctl->done, step);
+        // ---- 4. the last CTA done publishes the step's outputs to the host
+        if (threadIdx.x == 0) {
+            fence_acq_rel_gpu();   // release this CTA's outputs before its count
+            if (atomicAdd(gs + kSyncDone, 1u) == gridDim.x - 1) {
+                fence_acq_rel_gpu();   // acquire every other CTA's outputs
+                gs[kSyncDone] = 0;
+                if (rp.times) rp.times[4 * ((step - 1) % rp.times_cap) + 3] = globaltimer_ns();
+                fence_sc_sys();
+                st_release_sys(&rp.ctl->done, step);
+            }
+        }
+        if (rp.yield_every > 0 && (step - rp.first_step + 1) % static_cast<uint32_t>(rp.yield_every) == 0) {
+            yielded = true;   // leave the GPU; the host relaunches for the next step
+            break;
         }
     }
     if (threadIdx.x == 0 && sm.abort) drain_after_abort<D, G>(sm, status);
     if (blockIdx.x == 0 && threadIdx.x == 0) {
         fence_sc_sys();
-        st_release_sys(&rp.ctl->exited, failed ? 2u : 1u);
+        st_release_sys(&rp.ctl->exited, failed ? 2u : yielded ? 3u : 1u);
     }
 }
 

@@ -187,12 +187,20 @@ struct ResidentCtl {
     uint32_t step;       // host: the last step it has published (1, 2, ...)
     uint32_t stop;       // host: 1 = leave the loop instead of waiting for another step
     uint32_t done;       // kernel: the last step whose outputs are written
-    uint32_t exited;     // kernel: 1 once it has left the loop; 2 if it left on an error
+    uint32_t exited;     // kernel: 1 once it has left the loop; 2 if it left on an error; 3 if it
+                         // yielded the GPU after yield_every steps (the host relaunches it)
     uint32_t requests;   // host: slot requests to apply at the start of the published step
     uint32_t pad[3];
 };
 // grid_sync words (device memory, zero before the launch)
-enum ResidentSync { kSyncCount = 0, kSyncGen = 1, kSyncCmd = 2, kSyncAbort = 3, kSyncReq = 4, kSyncWords = 5 };
+enum ResidentSync {
+    kSyncCount = 0, kSyncGen = 1,   // grid barrier: arrivals, generation
+    kSyncCmd = 2,                   // the step's command (go / stop / fail), set by CTA 0
+    kSyncAbort = 3,                 // a bounded wait ran out somewhere: every CTA leaves
+    kSyncReq = 4,                   // slot requests of the step
+    kSyncDone = 5,                  // CTAs done with the step's decode (the last one publishes)
+    kSyncWords = 6
+};
 struct ResidentParams {
     AttnParams attn;            // persistent route over the device plan below
     DevPlanParams plan;         // allocation + plan of each step (lengths before its append)
@@ -207,6 +215,9 @@ struct ResidentParams {
     uint64_t* times;            // [times_cap][4] globaltimer of a step: seen, planned, appended, published
     int32_t times_cap;
     uint64_t idle_limit_ns;     // longest wait for the host's next step
+    uint32_t* row_ready;        // [B] the last step whose append of the row has landed
+    uint32_t first_step;        // the first step this launch runs
+    int32_t yield_every;        // leave the GPU after this many steps of the launch (0: never)
 };
 cudaError_t launch_resident(const ResidentParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap, int grid,
                             cudaStream_t stream);

@@ -102,11 +102,13 @@ SIGNATURES = {
     "pkv_session_device_plan": (ctypes.c_int, [_P, _P]),
     "pkv_session_device_queue": (ctypes.c_int, [_P, ctypes.POINTER(WorkItem), _I32P, _I32, _I32P]),
     "pkv_selftest_wait": (ctypes.c_int, [_I64, _U32P, _I32P]),
-    "pkv_resident_start": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, _P, _I64, _I32, ctypes.POINTER(ctypes.c_void_p)]),
+    "pkv_resident_start": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, _P, _I64, _I32, _I32,
+                                          ctypes.POINTER(ctypes.c_void_p)]),
     "pkv_resident_step": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _I64]),
     "pkv_resident_stop": (ctypes.c_int, [_P]),
     "pkv_resident_times": (ctypes.c_int, [_P, ctypes.POINTER(ctypes.c_uint64), _I32, _I32P]),
     "pkv_resident_destroy": (None, [_P]),
+    "pkv_resident_launches": (ctypes.c_int, [_P, _I32P]),
     "pkv_session_evict": (ctypes.c_int, [_P, _I32P, _I32, _P]),
     "pkv_session_admit": (ctypes.c_int, [_P, _I32P, _I32P, _I32, _P, _P, _P, _P, _P]),
     "pkv_session_free_pages": (ctypes.c_int, [_P, _I32P, _I32, _I32P, _I32P]),
@@ -545,7 +547,7 @@ class Resident:
     for the kernel's life."""
 
     def __init__(self, session: "Session", k_pages, v_pages, q, k_new, v_new, out, lse,
-                 idle_limit_ns: int = 2_000_000_000, times_cap: int = 4096):
+                 idle_limit_ns: int = 2_000_000_000, times_cap: int = 4096, yield_every: int = 0):
         import torch
         bf = _bf16_types()
         self._keep = (session, k_pages, v_pages, q, k_new, v_new, out, lse)
@@ -554,7 +556,7 @@ class Resident:
                                          _dev_ptr(q, "q", bf), _dev_ptr(k_new, "k_new", bf),
                                          _dev_ptr(v_new, "v_new", bf), _dev_ptr(out, "out", (torch.float32,)),
                                          _dev_ptr(lse, "lse", (torch.float32,)), int(idle_limit_ns), int(times_cap),
-                                         ctypes.byref(h)), "pkv_resident_start")
+                                         int(yield_every), ctypes.byref(h)), "pkv_resident_start")
         self._h = h
 
     def step(self, q_h=None, k_new_h=None, v_new_h=None, out_h=None, lse_h=None,
@@ -567,6 +569,12 @@ class Resident:
 
     def stop(self):
         _check(load().pkv_resident_stop(self._h), "pkv_resident_stop")
+
+    def launches(self) -> int:
+        """Launches of the resident kernel so far (1 + relaunches after yields)."""
+        n = ctypes.c_int32(0)
+        _check(load().pkv_resident_launches(self._h, ctypes.byref(n)), "pkv_resident_launches")
+        return n.value
 
     def evict(self, rows):
         """pkv_resident_evict: applied at the start of the next step."""

@@ -141,3 +141,59 @@ def test_resident_idle_limit_runs_out_and_reports():
     ref = oracle.decode(p.q, k_h, v_h, table_h, lens_h, nthreads=16)
     assert_close(sess.out.cpu().numpy(), sess.lse.cpu().numpy(), *ref, what="launched step after the timeout")
     assert sess.plan.status() == 0
+
+
+def test_resident_yields_every_few_steps_and_lets_other_work_run():
+    """yield_every = 7 over 40 steps: the kernel leaves the GPU after each 7th step
+    of a launch and the next step launches it again (6 launches); its outputs are
+    the launched steps' bit for bit, and while it is away another decode runs on
+    the GPU and matches the oracle ("GPUOS", arXiv 2604.17861, set_yield_every)."""
+    steps, every = 40, 7
+    p = wl.continuous(steps=steps)
+    rng = np.random.default_rng(12)
+    toks = [wl.new_tokens(rng, p.B, p.Hkv, p.D) for _ in range(steps)]
+    eager = ContinuousSessions(p, force_mode="persistent", num_splits=1)
+    eager.session.device_plan()
+    for kn, vn in toks:
+        eager.step(torch.from_numpy(kn.view(np.int16)).cuda(), torch.from_numpy(vn.view(np.int16)).cuda())
+    torch.cuda.synchronize()
+    e_out, e_lse = eager.out.cpu().numpy(), eager.lse.cpu().numpy()
+    del eager
+    torch.cuda.empty_cache()
+
+    other = wl.tiny()
+    other_ref = oracle.decode(other.q, other.k_pages, other.v_pages, other.block_table, other.seq_lens)
+    other_dev = dict(q=torch.from_numpy(other.q.view(np.int16)).cuda(),
+                     k=torch.from_numpy(other.k_pages.view(np.int16)).cuda(),
+                     v=torch.from_numpy(other.v_pages.view(np.int16)).cuda(),
+                     table=torch.from_numpy(other.block_table).cuda(), lens=torch.from_numpy(other.seq_lens).cuda(),
+                     out=torch.empty((other.B, other.Hq, other.D), dtype=torch.float32, device="cuda"),
+                     lse=torch.empty((other.B, other.Hq), dtype=torch.float32, device="cuda"))
+    other_plan = pkv.Plan(other.seq_lens, other.block_table, other.page_size, B=other.B, Hq=other.Hq, Hkv=other.Hkv,
+                          D=other.D, max_pages=other.max_pages, num_pages=other.num_pages, force_mode="split_queue",
+                          num_splits=4)
+
+    sess = ContinuousSessions(p, force_mode="persistent", num_splits=1)
+    sess.session.device_plan()
+    kbuf = torch.empty((p.B, p.Hkv, p.D), dtype=torch.int16, device="cuda")
+    vbuf = torch.empty_like(kbuf)
+    torch.cuda.synchronize()
+    res = pkv.Resident(sess.session, sess.k, sess.v, sess.q, kbuf, vbuf, sess.out, sess.lse,
+                       idle_limit_ns=5_000_000_000, times_cap=steps, yield_every=every)
+    out_h = np.empty((p.B, p.Hq, p.D), np.float32)
+    lse_h = np.empty((p.B, p.Hq), np.float32)
+    try:
+        for step, (kn, vn) in enumerate(toks):
+            res.step(k_new_h=kn.view(np.int16), v_new_h=vn.view(np.int16), out_h=out_h, lse_h=lse_h)
+            if step + 1 == 2 * every:   # the kernel has just yielded: the GPU runs other work
+                pkv.decode(other_dev["q"], other_dev["k"], other_dev["v"], other_dev["table"], other_dev["lens"],
+                           other_plan, other_dev["out"], other_dev["lse"])
+                torch.cuda.synchronize()
+                assert_close(other_dev["out"].cpu().numpy(), other_dev["lse"].cpu().numpy(), *other_ref,
+                             what="decode between two resident launches")
+        assert res.launches() == -(-steps // every)
+    finally:
+        res.stop()
+    res.close()
+    assert sess.plan.status() == 0
+    assert np.array_equal(out_h, e_out) and np.array_equal(lse_h, e_lse)
