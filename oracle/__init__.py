@@ -9,8 +9,7 @@ Contents
 ``decode``      full attention per (row, query head), C in fp64 (pkv_oracle.c)
 ``partial``     the partial softmax state of one split, C in fp64
 ``merge``       exact log-sum-exp merge of partial states, C in fp64
-``enumerate_queue`` / ``enumerate_padded_grid`` / ``enumerate_direct`` / ``enumerate_balanced``
-                work-tile lists (queue.py)
+``enumerate_queue`` / ``enumerate_padded_grid`` / ``enumerate_direct``   work-tile lists (queue.py)
 ``append``      the KV-cache append of one token per (row, KV head) (append.py)
 
 Everything follows "PersistentKV: Page-Aware Decode Scheduling for Long-Context
@@ -31,8 +30,7 @@ import sys
 
 import numpy as np
 
-from .queue import (enumerate_queue, enumerate_padded_grid, enumerate_direct, enumerate_balanced,  # noqa: F401
-                    chunk_pages_for_splits)
+from .queue import enumerate_queue, enumerate_padded_grid, enumerate_direct, chunk_pages_for_splits  # noqa: F401
 from .append import append  # noqa: F401
 
 _HERE = os.path.dirname(os.path.abspath(__file__))

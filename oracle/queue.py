@@ -21,12 +21,7 @@ Readings taken where the page is silent:
   * the single-pass route (the summary's unsplit kernel for large batches,
     Methodology section 2) has one tile per (row, KV head) over the whole row,
     pages [0, P_b), split index 0, listed for every row in (b, kvh) order (an
-    empty row's tile is empty and stands for its neutral state);
-  * the balanced route (not on the pages: its tiles cross (row, KV head)
-    boundaries so that every CTA of the launch streams the same number of pages,
-    within one) cuts the pages of all units, in (b, kvh, page) order, into equal
-    shares, and each share into pieces at unit boundaries; a unit's pieces merge
-    exactly as its splits do.
+    empty row's tile is empty and stands for its neutral state).
 Each tile is the int32 record (b, kvh, s, page_begin, page_end), end exclusive.
 """
 from __future__ import annotations
@@ -80,36 +75,3 @@ def enumerate_direct(seq_lens, page_size: int, num_kv_heads: int) -> np.ndarray:
         for kvh in range(num_kv_heads):
             tiles.append((b, kvh, 0, 0, pages_of(n, page_size)))
     return np.array(tiles, dtype=np.int32).reshape(-1, 5)
-
-
-def enumerate_balanced(seq_lens, page_size: int, num_kv_heads: int, num_ctas: int):
-    """Balanced pieces: the pages of every (b, kvh) unit, taken in (b, kvh, page)
-    order as one sequence of Hkv * sum_b P_b pages, are cut into n = min(num_ctas,
-    total) shares, share i being [floor(i * total / n), floor((i + 1) * total / n));
-    each share is cut again where it crosses from one unit into the next.  Returns
-    (pieces int32 [T][5] as (b, kvh, piece, page_begin, page_end) in share order,
-    where `piece` counts the unit's pieces from 0; starts int32 [n + 1], share i
-    owning pieces [starts[i], starts[i + 1])).  No pages: no pieces, starts [0]."""
-    units = []
-    for b, n in enumerate(seq_lens):
-        for kvh in range(num_kv_heads):
-            units.append((b, kvh, pages_of(n, page_size)))
-    total = sum(u[2] for u in units)
-    n = min(int(num_ctas), total)
-    pieces, starts = [], [0]
-    count = {}
-    unit_first = []   # global page index of each unit's first page
-    g = 0
-    for u in units:
-        unit_first.append(g)
-        g += u[2]
-    for i in range(n):
-        lo, hi = (i * total) // n, ((i + 1) * total) // n
-        for ui, (b, kvh, p) in enumerate(units):
-            a, z = max(lo, unit_first[ui]), min(hi, unit_first[ui] + p)
-            if a < z:
-                k = count.get(ui, 0)
-                pieces.append((b, kvh, k, a - unit_first[ui], z - unit_first[ui]))
-                count[ui] = k + 1
-        starts.append(len(pieces))
-    return np.array(pieces, dtype=np.int32).reshape(-1, 5), np.array(starts, dtype=np.int32)

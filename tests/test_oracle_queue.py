@@ -16,51 +16,14 @@ GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 
 
 def _golden_queues():
-    """{S: tiles} of the split queues, {"direct": tiles} of the single-pass route and
-    {"balanced": [share, b, kvh, piece, begin, end]} of the balanced route."""
+    """{S: tiles} of the split queues and {"direct": tiles} of the single-pass route."""
     out = {}
     for line in open(os.path.join(GOLDEN, "tiny_queue.txt")):
         if not line.strip() or line.startswith("#"):
             continue
         key, *tile = line.split()
-        out.setdefault(key if key in ("direct", "balanced") else int(key), []).append(list(map(int, tile)))
+        out.setdefault(key if key == "direct" else int(key), []).append(list(map(int, tile)))
     return out
-
-
-def test_tiny_balanced_pieces_match_hand_derivation():
-    p = wl.tiny()
-    pieces, starts = oracle.enumerate_balanced(p.seq_lens, p.page_size, p.Hkv, 4)
-    want = _golden_queues()["balanced"]
-    assert pieces.tolist() == [w[1:] for w in want]
-    share_of = [i for i in range(len(starts) - 1) for _ in range(starts[i], starts[i + 1])]
-    assert share_of == [w[0] for w in want]
-
-
-@pytest.mark.parametrize("seed", range(8))
-def test_balanced_pieces_cover_units_and_balance_shares(seed):
-    rng = np.random.default_rng(200 + seed)
-    B, Hkv, ps = int(rng.integers(1, 7)), int(rng.integers(1, 5)), int(rng.choice([1, 16, 32]))
-    lens = rng.integers(0, 600, size=B)
-    n = int(rng.integers(1, 40))
-    pieces, starts = oracle.enumerate_balanced(lens, ps, Hkv, n)
-    units = [(b, h, -(-int(x) // ps)) for b, x in enumerate(lens) for h in range(Hkv)]
-    total = sum(u[2] for u in units)
-    shares = min(n, total)
-    assert len(starts) == shares + 1 and starts[0] == 0 and starts[-1] == len(pieces)
-    assert np.all(np.diff(starts) >= 1)
-    sizes = [int((pieces[starts[i]:starts[i + 1], 4] - pieces[starts[i]:starts[i + 1], 3]).sum())
-             for i in range(shares)]
-    assert sum(sizes) == total and (not sizes or max(sizes) - min(sizes) <= 1)
-    # per unit: pieces 0, 1, ... tile [0, P_u) in order, brute force over the pages
-    for b, h, P in units:
-        mine = pieces[(pieces[:, 0] == b) & (pieces[:, 1] == h)]
-        assert mine[:, 2].tolist() == list(range(len(mine)))
-        covered = [pg for t in mine for pg in range(t[3], t[4])]
-        assert covered == list(range(P))
-    # share order is (b, kvh, page) order, and a share adds a piece only where it crosses a unit
-    keys = [(int(t[0]), int(t[1]), int(t[3])) for t in pieces]
-    assert keys == sorted(keys)
-    assert len(pieces) <= shares + sum(1 for u in units if u[2] > 0) - 1 if shares else len(pieces) == 0
 
 
 @pytest.mark.parametrize("S", [1, 2, 4])
