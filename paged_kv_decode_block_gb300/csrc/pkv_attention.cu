@@ -851,24 +851,30 @@ __device__ void merge_unit_staged(Smem<D, G>& sm, const AttnParams& p, int b, in
     // the LSEs of the first heads are requested before the partials, so their
     // latency overlaps the issue of the copies
     const float ls_first =
-        ns <= 32 && warp < G && lane < ns ? __ldcg(p.ws_lse + (base + lane) * G + warp) : -INFINITY;
+        ns <= 64 && warp < G && lane < ns ? __ldcg(p.ws_lse + (base + lane) * G + warp) : -INFINITY;
+    const float ls_first_hi =
+        ns <= 64 && warp < G && lane + 32 < ns ? __ldcg(p.ws_lse + (base + lane + 32) * G + warp) : -INFINITY;
     issue(0);
-    if (ns <= 32) {
-        // One warp per head, one split per lane: the LSEs go straight from L2 to
-        // registers, the max and sum are shuffles, and the normalised weights land
-        // in shared memory while the partials are still arriving.
+    if (ns <= 64) {
+        // One warp per head, splits lane and lane + 32 per lane: the LSEs go
+        // straight from L2 to registers, the max and sum are shuffles, and the
+        // normalised weights land in shared memory while the partials arrive.
         for (int g = warp; g < G; g += kThreads / 32) {
             const float ls = g == warp ? ls_first : lane < ns ? __ldcg(p.ws_lse + (base + lane) * G + g) : -INFINITY;
-            const bool nan = __any_sync(kFull, isnan(ls));
-            float M = ls;
+            const float ls2 = g == warp ? ls_first_hi
+                                        : lane + 32 < ns ? __ldcg(p.ws_lse + (base + lane + 32) * G + g) : -INFINITY;
+            const bool nan = __any_sync(kFull, isnan(ls) || isnan(ls2));
+            float M = fmaxf(ls, ls2);
 #pragma unroll
             for (int x = 16; x > 0; x >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, x));
             const float e = M != -INFINITY && lane < ns ? exp2f(ls - M) : 0.f;
-            float wsum = e;
+            const float e2 = M != -INFINITY && lane + 32 < ns ? exp2f(ls2 - M) : 0.f;
+            float wsum = e + e2;
 #pragma unroll
             for (int x = 16; x > 0; x >>= 1) wsum += __shfl_xor_sync(kFull, wsum, x);
             const float inv = M != -INFINITY ? 1.f / wsum : 0.f;
             if (lane < ns) w[lane * G + g] = e * inv;
+            if (lane + 32 < ns) w[(lane + 32) * G + g] = e2 * inv;
             if (lane == 0) {
                 sm.merge_nan_h[g] = nan ? 1 : 0;
                 const float lse2 = M != -INFINITY ? M + log2f(wsum) : -INFINITY;
