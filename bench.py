@@ -513,16 +513,34 @@ def decode_line(name, args, ctx, headline=True):
     q_host = torch.from_numpy(p.q.view(np.int16)).pin_memory()
     out_host = torch.empty(out.shape, dtype=torch.float32).pin_memory()
     lse_host = torch.empty(lse.shape, dtype=torch.float32).pin_memory()
-    e2e_s = []
+    e2e_s, replan_s, call_s = [], [], []
     for i in range(args.warmup + K):
         flush.zero_()
         torch.cuda.synchronize()
         t0 = time.perf_counter()
         plan.update(p.seq_lens)
+        t1 = time.perf_counter()
         pkv.decode_host(q_host, k, v, table, lens, plan, out_host, lse_host)
         if i >= args.warmup:
-            e2e_s.append(time.perf_counter() - t0)
+            t2 = time.perf_counter()
+            e2e_s.append(t2 - t0)
+            replan_s.append(t1 - t0)
+            call_s.append(t2 - t1)
     e2e_med = statistics.median(e2e_s)
+    # the same call's kernel alone, device time between events after the same flush
+    dev_ms = []
+    for i in range(max(min(K, 20), 5)):
+        plan.update(p.seq_lens)
+        flush.zero_()
+        starts[i % K].record(stream)
+        pkv.decode_host(q_host, k, v, table, lens, plan, out_host, lse_host)
+        ends[i % K].record(stream)
+        ends[i % K].synchronize()
+        dev_ms.append(starts[i % K].elapsed_time(ends[i % K]))
+    breakdown = {"replan_us": round(statistics.median(replan_s) * 1e6, 2),
+                 "decode_host_call_us": round(statistics.median(call_s) * 1e6, 2),
+                 "device_us": round(statistics.median(dev_ms) * 1e3, 2)}
+    breakdown["host_and_sync_us"] = round(breakdown["decode_host_call_us"] - breakdown["device_us"], 2)
     if not (np.array_equal(out_host.numpy(), out.cpu().numpy()) and np.array_equal(lse_host.numpy(), lse.cpu().numpy())):
         raise SystemExit("the host-buffer path disagrees with the device path")
     upload = 4 * (5 * info["num_work_items"] + 2 * p.B) if info["mode"] != pkv.MODE_DIRECT else 0
@@ -564,7 +582,13 @@ def decode_line(name, args, ctx, headline=True):
                 "us_per_step": round(e2e_med * 1e6, 2), "h2d_bytes_per_step": q_bytes + upload,
                 "d2h_bytes_per_step": o_bytes,
                 "path": "host re-plan + pkv_decode_host: the kernel reads the plan and q from pinned host "
-                        "memory and writes out/lse to pinned host memory (NVLink-C2C), then a synchronise"},
+                        "memory and writes out/lse to pinned host memory (NVLink-C2C), then a synchronise",
+                "breakdown": {**breakdown,
+                              "note": "medians per step: the host re-plan; the pkv_decode_host call (launch, "
+                                      "kernel, synchronise); the kernel's device time between events on the "
+                                      "stream after the same L2 flush (launch latency included); the call "
+                                      "minus that device time (host launch work and the wake-up of the "
+                                      "synchronise)"}},
         "gpu_launches": n_launch * K * R,
         "cpu_baseline": cpu,
         "clocks": clocks,
