@@ -820,8 +820,106 @@ __device__ void merge_unit(const AttnParams& p, int b, int kvh, int ns, float* w
     __syncthreads();
 }
 
-// The fused merge of the last-arriving CTA.  The ns partial outputs of
-// (b, kvh) are contiguous in the workspace: every thread copies its share of
+// Merge staging geometry: the weights, then the partials, in the idle stage
+// buffers; ns <= kMaxSplits take the one-pass path.
+template <int D, int G>
+struct MergeCfg {
+    static constexpr int kSplitBytes = G * D * 4;
+    static constexpr int kWeightBytes = 2048;   // [64][G] floats at most
+    static constexpr int kScratch = Cfg<D, G>::kStages * Cfg<D, G>::kMatBytes * 2;
+    static constexpr int kCap = (kScratch - kWeightBytes) / kSplitBytes;
+    static constexpr int kMaxSplits = kCap < 64 ? kCap : 64;
+    static_assert(64 * G * 4 <= kWeightBytes, "merge staging");
+};
+
+// The fused merge of the last-arriving CTA for up to MergeCfg::kMaxSplits
+// splits.  The ns partial outputs of (b, kvh) are contiguous in the
+// workspace; every thread copies its 16-byte pieces of them into the CTA's
+// idle stage buffers with cp.async (the fastest way into one SM: per-thread
+// loads are held back by the outstanding-request limit, and the bulk-copy
+// engine measured slower).  The LSEs come in meanwhile, one warp per head
+// holding splits lane and lane + 32; the max, sum and weights are shuffles.
+// The weighted sum runs once everything has landed: T = kThreads / (G*D/4)
+// lane groups share one float4 of the output (group `part` taking splits
+// part, part + T, ...; a quarter warp reads 128 contiguous bytes), so all
+// threads add, and the T part sums are added with a fixed butterfly: the
+// result is the same on every launch.  Same arithmetic as merge_unit up to
+// the order of the additions; all CTA threads call it.
+template <int D, int G>
+__device__ void merge_unit_onepass(Smem<D, G>& sm, const AttnParams& p, int b, int kvh, int ns, int base_slot) {
+    using MC = MergeCfg<D, G>;
+    constexpr int kOut = G * D / 4;       // float4 outputs of (b, kvh)
+    constexpr int T = kThreads / kOut;    // lane groups per output
+    constexpr int W = 32 / T;             // outputs per warp
+    static_assert(kThreads % kOut == 0 && T >= 1 && T <= 32 && (T & (T - 1)) == 0, "merge lane split");
+    const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+    const int out = warp * W + lane % W, part = lane / W;
+    const int g_out = out / (D / 4), d = (out % (D / 4)) * 4;
+    const size_t base = static_cast<size_t>(base_slot);
+    float* w = reinterpret_cast<float*>(&sm.k[0][0]);   // [ns][G] weights
+    float* obuf = reinterpret_cast<float*>(&sm.k[0][0] + MC::kWeightBytes);   // [ns][G][D] partials
+
+    const float ls_first = warp < G && lane < ns ? __ldcg(p.ws_lse + (base + lane) * G + warp) : -INFINITY;
+    const float ls_first_hi = warp < G && lane + 32 < ns ? __ldcg(p.ws_lse + (base + lane + 32) * G + warp) : -INFINITY;
+    {
+        const uint8_t* src = reinterpret_cast<const uint8_t*>(p.ws_o + base * G * D);
+        const uint32_t dst = smem_addr(obuf);
+        const int vecs = ns * (MC::kSplitBytes / 16);
+        for (int i = tid; i < vecs; i += kThreads) cp_async16_plain(dst + i * 16, src + static_cast<size_t>(i) * 16);
+    }
+    for (int g = warp; g < G; g += kThreads / 32) {
+        const float ls = g == warp ? ls_first : lane < ns ? __ldcg(p.ws_lse + (base + lane) * G + g) : -INFINITY;
+        const float ls2 =
+            g == warp ? ls_first_hi : lane + 32 < ns ? __ldcg(p.ws_lse + (base + lane + 32) * G + g) : -INFINITY;
+        const bool nan = __any_sync(kFull, isnan(ls) || isnan(ls2));
+        float M = fmaxf(ls, ls2);
+#pragma unroll
+        for (int x = 16; x > 0; x >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, x));
+        const float e = M != -INFINITY && lane < ns ? exp2f(ls - M) : 0.f;
+        const float e2 = M != -INFINITY && lane + 32 < ns ? exp2f(ls2 - M) : 0.f;
+        float wsum = e + e2;
+#pragma unroll
+        for (int x = 16; x > 0; x >>= 1) wsum += __shfl_xor_sync(kFull, wsum, x);
+        const float inv = M != -INFINITY ? 1.f / wsum : 0.f;
+        if (lane < ns) w[lane * G + g] = e * inv;
+        if (lane + 32 < ns) w[(lane + 32) * G + g] = e2 * inv;
+        if (lane == 0) {
+            sm.merge_nan_h[g] = nan ? 1 : 0;
+            const float lse2 = M != -INFINITY ? M + log2f(wsum) : -INFINITY;
+            p.lse[static_cast<size_t>(b) * p.Hq + kvh * G + g] = nan ? NAN : lse2 * kLn2;
+        }
+    }
+    cp_async_commit_wait_all();
+    __syncthreads();   // every thread's copies and the weights visible
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    const float* ob = obuf + g_out * D + d;
+#pragma unroll 2
+    for (int s = part; s < ns; s += T) {
+        const float ws = w[s * G + g_out];
+        const float4 o = *reinterpret_cast<const float4*>(ob + s * G * D);
+        acc.x = fmaf(ws, o.x, acc.x);
+        acc.y = fmaf(ws, o.y, acc.y);
+        acc.z = fmaf(ws, o.z, acc.z);
+        acc.w = fmaf(ws, o.w, acc.w);
+    }
+#pragma unroll
+    for (int x = W; x < 32; x <<= 1) {
+        acc.x += __shfl_xor_sync(kFull, acc.x, x);
+        acc.y += __shfl_xor_sync(kFull, acc.y, x);
+        acc.z += __shfl_xor_sync(kFull, acc.z, x);
+        acc.w += __shfl_xor_sync(kFull, acc.w, x);
+    }
+    if (part == 0)
+        *reinterpret_cast<float4*>(p.out + (static_cast<size_t>(b) * p.Hq + kvh * G + g_out) * D + d) =
+            sm.merge_nan_h[g_out] ? make_float4(NAN, NAN, NAN, NAN) : acc;
+    // A later TMA into the stages is ordered after the copies above; every
+    // caller that reuses the stages passes a CTA barrier before it does.
+    fence_proxy_async_shared();
+}
+
+// The fused merge of the last-arriving CTA for more splits than one pass
+// holds (MergeCfg::kMaxSplits).  The ns partial outputs of (b, kvh) are
+// contiguous in the workspace: every thread copies its share of
 // them into the CTA's idle stage buffers with 16-byte cp.async (all in flight
 // at once, a chunk of splits at a time), while the LSEs come in with plain L2
 // loads; the weighted sum then runs out of shared memory, one float4 of the
@@ -848,40 +946,7 @@ __device__ void merge_unit_staged(Smem<D, G>& sm, const AttnParams& p, int b, in
         for (int i = tid; i < vecs; i += kThreads) cp_async16_plain(dst + i * 16, src + static_cast<size_t>(i) * 16);
     };
     const int warp = tid / 32, lane = tid % 32;
-    // the LSEs of the first heads are requested before the partials, so their
-    // latency overlaps the issue of the copies
-    const float ls_first =
-        ns <= 64 && warp < G && lane < ns ? __ldcg(p.ws_lse + (base + lane) * G + warp) : -INFINITY;
-    const float ls_first_hi =
-        ns <= 64 && warp < G && lane + 32 < ns ? __ldcg(p.ws_lse + (base + lane + 32) * G + warp) : -INFINITY;
     issue(0);
-    if (ns <= 64) {
-        // One warp per head, splits lane and lane + 32 per lane: the LSEs go
-        // straight from L2 to registers, the max and sum are shuffles, and the
-        // normalised weights land in shared memory while the partials arrive.
-        for (int g = warp; g < G; g += kThreads / 32) {
-            const float ls = g == warp ? ls_first : lane < ns ? __ldcg(p.ws_lse + (base + lane) * G + g) : -INFINITY;
-            const float ls2 = g == warp ? ls_first_hi
-                                        : lane + 32 < ns ? __ldcg(p.ws_lse + (base + lane + 32) * G + g) : -INFINITY;
-            const bool nan = __any_sync(kFull, isnan(ls) || isnan(ls2));
-            float M = fmaxf(ls, ls2);
-#pragma unroll
-            for (int x = 16; x > 0; x >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, x));
-            const float e = M != -INFINITY && lane < ns ? exp2f(ls - M) : 0.f;
-            const float e2 = M != -INFINITY && lane + 32 < ns ? exp2f(ls2 - M) : 0.f;
-            float wsum = e + e2;
-#pragma unroll
-            for (int x = 16; x > 0; x >>= 1) wsum += __shfl_xor_sync(kFull, wsum, x);
-            const float inv = M != -INFINITY ? 1.f / wsum : 0.f;
-            if (lane < ns) w[lane * G + g] = e * inv;
-            if (lane + 32 < ns) w[(lane + 32) * G + g] = e2 * inv;
-            if (lane == 0) {
-                sm.merge_nan_h[g] = nan ? 1 : 0;
-                const float lse2 = M != -INFINITY ? M + log2f(wsum) : -INFINITY;
-                p.lse[static_cast<size_t>(b) * p.Hq + kvh * G + g] = nan ? NAN : lse2 * kLn2;
-            }
-        }
-    } else {
     for (int i = tid; i < ns * G; i += kThreads) w[i] = __ldcg(p.ws_lse + base * G + i);
     __syncthreads();
     // per head: max and sum over the splits, one warp per head
@@ -912,7 +977,6 @@ __device__ void merge_unit_staged(Smem<D, G>& sm, const AttnParams& p, int b, in
     for (int i = tid; i < ns * G; i += kThreads) {
         const int g = i % G;
         w[i] = sm.merge_m[g] != -INFINITY ? exp2f(w[i] - sm.merge_m[g]) * sm.merge_inv[g] : 0.f;
-    }
     }
     float4 acc[kPer];
 #pragma unroll
@@ -1216,7 +1280,10 @@ __device__ void merge_if_last(Smem<D, G>& sm, const AttnParams& p, int b, int kv
         // the stage buffers are idle here and serve as the merge's scratch
         static_assert(2 * Cfg<D, G>::kStages * Cfg<D, G>::kMatBytes >= kMergeCapFloats * 4 + 2 * G * D * 4,
                       "merge scratch");
-        merge_unit_staged<D, G>(sm, p, b, kvh, ns, sm.tile_base);
+        if (ns <= MergeCfg<D, G>::kMaxSplits)
+            merge_unit_onepass<D, G>(sm, p, b, kvh, ns, sm.tile_base);
+        else
+            merge_unit_staged<D, G>(sm, p, b, kvh, ns, sm.tile_base);
         trace_stamp(sm, p, kTrMergeEnd);
     }
 }

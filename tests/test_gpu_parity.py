@@ -137,7 +137,7 @@ def test_fused_merge_kinds(route, splits, merge):
 
 
 @pytest.mark.parametrize("merge", MERGES)
-@pytest.mark.parametrize("Hq,D", [(8, 128), (2, 64)])
+@pytest.mark.parametrize("Hq,D", [(8, 128), (16, 128), (2, 64)])
 def test_fused_merge_more_splits_than_lanes(merge, Hq, D):
     """64 splits of one (row, KV head): more than a warp's lanes; with G = 1 and
     D = 64 also more splits than float4 outputs, so some splits merge nothing."""
@@ -148,6 +148,39 @@ def test_fused_merge_more_splits_than_lanes(merge, Hq, D):
     info = plan.info()
     assert info["merge_name"] == merge and info["max_splits"] == 64
     assert_close(out, lse, *ref, what=f"{merge} merge, 64 splits")
+    assert plan.status() == 0
+
+
+@pytest.mark.parametrize("Hq,D,splits", [(16, 128, 16), (2, 64, 16), (4, 64, 40), (16, 64, 24), (2, 128, 16),
+                                          (8, 128, 40)])
+def test_last_merge_group_sizes(Hq, D, splits):
+    """The last arriver's chunked merge for every lanes-per-output split (G*D/4
+    outputs over 256 threads: 1, 2, 8 or 16 lanes each) and up to 7 chunks;
+    repeated launches give the same bits."""
+    p = wl.make_problem("groups", [4096, 1000, 17, 0], Hq=Hq, Hkv=2, D=D, page_size=16, num_pages=360, seed=30)
+    ref = oracle_result(p)
+    out, lse, plan, dev = run(p, force_mode="split_queue", num_splits=splits, merge="last")
+    assert_close(out, lse, *ref, what=f"Hq={Hq} D={D} S={splits}")
+    out2, lse2, _, _ = run(p, dev=dev, plan=plan)
+    assert np.array_equal(out2, out) and np.array_equal(lse2, lse)
+    assert plan.status() == 0
+
+
+@pytest.mark.parametrize("Hq,D", [(8, 128), (16, 128), (2, 64)])
+def test_fused_merge_beyond_64_splits(Hq, D):
+    """86 splits of the 4096-token row (3 pages each): past the register merge's
+    64, so the last arriver stages the partials in shared memory (the ALL merge
+    refuses more than 64 splits)."""
+    merge = "last"
+    p = wl.make_problem("splits86", [4096, 1000, 17, 0], Hq=Hq, Hkv=2, D=D, page_size=16,
+                        num_pages=360, seed=29)
+    ref = oracle_result(p)
+    out, lse, plan, dev = run(p, force_mode="split_queue", num_splits=96, merge=merge)
+    info = plan.info()
+    assert info["merge_name"] == merge and info["max_splits"] == 86, info["max_splits"]
+    assert_close(out, lse, *ref, what=f"{merge} merge, 86 splits")
+    out2, lse2, _, _ = run(p, dev=dev, plan=plan)
+    assert np.array_equal(out2, out) and np.array_equal(lse2, lse)
     assert plan.status() == 0
 
 
