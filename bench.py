@@ -907,6 +907,8 @@ def run_resident(args):
         raise SystemExit("device status word set")
     dev_us = (stamps[:, 3] - stamps[:, 0]) / 1e3
     dec_us = (stamps[:, 3] - stamps[:, 2]) / 1e3
+    plan_us = (stamps[:, 1] - stamps[:, 0]) / 1e3     # slot requests, allocation and plan, grid barrier
+    append_us = (stamps[:, 2] - stamps[:, 1]) / 1e3   # CTA 0's appends until its drain starts
     kv = [(lens0 + (i + 1) * p.B) * p.Hkv * p.D * 4 for i in range(args.warmup, total)]
     value = float(np.sum(kv)) / (float(np.sum(dev_us)) * 1e-6) / 1e9
     peak, peak_src = hbm_peak()
@@ -919,6 +921,8 @@ def run_resident(args):
         "warmup": args.warmup, "ms_per_step": round(float(np.median(dev_us)) / 1e3, 5),
         "us_per_step": {"device_p50": round(float(np.percentile(dev_us, 50)), 2),
                         "device_p99": round(float(np.percentile(dev_us, 99)), 2),
+                        "plan_phase_p50": round(float(np.percentile(plan_us, 50)), 2),
+                        "append_phase_p50": round(float(np.percentile(append_us, 50)), 2),
                         "decode_phase_p50": round(float(np.percentile(dec_us, 50)), 2),
                         "wall_p50": round(float(np.percentile(wall_us, 50)), 2),
                         "wall_p99": round(float(np.percentile(wall_us, 99)), 2)},

@@ -1694,9 +1694,8 @@ __global__ void __launch_bounds__(kThreads, MMA ? 2 : 1) resident_kernel(const R
                     }
                 }
                 __syncthreads();
-                int* scratch = reinterpret_cast<int*>(&sm.k[0][0]);   // the idle ring
-                devplan::plan_step<kThreads>(rp.plan, scratch, scratch + kDevPlanMaxRows,
-                                             scratch + 2 * kDevPlanMaxRows);
+                int* scratch = reinterpret_cast<int*>(&sm.k[0][0]);   // the idle ring (K and V stages)
+                devplan::plan_step<kThreads>(rp.plan, scratch);
                 fence_proxy_async_shared();   // generic writes to the ring before later TMA writes
             }
         }
@@ -1813,7 +1812,7 @@ template <int D, int G, bool MMA>
 cudaError_t launch_resident_t(const ResidentParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap, int grid,
                               cudaStream_t stream) {
     constexpr size_t smem = smem_bytes<D, G>();
-    static_assert(Cfg<D, G>::kStages * Cfg<D, G>::kMatBytes >= (2 * kDevPlanMaxRows + 32) * 4, "planner scratch");
+    static_assert(2 * Cfg<D, G>::kStages * Cfg<D, G>::kMatBytes >= devplan::kPlanScratchInts * 4, "planner scratch");
     cudaError_t e = cudaFuncSetAttribute(resident_kernel<D, G, MMA>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;

@@ -11,7 +11,9 @@
 // Embeddings on GPUs" lesson (engineermaxxing, the CUDA-graph section) asks of
 // a capturable step, with the dynamic decision moved into the kernel.
 //
-// One CTA of 1024 threads, for the lengths *before* the step's append:
+// One CTA of 1024 threads (the resident kernel runs the same code on one of
+// its 256-thread CTAs), rows one per thread, for the lengths *before* the
+// step's append:
 //   1. page allocation: every row whose next token starts a page with no table
 //      entry yet takes the next page of the device free list, in row order
 //      (the host pool's FIFO rule, so tables come out identical);
@@ -36,10 +38,8 @@ namespace {
 constexpr int kPlanThreads = 1024;
 
 __global__ void __launch_bounds__(kPlanThreads) plan_step_kernel(const DevPlanParams p) {
-    __shared__ int s_pages[kDevPlanMaxRows];   // P_b after the append
-    __shared__ int s_partial[kDevPlanMaxRows]; // size of the row's last tile if partial, else 0
-    __shared__ int warp_sums[32];
-    devplan::plan_step<kPlanThreads>(p, s_pages, s_partial, warp_sums);
+    __shared__ int scratch[devplan::kPlanScratchInts];
+    devplan::plan_step<kPlanThreads>(p, scratch);
 }
 
 }  // namespace

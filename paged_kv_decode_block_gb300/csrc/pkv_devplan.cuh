@@ -39,11 +39,22 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* total, int* warp
     return before;
 }
 
-// One planning step by the whole CTA of kThreads threads.  Shared scratch:
-// s_pages and s_partial of kDevPlanMaxRows ints each, warp_sums of 32 ints.
+// Ints of shared scratch plan_step needs: four per-row arrays and 32 warp sums.
+constexpr int kPlanScratchInts = 4 * kDevPlanMaxRows + 32;
+
+// One planning step by the whole CTA of kThreads threads, on `scratch`
+// (kPlanScratchInts ints of shared memory).  Rows go one per thread, in passes
+// of kThreads rows, so a small batch still spreads over the CTA: each pass's
+// prefix sums continue the last one's, which keeps everything in row order.
+// The tiles are then written by all threads, each finding its tile's row by a
+// binary search over the row starts.
 template <int kThreads>
-__device__ void plan_step(const DevPlanParams& p, int* s_pages, int* s_partial, int* warp_sums) {
-    constexpr int kRowsPerThread = (kDevPlanMaxRows + kThreads - 1) / kThreads;
+__device__ void plan_step(const DevPlanParams& p, int* scratch) {
+    int* s_pages = scratch;                       // P_b after the append
+    int* s_partial = s_pages + kDevPlanMaxRows;   // size of the row's last tile if partial, else 0
+    int* s_start = s_partial + kDevPlanMaxRows;   // row_start
+    int* s_full = s_start + kDevPlanMaxRows;      // hand-out slot of the row's first full-chunk tile
+    int* warp_sums = s_full + kDevPlanMaxRows;    // 32
     const int tid = threadIdx.x;
     const int B = p.B, Hkv = p.Hkv, ps = p.page_size, C = p.chunk;
     if (B > kDevPlanMaxRows) {
@@ -53,71 +64,68 @@ __device__ void plan_step(const DevPlanParams& p, int* s_pages, int* s_partial, 
         }
         return;
     }
-    const int r0 = tid * kRowsPerThread;   // this thread's rows: [r0, r0 + kRowsPerThread)
+    const int passes = (B + kThreads - 1) / kThreads;
 
     // ---- 1. page allocation, in row order
-    int need[kRowsPerThread];
-    int my_need = 0;
-#pragma unroll
-    for (int i = 0; i < kRowsPerThread; ++i) {
-        const int b = r0 + i;
-        need[i] = 0;
+    const uint32_t head = p.free_state[0], avail = p.free_state[1];
+    int taken = 0;   // pages handed out by earlier passes
+    for (int pass = 0; pass < passes; ++pass) {
+        const int b = pass * kThreads + tid;
+        int need = 0;
         if (b < B && (!p.active || p.active[b])) {   // idle slots take no page
             const int n = p.lens[b];
             if (n >= 0 && n % ps == 0) {
                 if (n / ps >= p.max_pages)
                     atomicOr(p.status, static_cast<uint32_t>(PKV_DEV_ROW_FULL));
                 else if (p.table[static_cast<size_t>(b) * p.max_pages + n / ps] < 0)
-                    need[i] = 1;
+                    need = 1;
             }
         }
-        my_need += need[i];
-    }
-    int total_need;
-    int rank = block_exclusive_scan(my_need, &total_need, warp_sums);
-    const uint32_t head = p.free_state[0], avail = p.free_state[1];
-#pragma unroll
-    for (int i = 0; i < kRowsPerThread; ++i) {
-        if (!need[i]) continue;
-        const int b = r0 + i;
-        if (static_cast<uint32_t>(rank) < avail) {
-            const int n = p.lens[b];
-            p.table[static_cast<size_t>(b) * p.max_pages + n / ps] =
-                p.free_list[(head + static_cast<uint32_t>(rank)) % static_cast<uint32_t>(p.free_cap)];
-        } else {
-            atomicOr(p.status, static_cast<uint32_t>(PKV_DEV_ROW_FULL));   // pool exhausted
+        int total;
+        const int rank = taken + block_exclusive_scan(need, &total, warp_sums);
+        if (need) {
+            if (static_cast<uint32_t>(rank) < avail) {
+                const int n = p.lens[b];
+                p.table[static_cast<size_t>(b) * p.max_pages + n / ps] =
+                    p.free_list[(head + static_cast<uint32_t>(rank)) % static_cast<uint32_t>(p.free_cap)];
+            } else {
+                atomicOr(p.status, static_cast<uint32_t>(PKV_DEV_ROW_FULL));   // pool exhausted
+            }
         }
-        ++rank;
+        taken += total;
     }
-    __syncthreads();
-    if (tid == 0) {
-        const uint32_t used = min(static_cast<uint32_t>(total_need), avail);
+    if (tid == 0) {   // every thread read free_state before the first scan's barrier
+        const uint32_t used = min(static_cast<uint32_t>(taken), avail);
         p.free_state[0] = (head + used) % static_cast<uint32_t>(p.free_cap);
         p.free_state[1] = avail - used;
     }
 
-    // ---- 2. plan for the lengths after the append
-    int splits[kRowsPerThread], fulls[kRowsPerThread];
-    int my_tiles = 0, my_full = 0;
-#pragma unroll
-    for (int i = 0; i < kRowsPerThread; ++i) {
-        const int b = r0 + i;
-        splits[i] = fulls[i] = 0;
+    // ---- 2. plan for the lengths after the append: splits, row starts, full-tile slots
+    int total_tiles = 0, total_full = 0;
+    for (int pass = 0; pass < passes; ++pass) {
+        const int b = pass * kThreads + tid;
+        int S = 0, F = 0;
         if (b < B) {
             const int n = max(p.lens[b], 0) + (!p.active || p.active[b] ? 1 : 0);   // idle slots do not grow
             const int pages = (n + ps - 1) / ps;
-            splits[i] = (pages + C - 1) / C;
+            S = (pages + C - 1) / C;
             const int rem = pages % C;
-            fulls[i] = rem == 0 ? splits[i] : splits[i] - 1;
+            F = rem == 0 ? S : S - 1;
             s_pages[b] = pages;
             s_partial[b] = rem;
         }
-        my_tiles += splits[i] * Hkv;
-        my_full += fulls[i] * Hkv;
+        int t_total, f_total;
+        const int start = total_tiles + block_exclusive_scan(S * Hkv, &t_total, warp_sums);
+        const int full_start = total_full + block_exclusive_scan(F * Hkv, &f_total, warp_sums);
+        if (b < B) {
+            s_start[b] = start;
+            s_full[b] = full_start;
+            p.row_start[b] = start;
+            p.row_splits[b] = S;
+        }
+        total_tiles += t_total;
+        total_full += f_total;
     }
-    int total_tiles, total_full;
-    int start = block_exclusive_scan(my_tiles, &total_tiles, warp_sums);
-    int full_start = block_exclusive_scan(my_full, &total_full, warp_sums);
     if (total_tiles > p.queue_cap) {
         if (tid == 0) {
             atomicOr(p.status, static_cast<uint32_t>(PKV_DEV_PLAN_MISMATCH));
@@ -125,37 +133,38 @@ __device__ void plan_step(const DevPlanParams& p, int* s_pages, int* s_partial, 
         }
         return;
     }
-    // ---- queue, row table and the full-tile part of the hand-out order
-#pragma unroll
-    for (int i = 0; i < kRowsPerThread; ++i) {
-        const int b = r0 + i;
-        if (b >= B) continue;
-        const int S = splits[i], F = fulls[i], pages = s_pages[b];
-        p.row_start[b] = start;
-        p.row_splits[b] = S;
-        for (int kvh = 0; kvh < Hkv; ++kvh)
-            for (int s = 0; s < S; ++s) {
-                const int t = start + kvh * S + s;
-                p.queue[t] = pkv_work_item{b, kvh, s, s * C, min((s + 1) * C, pages)};
-                if (s < F) p.order[full_start + kvh * F + s] = t;
-            }
-        start += S * Hkv;
-        full_start += F * Hkv;
+    __syncthreads();   // the per-row arrays complete
+
+    // ---- 3. the queue in (b, kvh, s) order, and the full-chunk tiles' hand-out slots
+    for (int t = tid; t < total_tiles; t += kThreads) {
+        int lo = 0, hi = B;   // first row whose tiles start after t
+        while (lo < hi) {
+            const int mid = (lo + hi) >> 1;
+            if (s_start[mid] <= t) lo = mid + 1;
+            else hi = mid;
+        }
+        const int b = lo - 1;   // the last row starting at or before t: it holds t
+        const int pages = s_pages[b];
+        const int S = (pages + C - 1) / C;
+        const int F = s_partial[b] == 0 ? S : S - 1;
+        const int local = t - s_start[b];
+        const int kvh = local / S, sp = local % S;
+        p.queue[t] = pkv_work_item{b, kvh, sp, sp * C, min((sp + 1) * C, pages)};
+        if (sp < F) p.order[s_full[b] + kvh * F + sp] = t;
     }
-    __syncthreads();   // s_partial complete
-    // ---- the partial tiles: rows ranked by their last tile's size (desc), then row
-#pragma unroll
-    for (int i = 0; i < kRowsPerThread; ++i) {
-        const int b = r0 + i;
+
+    // ---- 4. the partial tiles: rows ranked by their last tile's size (desc), then row
+    for (int pass = 0; pass < passes; ++pass) {
+        const int b = pass * kThreads + tid;
         if (b >= B || s_partial[b] == 0) continue;
         const int mine = s_partial[b];
         int before = 0;
         for (int c = 0; c < B; ++c) {
             const int other = s_partial[c];
-            before += (other > mine) || (other == mine && other != 0 && c < b);
+            before += (other > mine) || (other == mine && c < b);
         }
-        const int S = splits[i];
-        const int row_start = p.row_start[b];
+        const int S = (s_pages[b] + C - 1) / C;
+        const int row_start = s_start[b];
         for (int kvh = 0; kvh < Hkv; ++kvh)
             p.order[total_full + before * Hkv + kvh] = row_start + kvh * S + (S - 1);
     }
