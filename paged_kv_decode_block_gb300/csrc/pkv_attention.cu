@@ -1082,65 +1082,70 @@ __device__ void run_tile(Smem<D, G>& sm, const AttnParams& p, TileWork tw, uint3
         const int last_page = (tw.t_stream + ps - 1) / ps;   // exclusive
         const int32_t* bt_row = p.block_table + static_cast<size_t>(tw.b) * p.max_pages;
         const uint64_t policy = l2_evict_first_policy();
-        int j = 0;   // block index within the tile
+        const int bpp = ps / kBlockRows;   // blocks per page (page sizes are multiples of 16)
         int next_id = first_page + lane < last_page ? __ldg(bt_row + first_page + lane) : 0;
         for (int pg0 = first_page; pg0 < last_page; pg0 += 32) {
-            const int ids = next_id;
+            const int ids = next_id;   // lane l: the table entry of page pg0 + l
             const int pg_next = pg0 + 32 + lane;
             next_id = pg_next < last_page ? __ldg(bt_row + pg_next) : 0;
             const int n_here = min(32, last_page - pg0);
-            for (int i = 0; i < n_here; ++i) {
-                const int page = __shfl_sync(kFull, ids, i);
-                const int page_tok0 = (pg0 + i) * ps;
-                const int lo = max(page_tok0, tw.t0);
-                const int hi = min(page_tok0 + ps, tw.t_stream);
-                const bool page_ok = page >= 0 && page < p.num_pages;
-                for (int tok = lo; tok < hi; tok += kBlockRows, ++j) {
-                    if (j % kProducerWarps != pw) continue;
-                    const uint32_t it = pipe + j;
-                    const int s = it % kStages;
-                    const uint32_t use = it / kStages;
-                    int go = 0;
-                    if (lane == 0) {
-                        go = !sm.abort;
-                        if (go && use > 0) go = mbar_wait(&sm.empty[s], (use - 1) & 1u, status, &sm.abort);
-                        if (!page_ok) atomicOr(status, static_cast<uint32_t>(PKV_DEV_PAGE_OOB));
-                        go = go && page_ok;
-                        sm.bad[s] = !go;
-                        if (go) sm.issued[s] = use + 1;
-                        if (p.copy_lsu)
-                            mbar_arrive(&sm.full[s]);   // publishes bad[s]; the lanes' copies arrive below
-                        else if (go)
-                            mbar_arrive_expect_tx(&sm.full[s], C::kStageBytes);
-                        else
-                            mbar_arrive(&sm.full[s]);
-                    }
-                    go = __shfl_sync(kFull, go, 0);
-                    const int grow = page * ps + (tok - page_tok0);   // token row inside the pool
-                    if (p.copy_lsu) {
-                        // every lane moves D/16 16-byte chunks of K and as many of V
-                        // into the swizzled stage, then arrives when they have landed
-                        if (go) {
-                            const size_t row0 = (static_cast<size_t>(grow) * p.Hkv + tw.kvh) * D;
-                            const size_t pitch = static_cast<size_t>(p.Hkv) * D;
-                            const uint32_t ks = smem_addr(sm.k[s]), vs = smem_addr(sm.v[s]);
+            // Every lane checks its own entry once, and a batch with an entry outside
+            // the pool is reported once; a block of such a page is not copied.
+            if (__any_sync(kFull, lane < n_here && (ids < 0 || ids >= p.num_pages)) && lane == 0)
+                atomicOr(status, static_cast<uint32_t>(PKV_DEV_PAGE_OOB));
+            const int jb0 = (pg0 - first_page) * bpp;                     // the batch's blocks: [jb0, jb1)
+            const int jb1 = min(nblk, (pg0 + n_here - first_page) * bpp);
+            // this warp's blocks are j = pw (mod kProducerWarps)
+            int j = jb0 + (pw - jb0 % kProducerWarps + kProducerWarps) % kProducerWarps;
+            for (; j < jb1; j += kProducerWarps) {
+                // the page's lane in the batch (one block per page for 16-token pages)
+                const int pi = bpp == 1 ? j - jb0 : j / bpp - (pg0 - first_page);
+                const int page = __shfl_sync(kFull, ids, pi);
+                const int tok = tw.t0 + j * kBlockRows;
+                const int page_tok0 = (pg0 + pi) * ps;
+                const bool page_ok = (page >= 0) & (page < p.num_pages);
+                const uint32_t it = pipe + j;
+                const int s = it % kStages;
+                const uint32_t use = it / kStages;
+                int go = 0;
+                if (lane == 0) {
+                    go = !sm.abort;
+                    if (go && use > 0) go = mbar_wait(&sm.empty[s], (use - 1) & 1u, status, &sm.abort);
+                    go &= page_ok;
+                    sm.bad[s] = !go;
+                    if (go) sm.issued[s] = use + 1;
+                    if (p.copy_lsu)
+                        mbar_arrive(&sm.full[s]);   // publishes bad[s]; the lanes' copies arrive below
+                    else if (go)
+                        mbar_arrive_expect_tx(&sm.full[s], C::kStageBytes);
+                    else
+                        mbar_arrive(&sm.full[s]);
+                }
+                go = __shfl_sync(kFull, go, 0);
+                const int grow = page * ps + (tok - page_tok0);   // token row inside the pool
+                if (p.copy_lsu) {
+                    // every lane moves D/16 16-byte chunks of K and as many of V
+                    // into the swizzled stage, then arrives when they have landed
+                    if (go) {
+                        const size_t row0 = (static_cast<size_t>(grow) * p.Hkv + tw.kvh) * D;
+                        const size_t pitch = static_cast<size_t>(p.Hkv) * D;
+                        const uint32_t ks = smem_addr(sm.k[s]), vs = smem_addr(sm.v[s]);
 #pragma unroll
-                            for (int i = 0; i < kBlockRows * (D / 8) / 32; ++i) {
-                                const int q = lane + 32 * i;
-                                const int r = q / (D / 8), c = (q % (D / 8)) * 8;
-                                const size_t off = row0 + r * pitch + c;
-                                cp_async16(ks + swz(r, c), p.k_pages + off, policy);
-                                cp_async16(vs + swz(r, c), p.v_pages + off, policy);
-                            }
+                        for (int i = 0; i < kBlockRows * (D / 8) / 32; ++i) {
+                            const int q = lane + 32 * i;
+                            const int r = q / (D / 8), c = (q % (D / 8)) * 8;
+                            const size_t off = row0 + r * pitch + c;
+                            cp_async16(ks + swz(r, c), p.k_pages + off, policy);
+                            cp_async16(vs + swz(r, c), p.v_pages + off, policy);
                         }
-                        cp_async_arrive_noinc(&sm.full[s]);
-                    } else if (go && lane < 2 * (D / 64)) {
-                        // the block's D/64 K boxes and D/64 V boxes, after lane 0 armed the barrier
-                        const int h = lane % (D / 64);
-                        const bool is_v = lane >= D / 64;
-                        tma_load_3d((is_v ? sm.v[s] : sm.k[s]) + h * (kBlockRows * 128), is_v ? vmap : kmap, h * 64,
-                                    tw.kvh, grow, &sm.full[s], policy);
                     }
+                    cp_async_arrive_noinc(&sm.full[s]);
+                } else if (go && lane < 2 * (D / 64)) {
+                    // the block's D/64 K boxes and D/64 V boxes, after lane 0 armed the barrier
+                    const int h = lane % (D / 64);
+                    const bool is_v = lane >= D / 64;
+                    tma_load_3d((is_v ? sm.v[s] : sm.k[s]) + h * (kBlockRows * 128), is_v ? vmap : kmap, h * 64,
+                                tw.kvh, grow, &sm.full[s], policy);
                 }
             }
         }
