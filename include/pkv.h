@@ -133,7 +133,8 @@ enum pkv_merge {
 
 /* How the producer warp moves K/V blocks into shared memory. */
 enum pkv_copy {
-    PKV_COPY_AUTO = 0,   /* cp.async */
+    PKV_COPY_AUTO = 0,   /* TMA on the direct, split-queue and padded routes; cp.async on the
+                            persistent route (the faster of the two on each, as measured) */
     PKV_COPY_LSU = 1,    /* cp.async 16-byte copies issued by all 32 producer lanes */
     PKV_COPY_TMA = 2     /* cp.async.bulk.tensor boxes of 16 tokens x 64 elements */
 };

@@ -719,7 +719,9 @@ int prepare_decode(pkv_plan_t p, const void* q, const void* k_pages, const void*
     a.fused_merge = p->opts.separate_merge ? 0 : 1;
     a.all_merge = pl.merge == PKV_MERGE_ALL ? 1 : 0;
     a.use_mma = p->opts.math != PKV_MATH_FMA;
-    a.copy_lsu = p->opts.copy != PKV_COPY_TMA;
+    // AUTO: TMA boxes on the one-tile-per-CTA routes, cp.async on the persistent
+    // route (each measured faster there)
+    a.copy_lsu = p->opts.copy == PKV_COPY_LSU || (p->opts.copy == PKV_COPY_AUTO && pl.mode == PKV_MODE_PERSISTENT);
     a.queue_host_staged = dp || src == PlanSource::kKernelCopied ? 0 : 1;
     a.no_empty_rows = !dp && !pl.any_empty_row ? 1 : 0;
     a.k_pages = static_cast<const uint16_t*>(k_pages);
