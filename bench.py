@@ -562,7 +562,7 @@ def decode_line(name, args, ctx, headline=True):
         "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16 in, fp32 accumulate", "data": "synthetic (seeded, bf16 ~N(0,1))",
         "config": {**workload_config(p, name, world),
-                   "mode": info["mode_name"], "math": args.math, "copy": args.copy,
+                   "mode": info["mode_name"], "math": args.math, "copy": info["copy_name"],
                    "merge": info["merge_name"],
                    "num_splits": info["max_splits"],
                    "chunk_pages": info["chunk_pages"], "tiles": info["num_work_items"],
@@ -807,7 +807,7 @@ def continuous_line(args, ctx, steps=None, warmup=None, headline=True):
         "dtype": "bf16 in, fp32 accumulate", "data": "synthetic (seeded, bf16 ~N(0,1))",
         "config": {"workload": p.name, "sessions": p.B, "seq_lens": "U[1024, 8192] + appended",
                    "q_heads": p.Hq, "kv_heads": p.Hkv, "head_dim": p.D, "page_size": p.page_size,
-                   "num_pages": p.num_pages, "mode": info["mode_name"], "math": args.math, "copy": args.copy,
+                   "num_pages": p.num_pages, "mode": info["mode_name"], "math": args.math, "copy": info["copy_name"],
                    "num_splits": info["max_splits"], "tiles": info["num_work_items"],
                    "grid_ctas": info["grid_ctas"], "launches_per_step": launches,
                    "l2": "not flushed: each step reads ~1 GB of KV, far above L2", "step": step_words},
@@ -931,7 +931,7 @@ def run_resident(args):
         "config": {"workload": p.name, "sessions": p.B, "seq_lens": "U[1024, 8192] + appended",
                    "q_heads": p.Hq, "kv_heads": p.Hkv, "head_dim": p.D, "page_size": p.page_size,
                    "num_pages": p.num_pages, "mode": "resident (one cooperative launch for all steps)",
-                   "math": args.math, "copy": args.copy, "num_splits": splits,
+                   "math": args.math, "copy": info["copy_name"], "num_splits": splits,
                    "l2": "not flushed: each step reads ~1 GB of KV, far above L2",
                    "step": "device plan + append + persistent decode inside one resident kernel, grid barriers "
                            "between them; the host publishes each step through mapped pinned memory"},

@@ -166,6 +166,7 @@ typedef struct {
     int64_t kv_bytes;           /* sum_b N_b * Hkv * D * 2 (K and V) * 2 B */
     int64_t workspace_bytes;    /* split partial states written + read per step */
     int64_t table_bytes;        /* block-table entries read per step */
+    int32_t copy;               /* the resolved pkv_copy: PKV_COPY_LSU or PKV_COPY_TMA */
 } pkv_plan_info;
 
 typedef struct pkv_plan_s *pkv_plan_t;

@@ -290,7 +290,15 @@ int compute_plan(const pkv_geom& g, int32_t ps, const int32_t* lens, const Optio
 
 int32_t launches_of(const Plan& p) { return (p.grid > 0 ? 1 : 0) + (p.need_merge ? 1 : 0); }
 
-void fill_info(const Plan& p, const pkv_geom& g, int num_sms, pkv_plan_info* info) {
+// How K/V reach shared memory for a plan: AUTO takes TMA boxes on the
+// one-tile-per-CTA routes and cp.async on the persistent route (each measured
+// faster there).
+int32_t resolved_copy(const Options& o, int32_t mode) {
+    if (o.copy != PKV_COPY_AUTO) return o.copy;
+    return mode == PKV_MODE_PERSISTENT ? PKV_COPY_LSU : PKV_COPY_TMA;
+}
+
+void fill_info(const Plan& p, const pkv_geom& g, int num_sms, const Options& o, pkv_plan_info* info) {
     memset(info, 0, sizeof(*info));
     info->mode = p.mode;
     info->chunk_pages = p.chunk;
@@ -306,6 +314,7 @@ void fill_info(const Plan& p, const pkv_geom& g, int num_sms, pkv_plan_info* inf
     info->kv_bytes = p.kv_bytes;
     info->workspace_bytes = p.ws_bytes;
     info->table_bytes = p.table_bytes;
+    info->copy = resolved_copy(o, p.mode);
 }
 
 // ------------------------------------------------------------------ TMA descriptors
@@ -524,7 +533,7 @@ int pkv_plan_dry_run(const int32_t* seq_lens_h, const int32_t* block_table_h, in
     if ((rc = compute_plan(*geom, page_size, seq_lens_h, o, o.num_sms, std::max(1, o.ctas_per_sm),
                            static_cast<int64_t>(o.num_sms) * std::max(1, o.ctas_per_sm), &pl)))
         return rc;
-    if (info) fill_info(pl, *geom, o.num_sms, info);
+    if (info) fill_info(pl, *geom, o.num_sms, o, info);
     const int32_t n = static_cast<int32_t>(pl.items.size());
     if (count) *count = n;
     if (items && capacity > 0) memcpy(items, pl.items.data(), sizeof(pkv_work_item) * std::min(n, capacity));
@@ -611,7 +620,7 @@ void pkv_plan_destroy(pkv_plan_t p) { release(p); }
 
 int pkv_plan_get_info(pkv_plan_t p, pkv_plan_info* info) {
     if (!p || !info) return PKV_EINVAL;
-    fill_info(p->plan, p->g, p->num_sms, info);
+    fill_info(p->plan, p->g, p->num_sms, p->opts, info);
     return PKV_OK;
 }
 
@@ -719,9 +728,7 @@ int prepare_decode(pkv_plan_t p, const void* q, const void* k_pages, const void*
     a.fused_merge = p->opts.separate_merge ? 0 : 1;
     a.all_merge = pl.merge == PKV_MERGE_ALL ? 1 : 0;
     a.use_mma = p->opts.math != PKV_MATH_FMA;
-    // AUTO: TMA boxes on the one-tile-per-CTA routes, cp.async on the persistent
-    // route (each measured faster there)
-    a.copy_lsu = p->opts.copy == PKV_COPY_LSU || (p->opts.copy == PKV_COPY_AUTO && pl.mode == PKV_MODE_PERSISTENT);
+    a.copy_lsu = resolved_copy(p->opts, pl.mode) == PKV_COPY_LSU ? 1 : 0;
     a.queue_host_staged = dp || src == PlanSource::kKernelCopied ? 0 : 1;
     a.no_empty_rows = !dp && !pl.any_empty_row ? 1 : 0;
     a.k_pages = static_cast<const uint16_t*>(k_pages);

@@ -21,6 +21,7 @@ MODE_NAMES = {MODE_AUTO: "auto", MODE_DIRECT: "direct", MODE_SPLIT_QUEUE: "split
 MODES = {v: k for k, v in MODE_NAMES.items()}
 MATH = {"auto": 0, "fma": 1, "mma": 2}
 COPY = {"auto": 0, "lsu": 1, "tma": 2}
+COPY_NAMES = {v: k for k, v in COPY.items()}
 MERGE = {"auto": 0, "last": 1, "all": 2}
 MERGE_NAMES = {0: "none", 1: "last", 2: "all", 3: "separate"}
 
@@ -58,12 +59,13 @@ class PlanInfo(ctypes.Structure):
                 ("launches_per_step", ctypes.c_int32), ("grid_ctas", ctypes.c_int32),
                 ("num_sms", ctypes.c_int32), ("merge", ctypes.c_int32),
                 ("kv_bytes", ctypes.c_int64), ("workspace_bytes", ctypes.c_int64),
-                ("table_bytes", ctypes.c_int64)]
+                ("table_bytes", ctypes.c_int64), ("copy", ctypes.c_int32)]
 
     def as_dict(self) -> dict:
         d = {name: getattr(self, name) for name, _ in self._fields_}
         d["mode_name"] = MODE_NAMES.get(self.mode, "?")
         d["merge_name"] = MERGE_NAMES.get(self.merge, "?")
+        d["copy_name"] = COPY_NAMES.get(self.copy, "?")
         return d
 
 

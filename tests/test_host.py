@@ -128,6 +128,40 @@ def test_workload_policies():
     assert info["grid_ctas"] == min(len(q), 2 * NUM_SMS)
 
 
+def test_copy_engine_resolution():
+    """copy=auto takes TMA boxes on the one-tile-per-CTA routes and cp.async on the
+    persistent route; an explicit choice is kept."""
+    b1 = _geom_problem([32768], Hq=32, Hkv=8, D=128)
+    for route, want in (("split_queue", "tma"), ("split_padded", "tma"), ("direct", "tma"), ("persistent", "lsu")):
+        info, _ = _dry(b1, force_mode=route, num_splits=32, ctas_per_sm=2)
+        assert (info["mode_name"], info["copy_name"]) == (route, want)
+        for forced in ("lsu", "tma"):
+            info, _ = _dry(b1, force_mode=route, num_splits=32, ctas_per_sm=2, copy=forced)
+            assert info["copy_name"] == forced
+
+
+def test_plan_info_layout_matches_the_header():
+    """The binding's pkv_plan_info is the header's struct: its size is checked by a dry
+    run writing a full struct, with a guard word past the end left alone."""
+    import ctypes
+    b1 = _geom_problem([4096], Hq=32, Hkv=8, D=128)
+    lib = pkv.load()
+    lens = np.ascontiguousarray(b1.seq_lens, np.int32)
+
+    class Guarded(ctypes.Structure):
+        _fields_ = [("info", pkv.PlanInfo), ("guard", ctypes.c_uint64)]
+
+    g = Guarded()
+    g.guard = 0x0123456789ABCDEF
+    n = ctypes.c_int32(0)
+    geom = pkv._geom(b1.B, b1.Hq, b1.Hkv, b1.D, b1.max_pages, b1.num_pages)
+    opts = pkv._opts(num_sms=NUM_SMS)
+    rc = lib.pkv_plan_dry_run(lens.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)), None, 16, ctypes.byref(geom),
+                              ctypes.byref(opts), ctypes.byref(g.info), None, 0, ctypes.byref(n))
+    assert rc == 0 and g.guard == 0x0123456789ABCDEF
+    assert g.info.copy in (pkv.COPY["lsu"], pkv.COPY["tma"]) and g.info.kv_bytes == 4096 * 8 * 128 * 4
+
+
 def test_splits_are_capped_by_the_merge_scratch():
     p = _geom_problem([4096 * 16], Hq=8, Hkv=1, D=64)   # G = 8: at most 4096 / 8 splits
     info, q = _dry(p, force_mode="split_queue", num_splits=5000)
