@@ -107,7 +107,8 @@ typedef struct {
 typedef struct {
     int32_t force_mode;          /* pkv_mode; PKV_MODE_AUTO lets the policy choose */
     int32_t num_splits;          /* > 0: split count S, chunk C = ceil(P_max / S) pages */
-    int32_t direct_units_per_sm; /* policy: DIRECT when B*Hkv >= this * SMs (default 2) */
+    int32_t direct_units_per_sm; /* policy: DIRECT when B*Hkv >= this * SMs (default 2); smaller
+                                    batches take SPLIT_QUEUE, one split per row if rows are short */
     int32_t target_ctas_per_sm;  /* policy: aim for this many tiles per SM (default 2) */
     int32_t min_chunk_pages;     /* policy: smallest split chunk in pages (default 8) */
     int32_t ctas_per_sm;         /* persistent grid = SMs * this (default: occupancy) */

@@ -90,8 +90,10 @@ def test_planner_queue_bit_exact_against_oracle_enumeration(seed, mode):
 
 def test_workload_policies():
     tiny = wl.tiny()
-    info, _ = _dry(tiny)
-    assert info["mode_name"] == "direct"                     # 7 pages fit one chunk
+    info, q = _dry(tiny)
+    # 7 pages fit one chunk: one queue tile per row, finalised in place
+    assert (info["mode_name"], info["chunk_pages"], info["max_splits"]) == ("split_queue", 8, 1)
+    assert np.array_equal(q, oracle.enumerate_queue(tiny.seq_lens, 16, 1, 8))
     for S, C in [(1, 7), (2, 4), (4, 2)]:
         info, q = _dry(tiny, force_mode="split_queue", num_splits=S)
         assert info["chunk_pages"] == C
